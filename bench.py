@@ -1,0 +1,395 @@
+"""Benchmark of the KDA decode / spec-verify step on GB300.
+
+One step = one kda_step over one batch of the workload (default: large
+decode, B = 512 rows x 12 heads x 128, conv width 4, a 1024-slot pool;
+805 MB of fp32 state read and written per step, larger than L2).
+
+Prints ONE JSON line:
+  value      tokens/s with every input resident in HBM (CUDA events on the
+             launching stream, around exactly --steps steps)
+  e2e        the same metric through the public API with host buffers:
+             each step copies its projected rows, slots (and accepted) from
+             pinned host memory and reads `out` back
+  roofline   the step kernel's algorithmic bytes / its average launch time
+             against the measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle (plain fp64 C, 1 thread) on a bounded sample
+             of the same workload
+  clocks     nvidia-smi samples taken during the timed region
+
+`--impl reference` times the CPU oracle as the reference arm instead.
+With torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step); value = all ranks' tokens / the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from linear_attention_decode_03_gb300 import inputs as I  # noqa: E402
+
+METRIC = "KDA tokens/s and achieved HBM GB/s (state R+W) vs GB300 peak, 1 GPU"
+L2_BYTES = 129 * 1024 * 1024
+HEAD_DIM = 128
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) with host timestamps."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        used = inside
+        if not used:  # region shorter than the sampling period: nearest samples after its start
+            used = [s for t, s in self.samples if t >= t0][:2]
+        sm = [float(s[0]) for s in used if s[0].replace(".", "").isdigit()]
+        smax = [float(s[1]) for s in used if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in used for n, v in zip(names, s[4:8]) if v.lower() == "active"})
+        power = [float(s[2]) for s in used if s[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(used), "samples_in_region": len(inside),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------ device setup
+class DeviceWorkload:
+    """One workload's inputs resident on the device (pools sentinel-filled,
+    read slots filled from the seeded generator)."""
+
+    def __init__(self, si: I.StepInputs, device):
+        import torch
+        import linear_attention_decode_03_gb300 as kda
+
+        self.si, self.w = si, si.workload
+        w = self.w
+        self.device = device
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+        wt = si.weights
+        self.prep = kda.PreparedKda(bf16(wt.conv_w), None if wt.bias is None else bf16(wt.bias), bf16(wt.f_b),
+                                    torch.from_numpy(wt.A_log).to(device), torch.from_numpy(wt.dt_bias).to(device),
+                                    torch.from_numpy(wt.o_norm).to(device), gate_lower_bound=wt.gate_lower_bound,
+                                    eps=wt.eps, conv_dim_first=True)
+        self.projected = bf16(si.projected)
+        self.state = torch.empty((w.pool, w.heads, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=device)
+        self.state.view(torch.int32).fill_(int(I.STATE_SENTINEL.view(np.int32)))
+        idx = torch.from_numpy(si.read_slots).to(device)
+        self.state[idx] = torch.from_numpy(si.states).to(device)
+        self.conv = torch.empty((w.pool, 3 * w.dim, w.width - 1), dtype=torch.bfloat16, device=device)
+        self.conv.view(torch.int16).fill_(int(np.array(I.CONV_SENTINEL).view(np.int16)))
+        self.conv[idx] = bf16(si.windows)
+        self.slots = torch.from_numpy(si.slots.copy()).to(device)
+        if w.verify:
+            self.slots = self.slots.view(w.requests, w.L)
+        self.accepted = None if si.accepted is None else torch.from_numpy(si.accepted.copy()).to(device)
+        self.out = torch.empty((w.rows, w.dim), dtype=torch.bfloat16, device=device)
+
+    def step(self):
+        self.prep.run(self.projected, self.out, caches=(self.conv, self.state), slots=self.slots,
+                      accepted=self.accepted)
+
+
+def algorithmic_bytes(w: I.Workload):
+    return w.state_bytes, w.state_bytes + w.other_bytes
+
+
+# ----------------------------------------------------------- CPU oracle arm
+def oracle_sample_inputs(si: I.StepInputs, reqs):
+    """Inputs of requests `reqs` with the pools compacted to the slots they touch."""
+    w = si.workload
+    L = w.L
+    slots2 = si.slots.reshape(w.requests, L)[reqs]
+    used = np.unique(slots2)
+    pos = {int(s): i for i, s in enumerate(used)}
+    read_pos = {int(s): i for i, s in enumerate(si.read_slots)}
+    cpool = np.empty((len(used), w.heads, HEAD_DIM, HEAD_DIM), dtype=np.float32)
+    cpool.view(np.uint32)[...] = I.STATE_SENTINEL
+    cconv = np.full((len(used), 3 * w.dim, w.width - 1), I.CONV_SENTINEL, dtype=np.uint16)
+    for s, i in pos.items():
+        if s in read_pos:
+            cpool[i] = si.states[read_pos[s]]
+            cconv[i] = si.windows[read_pos[s]]
+    cslots = np.array([pos[int(s)] for s in slots2.reshape(-1)], dtype=np.int32)
+    rows = (np.asarray(reqs)[:, None] * L + np.arange(L)[None, :]).reshape(-1)
+    acc = None if si.accepted is None else si.accepted[reqs]
+    return si.projected[rows], cconv, cpool, cslots, acc
+
+
+def time_oracle(si: I.StepInputs, n_requests: int, repeats: int = 1):
+    """Seconds per token of the C oracle over `n_requests` requests (1 thread)."""
+    import oracle
+
+    W = oracle.Weights(**si.weights.as_dict())
+    reqs = np.arange(min(n_requests, si.workload.requests))
+    proj, cconv, cpool, cslots, acc = oracle_sample_inputs(si, reqs)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.step(W, proj, cconv, cpool, cslots, si.workload.L, acc)
+    dt = time.perf_counter() - t0
+    return dt, len(reqs) * si.workload.L * repeats
+
+
+def cpu_baseline(si: I.StepInputs, budget_s: float = 12.0):
+    """The oracle on a bounded sample: as many whole requests (in order) as fit
+    in about `budget_s` seconds, estimated from one request."""
+    dt1, tok1 = time_oracle(si, 1)
+    n = int(max(1, min(si.workload.requests, budget_s / max(dt1, 1e-6))))
+    dt, tok = time_oracle(si, n)
+    return {"value": tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} of {si.workload.requests} requests ({tok} tokens x {si.workload.heads} heads) "
+                      f"of the {si.workload.name} workload, fp64 C oracle, 1 thread, {dt:.1f} s"}
+
+
+def run_reference(args, w: I.Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    si = I.make_step_inputs(w)
+    dt1, _ = time_oracle(si, 1)
+    per_step_budget = 150.0 / max(args.steps + args.warmup, 1)
+    n = int(max(1, min(w.requests, per_step_budget / max(dt1, 1e-6))))
+    for _ in range(args.warmup):
+        time_oracle(si, n)
+    total_t, total_tok = 0.0, 0
+    for _ in range(args.steps):
+        dt, tok = time_oracle(si, n)
+        total_t += dt
+        total_tok += tok
+    value = total_tok / total_t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, args),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: first {n} of {w.requests} requests of {w.name} "
+                                   f"({n * w.L} tokens x {w.heads} heads), fp64 C oracle, 1 thread"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w: I.Workload, args):
+    state, allb = algorithmic_bytes(w)
+    big = state > L2_BYTES
+    return {"workload": w.name, "heads": w.heads, "head_dim": HEAD_DIM, "requests": w.requests, "tokens_per_request": w.L,
+            "rows": w.rows, "pool_slots": w.pool, "conv_width": w.width, "state_bytes_per_step": state,
+            "algorithmic_bytes_per_step": allb,
+            "l2": ("inputs larger than L2 (%.0f MB of state per step)" % (state / 1e6)) if big
+            else "L2 flushed between timed steps (256 MiB write, outside the per-step events)",
+            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+
+
+# -------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
+    ap.add_argument("--workload", default="large_decode", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = I.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import linear_attention_decode_03_gb300 as kda
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    kda.build()
+    kda.load_library()
+
+    si = I.make_step_inputs(w)
+    dw = DeviceWorkload(si, device)
+    state_b, all_b = algorithmic_bytes(w)
+    flush = state_b <= L2_BYTES
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device) if flush else None
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        dw.step()
+    if dw.prep.check() != 0:
+        raise RuntimeError("device error bits set during warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    t_host0 = time.time()
+    if flush:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            scratch.fill_(float(i))
+            starts[i].record(stream)
+            dw.step()
+            ends[i].record(stream)
+        barrier()
+        elapsed_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    else:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            dw.step()
+        ev1.record(stream)
+        barrier()
+        elapsed_ms = ev0.elapsed_time(ev1)
+    t_host1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    flags = dw.prep.check()
+    if flags != 0:
+        raise RuntimeError(f"device error bits {flags} during the timed steps")
+
+    # e2e through the public API with host buffers (pinned), copies inside the region
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 500))
+    h_proj = torch.from_numpy(np.ascontiguousarray(si.projected).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_slots = torch.from_numpy(si.slots.copy()).pin_memory()
+    h_acc = None if si.accepted is None else torch.from_numpy(si.accepted.copy()).pin_memory()
+    h_out = torch.empty((w.rows, w.dim), dtype=torch.bfloat16).pin_memory()
+    d_proj = torch.empty_like(dw.projected)
+    d_slots = torch.empty_like(dw.slots)
+    d_acc = None if h_acc is None else torch.empty_like(dw.accepted)
+    h2d = h_proj.numel() * 2 + h_slots.numel() * 4 + (0 if h_acc is None else h_acc.numel() * 4)
+    d2h = h_out.numel() * 2
+
+    def e2e_step():
+        d_proj.copy_(h_proj, non_blocking=True)
+        d_slots.view(-1).copy_(h_slots, non_blocking=True)
+        if d_acc is not None:
+            d_acc.copy_(h_acc, non_blocking=True)
+        dw.prep.run(d_proj, dw.out, caches=(dw.conv, dw.state), slots=d_slots, accepted=d_acc)
+        h_out.copy_(dw.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if dw.prep.check() != 0:
+        raise RuntimeError("device error bits set during the e2e steps")
+
+    # max over ranks
+    if dist is not None:
+        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    ms_step = elapsed_ms / args.steps
+    tokens_per_s = world * w.rows * args.steps / (elapsed_ms / 1e3)
+    peak, peak_kind = load_peaks()
+    achieved = all_b / (ms_step / 1e3) / 1e9
+    state_gbs = state_b / (ms_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload_config(w, args),
+        "state_gbs": state_gbs, "state_frac_of_peak": state_gbs / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "kda_step_kernel",
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": {"value": world * w.rows * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(t_host0, t_host1),
+    }
+    if dist is not None:
+        dist.destroy_process_group()
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(si)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

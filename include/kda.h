@@ -1,0 +1,147 @@
+/*
+ * kda.h -- C ABI of libkda.so: the Kimi Delta Attention (KDA) decode and
+ * spec-verify core of a Kimi-K3 layer on one GB300 GPU (sm_103a).
+ *
+ * One step runs, for every request r and head h, from the packed bf16
+ * projection row to the gated-RMSNorm bf16 core output:
+ *   1. split the row into q|k|v | out-gate | f_a | beta
+ *      ("...cutedsl.kda.prepared" page, PreparedKda._operands);
+ *   2. causal depthwise short conv of the q/k/v channels against the slot's
+ *      conv window, SiLU, bf16 ("...mono.attention.kda" page, K1 docstring,
+ *      kda_conv);
+ *   3. z = f_b . f_a (bf16), g = lb * sigmoid(exp(A_log[h]) * (z + dt_bias)),
+ *      beta = sigmoid(beta_logit) (K1 docstring, kda_gates: "f_b MFMA +
+ *      lower-bound gate");
+ *   4. q^ = q / |q| * 128^-0.5, k^ = k / |k| (l2norm, eps 1e-6 inside the root);
+ *   5. gated delta rule on the 128 x 128 fp32 state:
+ *      S <- diag(e^g) S;  S <- S + beta k^ (v - S^T k^)^T;  o = S^T q^
+ *      (K1 docstring, kda_recur: "a state a token written");
+ *   6. gated RMSNorm of bf16 o with the fp32 o_norm weight times
+ *      sigmoid(out-gate) -> bf16 core_out (K1 docstring, kda_norm;
+ *      PreparedKda.__init__: fp32 norm weight, eps = o_norm.eps).
+ *
+ * Layouts (D = 128 H, C = 3 D conv channels, W = conv width, SL = W - 1):
+ *   projected   bf16 [rows, pitch], pitch >= 4D + 128 + H elements:
+ *               cols [0,3D) q|k|v, [3D,4D) out-gate, [4D,4D+128) f_a,
+ *               [4D+128, 4D+128+H) beta logits.
+ *   conv_state  bf16 [pool, C, SL] (conv_dim_first = 1) or [pool, SL, C];
+ *               each window holds the last SL inputs, oldest first.
+ *   state_pool  fp32 [pool, H, 128 (v), 128 (k)]: one contiguous 64 KiB block
+ *               per (slot, head), k contiguous within a 512-byte v row.
+ *   out         bf16 [rows, D].
+ * Decode: L = 1, accepted = NULL, row b reads and writes slot slots[b].
+ * Verify: rows = R L request-major (row = r L + t), slots [R, L] contiguous,
+ *   accepted [R] in 1..L; request r starts from slot slots[r, accepted[r]-1]
+ *   and after token t stores its state and conv window into slots[r, t]
+ *   (PreparedKda.run: rows = batch // tokens, accepted[:rows]).
+ * A slot of -1 in slots[r, 0] marks a padding request: no cache is read or
+ *   written and its out rows are zero.  Duplicate slots within one step are
+ *   undefined behaviour.
+ *
+ * All pointers passed to kda_step are DEVICE pointers on the device that was
+ * current when the handle was prepared; the caller keeps ownership of every
+ * buffer and keeps it alive until the step has completed on its stream.
+ *
+ * Thread safety: one handle may be used from one host thread at a time.
+ * Steps enqueued on different streams against the same caches race.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kda_handle kda_handle;
+
+/* Return codes. */
+#define KDA_OK 0
+#define KDA_EINVAL (-1) /* an argument is invalid; nothing was enqueued   */
+#define KDA_ECUDA (-2)  /* a CUDA call or a launch failed                 */
+
+/* Device error bits, accumulated in the handle's device error word and
+ * returned (then cleared) by kda_check. */
+#define KDA_ERR_SLOT 1u     /* a slot outside [0, pool) other than a padding -1: request skipped */
+#define KDA_ERR_ACCEPTED 2u /* accepted[r] outside 1..L: request skipped                         */
+#define KDA_ERR_TIMEOUT 4u  /* a bounded wait for a state tile gave up: that tile is not written  */
+
+/* Maximum verify tokens per request. */
+#define KDA_MAX_TOKENS 8
+
+/*
+ * kda_prepare -- copy the layer's weights into handle-owned device buffers,
+ * re-laying out the conv weight [3D, 1, W] into [3, W, D] (q, k, v blocks,
+ * taps outer, channel contiguous), as PreparedKda.__init__ /
+ * decode_conv_weight do ("...cutedsl.kda.prepared" page).
+ *
+ *   heads             H >= 1 (D = 128 H)
+ *   conv_width        W in 2..4
+ *   conv_w            device bf16 [3D, 1, W]
+ *   bias              device bf16 [3D], or NULL for no conv bias
+ *   f_b               device bf16 [D, 128]
+ *   A_log             device fp32 [H]
+ *   dt_bias           device fp32 [D]
+ *   o_norm            device fp32 [128] (shared by all heads)
+ *   gate_lower_bound  lb < 0 of the gate (the model's gate_lower_bound)
+ *   eps               o_norm epsilon (> 0)
+ *   out               receives the handle
+ *
+ * Synchronous on the device that is current.  The source buffers may be
+ * freed once it returns.  Returns KDA_OK, KDA_EINVAL (NULL pointer, heads < 1,
+ * W outside 2..4, eps <= 0, a misaligned pointer) or KDA_ECUDA.
+ */
+int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias, const void* f_b,
+                const float* A_log, const float* dt_bias, const float* o_norm,
+                float gate_lower_bound, float eps, kda_handle** out);
+
+/*
+ * kda_step -- enqueue one decode or verify step on `cuda_stream` (a
+ * cudaStream_t; NULL = the legacy default stream) without a host sync.
+ *
+ *   projected       device bf16 [rows, pitch]                 (read)
+ *   rows, pitch     rows >= 0, a multiple of L; pitch >= 4D + 128 + H
+ *   conv_state      device bf16 windows, see layouts          (read + written)
+ *   conv_dim_first  1: [pool, 3D, W-1]; 0: [pool, W-1, 3D]
+ *   state_pool      device fp32 [pool, H, 128, 128], 16-byte aligned (read + written)
+ *   pool_slots      pool size (slots)
+ *   slots           device int32 [rows]
+ *   L               1..KDA_MAX_TOKENS tokens per request
+ *   accepted        device int32 [rows / L] for verify, NULL for decode (L must be 1)
+ *   out             device bf16 [rows, D], 8-byte aligned     (written)
+ *
+ * rows = 0 enqueues nothing.  Returns KDA_OK, KDA_EINVAL (NULL handle or
+ * buffer, bad sizes, L outside 1..8, rows % L != 0, L > 1 without accepted,
+ * misalignment) or KDA_ECUDA (launch failure).  Bad slot / accepted VALUES
+ * are found on the device: they set KDA_ERR_* bits in the handle's error
+ * word and the request is skipped (nothing written for it); they never trap.
+ */
+int kda_step(kda_handle* handle, const void* projected, long long rows, long long pitch,
+             void* conv_state, int conv_dim_first, float* state_pool, long long pool_slots,
+             const int* slots, int L, const int* accepted, void* out, void* cuda_stream);
+
+/*
+ * kda_check -- synchronise `cuda_stream`, then read and clear the handle's
+ * device error word into *device_flags (may be NULL).  Returns KDA_OK,
+ * KDA_EINVAL (NULL handle) or KDA_ECUDA (the stream reported an error).
+ */
+int kda_check(kda_handle* handle, void* cuda_stream, unsigned* device_flags);
+
+/* kda_destroy -- free the handle's device buffers (synchronises the device). NULL is a no-op. */
+void kda_destroy(kda_handle* handle);
+
+/* kda_strerror -- a static string for a return code. */
+const char* kda_strerror(int code);
+
+/*
+ * kda_launch_info -- the launch shape kda_step uses for L tokens: CTAs per
+ * (request, head), threads per CTA, dynamic shared memory bytes and the
+ * resident CTAs per SM the occupancy calculator reports.  Returns KDA_OK,
+ * KDA_EINVAL or KDA_ECUDA.  Needs a current CUDA device.
+ */
+int kda_launch_info(int L, int* threads, int* smem_bytes, int* ctas_per_sm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

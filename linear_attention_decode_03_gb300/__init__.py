@@ -1,1 +1,211 @@
-"""KDA decode / spec-verify core for GB300 (placeholder; binding follows)."""
+"""KDA decode / spec-verify core on GB300 (sm_103a): thin Python binding.
+
+Every step of the path runs in the CUDA kernels of ``libkda.so`` (built
+in-tree from ``csrc/kda_step.cu``); this module only marshals arguments
+through the C ABI declared in ``include/kda.h``.  PyTorch supplies device
+memory and the current stream.  There is no fallback: if the library is
+missing or fails to load, every call raises.
+
+Low-level functions carry the C names (:func:`kda_prepare`, :func:`kda_step`,
+:func:`kda_check`, :func:`kda_destroy`, :func:`kda_strerror`,
+:func:`kda_launch_info`) and take raw device pointers.  :class:`PreparedKda`
+mirrors the PreparedKda wrapper on the
+"vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.prepared" page:
+weights prepared once, then ``run(projected, out, caches=..., slots=...,
+accepted=None)`` per step, with ``accepted[:R]`` and contiguous ``slots[:R]``
+for verify steps.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+from ._build import LIB_PATH, build
+
+__all__ = [
+    "KdaError", "build", "load_library", "kda_prepare", "kda_step", "kda_check", "kda_destroy",
+    "kda_strerror", "kda_launch_info", "PreparedKda", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
+    "KDA_ERR_TIMEOUT", "KDA_MAX_TOKENS", "HEAD_DIM",
+]
+
+HEAD_DIM = 128
+KDA_OK, KDA_EINVAL, KDA_ECUDA = 0, -1, -2
+KDA_ERR_SLOT, KDA_ERR_ACCEPTED, KDA_ERR_TIMEOUT = 1, 2, 4
+KDA_MAX_TOKENS = 8
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {kda_strerror(code)} ({code})")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with linear_attention_decode_03_gb300.build()")
+    lib = ctypes.CDLL(path)
+    vp, ll, i32, f32 = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_float
+    lib.kda_prepare.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, f32, f32, ctypes.POINTER(vp)]
+    lib.kda_prepare.restype = i32
+    lib.kda_step.argtypes = [vp, vp, ll, ll, vp, i32, vp, ll, vp, i32, vp, vp, vp]
+    lib.kda_step.restype = i32
+    lib.kda_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.kda_check.restype = i32
+    lib.kda_destroy.argtypes = [vp]
+    lib.kda_destroy.restype = None
+    lib.kda_strerror.argtypes = [i32]
+    lib.kda_strerror.restype = ctypes.c_char_p
+    lib.kda_launch_info.argtypes = [i32, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.kda_launch_info.restype = i32
+    _lib = lib
+    return lib
+
+
+def kda_strerror(code: int) -> str:
+    return load_library().kda_strerror(int(code)).decode()
+
+
+def kda_prepare(heads: int, conv_width: int, conv_w: int, bias: int, f_b: int, A_log: int, dt_bias: int,
+                o_norm: int, gate_lower_bound: float, eps: float) -> int:
+    """Device pointers in, an opaque handle (int) out."""
+    h = ctypes.c_void_p()
+    rc = load_library().kda_prepare(heads, conv_width, conv_w, bias or None, f_b, A_log, dt_bias, o_norm,
+                                    gate_lower_bound, eps, ctypes.byref(h))
+    if rc != KDA_OK:
+        raise KdaError("kda_prepare", rc)
+    return h.value
+
+
+def kda_step(handle: int, projected: int, rows: int, pitch: int, conv_state: int, conv_dim_first: bool,
+             state_pool: int, pool_slots: int, slots: int, L: int, accepted: Optional[int], out: int,
+             stream: int) -> None:
+    rc = load_library().kda_step(handle, projected, rows, pitch, conv_state, 1 if conv_dim_first else 0,
+                                 state_pool, pool_slots, slots, L, accepted or None, out, stream or None)
+    if rc != KDA_OK:
+        raise KdaError("kda_step", rc)
+
+
+def kda_check(handle: int, stream: int = 0) -> int:
+    flags = ctypes.c_uint(0)
+    rc = load_library().kda_check(handle, stream or None, ctypes.byref(flags))
+    if rc != KDA_OK:
+        raise KdaError("kda_check", rc)
+    return int(flags.value)
+
+
+def kda_destroy(handle: int) -> None:
+    if handle:
+        load_library().kda_destroy(handle)
+
+
+def kda_launch_info(L: int) -> Tuple[int, int, int]:
+    """(threads per CTA, dynamic shared bytes, resident CTAs per SM) for L tokens."""
+    t, s, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = load_library().kda_launch_info(L, ctypes.byref(t), ctypes.byref(s), ctypes.byref(c))
+    if rc != KDA_OK:
+        raise KdaError("kda_launch_info", rc)
+    return t.value, s.value, c.value
+
+
+def _dev(t, dtype, name):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class PreparedKda:
+    """Prepared KDA core for one layer (weights copied into the handle).
+
+    ``conv_w`` [3D, 1, W] bf16, ``conv_bias`` [3D] bf16 or None, ``f_b`` [D, 128]
+    bf16, ``A_log`` [H] f32, ``dt_bias`` [D] f32, ``o_norm`` [128] f32 (cast
+    to fp32 as the page's __init__ does).
+    """
+
+    def __init__(self, conv_w, conv_bias, f_b, A_log, dt_bias, o_norm, *, gate_lower_bound: float = -5.0,
+                 eps: float = 1e-6, conv_dim_first: bool = True):
+        import torch
+
+        self.heads = int(A_log.numel())
+        self.dim = self.heads * HEAD_DIM
+        self.width = int(conv_w.shape[-1])
+        self.conv_dim_first = conv_dim_first
+        o_norm = o_norm.detach().float().contiguous()
+        self._keep = [_dev(conv_w.detach().contiguous(), torch.bfloat16, "conv_w"),
+                      _dev(f_b.detach().contiguous(), torch.bfloat16, "f_b"),
+                      _dev(A_log.detach().contiguous(), torch.float32, "A_log"),
+                      _dev(dt_bias.detach().contiguous(), torch.float32, "dt_bias"),
+                      _dev(o_norm, torch.float32, "o_norm")]
+        bias_ptr = 0
+        if conv_bias is not None:
+            b = _dev(conv_bias.detach().contiguous(), torch.bfloat16, "conv_bias")
+            self._keep.append(b)
+            bias_ptr = b.data_ptr()
+        cw, fb, al, dt, on = self._keep[:5]
+        self.device = cw.device
+        with torch.cuda.device(self.device):
+            self.handle = kda_prepare(self.heads, self.width, cw.data_ptr(), bias_ptr, fb.data_ptr(),
+                                      al.data_ptr(), dt.data_ptr(), on.data_ptr(), float(gate_lower_bound),
+                                      float(eps))
+
+    def run(self, projected, out, *, caches, slots, accepted=None, stream=None):
+        """One step.  ``caches`` = (conv_state, state_pool); decode when
+        ``accepted`` is None (``slots`` [>= B]), verify otherwise (``slots``
+        [>= R, L], ``accepted`` [>= R])."""
+        import torch
+
+        conv, state = caches[:2]
+        batch = projected.shape[0]
+        L = 1
+        if accepted is not None:
+            L = int(slots.shape[1])
+            rows = batch // L
+            accepted = _dev(accepted[:rows].contiguous(), torch.int32, "accepted")
+            slots = slots[:rows]
+            if slots.stride() != (L, 1):
+                slots = slots.contiguous()
+        else:
+            slots = slots[:batch]
+        _dev(slots, torch.int32, "slots")
+        if projected.dtype != torch.bfloat16 or not projected.is_cuda or projected.stride(1) != 1:
+            raise TypeError("projected must be a CUDA bf16 tensor with unit column stride")
+        _dev(out, torch.bfloat16, "out")
+        _dev(conv, torch.bfloat16, "conv_state")
+        _dev(state, torch.float32, "state_pool")
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device).cuda_stream
+        kda_step(self.handle, projected.data_ptr(), batch, projected.stride(0), conv.data_ptr(),
+                 self.conv_dim_first, state.data_ptr(), state.shape[0], slots.data_ptr(), L,
+                 None if accepted is None else accepted.data_ptr(), out.data_ptr(), stream)
+        return out
+
+    def check(self, stream=None) -> int:
+        """Synchronise the stream; return and clear the device error bits."""
+        import torch
+
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device).cuda_stream
+        return kda_check(self.handle, stream)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            kda_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,125 @@
+"""GPU-side harness for the parity tests: put seeded inputs on the device, run
+one step through the C ABI (via the binding), and run the CPU oracle on the
+same requests with a compacted pool.
+
+Nothing here computes a step of the method: the GPU side is libkda.so, the
+reference side is the oracle package.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import linear_attention_decode_03_gb300 as kda
+from linear_attention_decode_03_gb300 import inputs as I
+
+HEAD_DIM = 128
+OUT_SENTINEL = np.uint16(0x7FDB)
+
+# Tolerances of the parity contract: bf16 outputs |gpu - oracle| <= 2e-2 +
+# 1e-2 |oracle| elementwise; fp32 state max-abs 1e-3; conv windows and every
+# index decision bit-exact.
+OUT_ATOL, OUT_RTOL, STATE_ATOL = 2e-2, 1e-2, 1e-3
+
+
+def bf16_np_to_torch(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def torch_bf16_to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_value(bits) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def prepare(weights: I.LayerWeights, device, dim_first=True) -> kda.PreparedKda:
+    return kda.PreparedKda(
+        bf16_np_to_torch(weights.conv_w, device),
+        None if weights.bias is None else bf16_np_to_torch(weights.bias, device),
+        bf16_np_to_torch(weights.f_b, device),
+        torch.from_numpy(weights.A_log).to(device),
+        torch.from_numpy(weights.dt_bias).to(device),
+        torch.from_numpy(weights.o_norm).to(device),
+        gate_lower_bound=weights.gate_lower_bound, eps=weights.eps, conv_dim_first=dim_first)
+
+
+class DeviceStep:
+    """Device copies of one step's inputs (full pools, sentinel-filled)."""
+
+    def __init__(self, si: I.StepInputs, device="cuda:0", dim_first=True, weights=None):
+        w = si.workload
+        self.si, self.w, self.dim_first = si, w, dim_first
+        self.device = torch.device(device)
+        self.prep = prepare(weights or si.weights, self.device, dim_first)
+        self.projected = bf16_np_to_torch(si.projected, self.device)
+        H, sl = w.heads, w.width - 1
+        self.state = torch.empty((w.pool, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=self.device)
+        self.state.view(torch.int32).fill_(int(I.STATE_SENTINEL.view(np.int32)))
+        if len(si.read_slots):
+            idx = torch.from_numpy(si.read_slots).to(self.device)
+            self.state[idx] = torch.from_numpy(si.states).to(self.device)
+        shape = (w.pool, 3 * w.dim, sl) if dim_first else (w.pool, sl, 3 * w.dim)
+        self.conv = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+        self.conv.view(torch.int16).fill_(int(np.array(I.CONV_SENTINEL).view(np.int16)))
+        if len(si.read_slots):
+            win = si.windows if dim_first else np.ascontiguousarray(si.windows.transpose(0, 2, 1))
+            self.conv[idx] = bf16_np_to_torch(win, self.device)
+        self.slots = torch.from_numpy(si.slots.copy()).to(self.device)
+        if w.verify:
+            self.slots = self.slots.view(w.requests, w.L)
+        self.accepted = None if si.accepted is None else torch.from_numpy(si.accepted.copy()).to(self.device)
+        self.out = torch.empty((w.rows, w.dim), dtype=torch.bfloat16, device=self.device)
+        self.out.view(torch.int16).fill_(int(np.array(OUT_SENTINEL).view(np.int16)))
+
+    def run(self) -> int:
+        self.prep.run(self.projected, self.out, caches=(self.conv, self.state), slots=self.slots,
+                      accepted=self.accepted)
+        return self.prep.check()
+
+    def close(self):
+        self.prep.close()
+
+
+def oracle_requests(si: I.StepInputs, reqs, dim_first=True):
+    """The C oracle on requests `reqs` only, with a pool compacted to the slots
+    they touch.  Returns (out rows, used slots, pool [n_used], conv [n_used], err)."""
+    w = si.workload
+    L = w.L
+    reqs = np.asarray(reqs)
+    slots2 = si.slots.reshape(w.requests, L)[reqs]
+    used = np.unique(slots2[slots2 >= 0])
+    pos = {int(s): i for i, s in enumerate(used)}
+    read_pos = {int(s): i for i, s in enumerate(si.read_slots)}
+    n = max(len(used), 1)
+    cpool = np.empty((n, w.heads, HEAD_DIM, HEAD_DIM), dtype=np.float32)
+    cpool.view(np.uint32)[...] = I.STATE_SENTINEL
+    cconv = np.full((n, 3 * w.dim, w.width - 1), I.CONV_SENTINEL, dtype=np.uint16)
+    for s, i in pos.items():
+        if s in read_pos:
+            cpool[i] = si.states[read_pos[s]]
+            cconv[i] = si.windows[read_pos[s]]
+    cslots = np.array([pos.get(int(s), -1) if s >= 0 else int(s) for s in slots2.reshape(-1)], dtype=np.int32)
+    rows = (reqs[:, None] * L + np.arange(L)[None, :]).reshape(-1)
+    acc = None if si.accepted is None else si.accepted[reqs]
+    W = oracle.Weights(**si.weights.as_dict())
+    if not dim_first:
+        cconv = np.ascontiguousarray(cconv.transpose(0, 2, 1))
+    out, nconv, npool, err = oracle.step(W, si.projected[rows], cconv, cpool, cslots, L, acc, dim_first=dim_first)
+    return out, rows, used, npool[: len(used)], nconv[: len(used)], err
+
+
+def assert_out_close(gpu_bits: np.ndarray, ref_bits: np.ndarray):
+    g, r = bf16_value(gpu_bits), bf16_value(ref_bits)
+    err = np.abs(g - r)
+    bound = OUT_ATOL + OUT_RTOL * np.abs(r)
+    bad = ~(err <= bound)
+    assert not bad.any(), f"{bad.sum()} out elements beyond tolerance; worst {np.nanmax(err)}"
+
+
+def assert_state_close(gpu: np.ndarray, ref: np.ndarray):
+    assert np.isfinite(gpu).all()
+    diff = np.abs(gpu.astype(np.float64) - ref.astype(np.float64))
+    assert diff.max() <= STATE_ATOL, f"state max-abs diff {diff.max()}"
