@@ -158,6 +158,33 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// ---- correctly rounded bf16 hand-offs ------------------------------------
+// The conv outputs (q, k, v) and z = f_b . f_a are handed on as bf16.  They
+// are computed in fp32 with a running bound on the fp32 error; when the fp32
+// value lies within that bound of a bf16 rounding boundary, it is recomputed
+// exactly enough (fp64, or a compensated fp32 sum) before rounding, so the
+// bf16 value equals the correctly rounded one.
+constexpr float U32 = 5.9604644775390625e-08f;  // 2^-24, fp32 unit roundoff
+
+// True when rounding v to bf16 may differ from rounding a value within `bound` of v.
+__device__ __forceinline__ bool bf16_rounding_uncertain(float v, float bound) {
+  const unsigned a = __float_as_uint(v) & 0x7fffffffu;
+  const float lo = __uint_as_float(a & 0xffff0000u);            // v truncated to bf16
+  const float mid = __uint_as_float((a & 0xffff0000u) | 0x8000u); // lo + half a bf16 ulp
+  return fabsf(__uint_as_float(a) - mid) <= bound || 2.0f * bound >= (mid - lo);
+}
+
+// fp64 -> bf16, round to nearest even, via round-to-odd to fp32 (fp32 keeps
+// 16 more bits than bf16, so the second rounding is exact; Boldo & Melquiond,
+// "Emulation of FMA and correctly rounded sums: proved algorithms using
+// rounding to odd").
+__device__ __forceinline__ float bf16_round_f64(double x) {
+  const float f = __double2float_rz(x);
+  unsigned b = __float_as_uint(f);
+  if ((double)f != x) b |= 1u;
+  return __bfloat162float(__float2bfloat16_rn(__uint_as_float(b)));
+}
+
 __device__ __forceinline__ long long conv_index(const StepArgs& a, long long slot, int ch, int j) {
   const int C = 3 * a.D, SL = a.W - 1;
   return a.conv_dim_first ? (slot * C + ch) * SL + j : (slot * SL + j) * C + ch;
@@ -251,9 +278,9 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     // z = f_b . f_a for decay channel c of head h, then the lower-bound gate.
     const int c = tid;
     const uint4* fbrow = reinterpret_cast<const uint4*>(a.f_b + (long long)(h * HD + c) * HD);
-    float acc[L];
+    float acc[L], run[L];  // the fp32 dot and the sum of |partial sums| (its error bound / u)
 #pragma unroll
-    for (int t = 0; t < L; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < L; ++t) acc[t] = run[t] = 0.0f;
 #pragma unroll 2
     for (int j8 = 0; j8 < HD / 8; ++j8) {
       const uint4 w = __ldg(fbrow + j8);
@@ -266,14 +293,34 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         const uint4 fa = *reinterpret_cast<const uint4*>(ob + t * HD + j8 * 8);
         const __nv_bfloat16* fb = reinterpret_cast<const __nv_bfloat16*>(&fa);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[t] = fmaf(wf[e], bf(fb[e]), acc[t]);
+        for (int e = 0; e < 8; ++e) {
+          acc[t] = fmaf(wf[e], bf(fb[e]), acc[t]);  // bf16 x bf16 products are exact in fp32
+          run[t] += fabsf(acc[t]);
+        }
       }
     }
     const float expA = expf(a.A_log[h]);
     const float dtc = a.dt_bias[h * HD + c];
 #pragma unroll
     for (int t = 0; t < L; ++t) {
-      const float z = bf_round(acc[t]);
+      // |acc - exact| <= u (1 + 2u) sum|partials|; margin x2
+      float z;
+      if (!bf16_rounding_uncertain(acc[t], 2.0f * U32 * run[t])) {
+        z = bf_round(acc[t]);
+      } else {
+        // compensated (TwoSum) re-summation: s + e carries the exact dot up to
+        // an error of order n^2 u^2 sum|p|, then one correctly rounded conversion.
+        const __nv_bfloat16* row = a.f_b + (long long)(h * HD + c) * HD;
+        float sum = 0.0f, err = 0.0f;
+        for (int j = 0; j < HD; ++j) {
+          const float p = bf(row[j]) * bf(ob[t * HD + j]);
+          const float nsum = sum + p;
+          const float bp = nsum - sum;
+          err += (sum - (nsum - bp)) + (p - bp);
+          sum = nsum;
+        }
+        z = bf16_round_f64((double)sum + (double)err);
+      }
       const float g = a.lb * sigmoidf_(expA * (z + dtc));
       eg[t * HD + c] = expf(g);
     }
@@ -299,13 +346,28 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
       for (int t = 0; t < L; ++t) {
         const float x = bf(a.projected[(row0 + t) * a.pitch + ch]);
-        float y = b;
+        float y = b, run = 0.0f;  // run: sum of |partial sums|, the fp32 error bound / u
 #pragma unroll
         for (int j = 0; j < 3; ++j)
-          if (j < SL) y = fmaf(w[j], win[j], y);
+          if (j < SL) {
+            y = fmaf(w[j], win[j], y);
+            run += fabsf(y);
+          }
         y = fmaf(w_cur, x, y);
-        y = y * sigmoidf_(y);  // SiLU
-        const float yb = bf_round(y);
+        run += fabsf(y);
+        const float sy = y * sigmoidf_(y);  // SiLU
+        // |sy - silu(exact y)| <= 1.1 u (1+2u) run + 2^-21 |sy| (expf within 2 ulp); margin x2
+        float yb;
+        if (!bf16_rounding_uncertain(sy, 2.0f * (1.1f * U32 * run + 4.0f * U32 * fabsf(sy)))) {
+          yb = bf_round(sy);
+        } else {
+          double yd = (double)b;
+#pragma unroll
+          for (int j = 0; j < 3; ++j)
+            if (j < SL) yd = fma((double)w[j], (double)win[j], yd);
+          yd = fma((double)w_cur, (double)x, yd);
+          yb = bf16_round_f64(yd / (1.0 + exp(-yd)));
+        }
         if (blk == 0) qh[t * HD + i] = yb;
         else if (blk == 1) kh[t * HD + i] = yb;
         else vv[t * HD + i] = __float2bfloat16_rn(yb);
@@ -551,10 +613,10 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
              const int* accepted, void* out, void* cuda_stream) {
   if (h == nullptr) return KDA_EINVAL;
   if (L < 1 || L > KDA_MAX_TOKENS || rows < 0 || rows % L != 0 || pool_slots < 0) return KDA_EINVAL;
-  if (L > 1 && accepted == nullptr) return KDA_EINVAL;
   const long long D = (long long)HD * h->heads;
   if (pitch < 4 * D + HD + h->heads) return KDA_EINVAL;
   if (rows == 0) return KDA_OK;
+  if (L > 1 && accepted == nullptr) return KDA_EINVAL;
   if (!projected || !conv_state || !state_pool || !slots || !out) return KDA_EINVAL;
   if (!aligned(projected, 2) || !aligned(conv_state, 2) || !aligned(state_pool, 16) || !aligned(slots, 4) ||
       !aligned(out, 8) || (accepted && !aligned(accepted, 4)))
