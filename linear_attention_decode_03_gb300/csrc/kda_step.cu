@@ -8,28 +8,33 @@
 //   "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.prepared"
 //   (PreparedKda.__init__, _operands, run, decode_conv_weight).
 //
-// Design (one launch per step, one CTA per (request, head)):
-//   * stage   -- thread 0 validates the request's slots, then issues the whole
-//                64 KiB start state of (slot, head) as four 16 KiB bulk async
-//                copies (cp.async.bulk, evict-first L2 hint) into shared
-//                memory, each completing on its own mbarrier.  The bytes are
-//                in flight before any other work starts (the pages' kda_stage
-//                idea: inputs that need no hand-off go first).
-//   * prologue, overlapping those copies -- warps 0-3: z = f_b . f_a and the
-//                lower-bound gate for the head's 128 decay channels; warps
-//                4-7: the causal conv of the head's q, k, v channels over the
-//                L tokens and the conv-window stores.  Then one warp per token
-//                l2-normalises q and k and computes k^.q^ and beta.
-//   * recurrence -- per 32-row quarter of the state (rows = v), a group of 8
-//                lanes owns one v row (16 k values per lane, kept in registers
-//                across the L tokens); S^T k^ and S^T q^ are reduced with 3
-//                xor shuffles; each token's state row goes out with streaming
-//                128-bit stores into slots[r, t].  o = S'^T q^ + beta u (k^.q^)
-//                with S' the decayed state, an exact reassociation of S_new^T q^.
-//   * norm   -- one warp per token: gated RMSNorm of the bf16 o over the
-//                head's 128 values -> bf16 core_out.
-// Every wait is bounded (1 s of %globaltimer); a wait that gives up sets
-// KDA_ERR_TIMEOUT and the affected outputs are not written.
+// Design: one CTA of 8 warps per (request, head), up to three resident per
+// SM, every global access issued as early as its address is known, so that a
+// CTA spends two memory round trips before its compute:
+//   * round trip 1 (issued at entry, by every thread, with no dependence):
+//       the request's slots / accepted, this warp's 16 rows of the head's f_b
+//       (256 contiguous bytes a row, 8 bytes a lane), the f_a, out-gate and
+//       beta values, the q/k/v inputs and conv taps of the thread's channels.
+//   * round trip 2 (once the slots are in): thread 0 validates them and puts
+//       the 64 KiB start state of (slot, head) in flight as four 16 KiB bulk
+//       async copies (cp.async.bulk, L2 evict-first) on four mbarriers; every
+//       thread loads the start conv windows of its channels.
+//   * while the state lands: z = f_b . f_a per warp (16 channels, 4 products
+//       a lane and a 5-level xor butterfly that also carries the fp32 error
+//       bound), the lower-bound gate and e^g; the causal conv of the q, k, v
+//       channels over the L tokens (window stores into slots[r, t]); one warp
+//       per token l2-normalises q and k and forms k^.q^ and beta.
+//   * recurrence: two passes over pairs of 32-row quarters of the state
+//       (rows = v; each pass waits on its two copies); a group of 8 lanes owns
+//       one v row of each quarter, 16 k values per lane in registers across
+//       the L tokens; S'^T k^ and S'^T q^ are reduced with 3 xor shuffles;
+//       every token's rows go out with 128-bit streaming stores to slots[r, t].
+//   * gated RMSNorm, one warp per token -> bf16 core_out.
+// The bf16 hand-offs (conv outputs, z) are rounded correctly: each fp32 value
+// carries a bound on its error and is recomputed exactly (fp64, or a
+// compensated TwoSum butterfly) when the bound straddles a bf16 rounding
+// boundary.  Every wait is bounded (1 s of %globaltimer); a wait that gives up
+// sets KDA_ERR_TIMEOUT and the request's outputs are not written.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -38,14 +43,19 @@
 
 namespace {
 
-constexpr int HD = 128;                       // head dim (k and v)
-constexpr int THREADS = 256;                  // 8 warps
-constexpr int STATE_FLOATS = HD * HD;         // one (slot, head) state
-constexpr int STATE_BYTES = STATE_FLOATS * 4; // 64 KiB
+constexpr int HD = 128;                        // head dim (k and v)
+constexpr int THREADS = 256;                   // 8 warps
+constexpr int WARPS = THREADS / 32;
+constexpr int Z_CHANNELS = HD / WARPS;         // 16 decay channels a warp
+constexpr int CONV_JOBS = 3 * HD;              // q, k, v channels of the head
+constexpr int STATE_FLOATS = HD * HD;          // one (slot, head) state
+constexpr int STATE_BYTES = STATE_FLOATS * 4;  // 64 KiB
 constexpr int QUARTERS = 4;
-constexpr int QUARTER_ROWS = HD / QUARTERS;   // 32 v rows
+constexpr int QUARTER_ROWS = HD / QUARTERS;    // 32 v rows
 constexpr int QUARTER_BYTES = STATE_BYTES / QUARTERS;
 constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;
+
+enum { TASK_OK = 0, TASK_PADDING = 1, TASK_SKIP = 2 };
 
 struct StepArgs {
   const __nv_bfloat16* projected;
@@ -70,17 +80,18 @@ struct StepArgs {
 // Shared-memory carve-up for L tokens (byte offsets from the dynamic base).
 template <int L>
 struct Smem {
-  static constexpr int state = 0;
-  static constexpr int eg = state + STATE_BYTES;      // float [L][128]  e^g
-  static constexpr int kh = eg + L * HD * 4;          // float [L][128]  k, then k^
-  static constexpr int qh = kh + L * HD * 4;          // float [L][128]  q, then q^
-  static constexpr int vv = qh + L * HD * 4;          // bf16  [L][128]  v
-  static constexpr int ob = vv + L * HD * 2;          // bf16  [L][128]  f_a, then o
-  static constexpr int beta = ob + L * HD * 2;        // float [L]
-  static constexpr int kq = beta + 4 * L;             // float [L]       k^.q^
-  static constexpr int slot = kq + 4 * L;             // int   [L]
-  static constexpr int ctl = slot + 4 * L;            // int   [4]       status, start, timeout
-  static constexpr int mbar = (ctl + 16 + 7) / 8 * 8; // u64   [4]
+  static constexpr int state = 0;                     // float [128][128]  start state
+  static constexpr int eg = state + STATE_BYTES;      // float [L][128]    e^g
+  static constexpr int kh = eg + L * HD * 4;          // float [L][128]    k, then k^
+  static constexpr int qh = kh + L * HD * 4;          // float [L][128]    q, then q^
+  static constexpr int fa = qh + L * HD * 4;          // float [L][128]    f_a; later bf16 o
+  static constexpr int vv = fa + L * HD * 4;          // bf16  [L][128]    v
+  static constexpr int gate = vv + L * HD * 2;        // bf16  [L][128]    out-gate
+  static constexpr int beta = gate + L * HD * 2;      // float [L]
+  static constexpr int kq = beta + 4 * L;             // float [L]         k^.q^
+  static constexpr int slot = kq + 4 * L;             // int   [L]         slots[r, t]
+  static constexpr int ctl = slot + 4 * L;            // int   [2]         timeout flag
+  static constexpr int mbar = (ctl + 8 + 7) / 8 * 8;  // u64   [4]
   static constexpr int bytes = mbar + 8 * QUARTERS;
 };
 
@@ -123,14 +134,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, unsigned parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after WAIT_LIMIT_NS.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer() - t0 > WAIT_LIMIT_NS) return false;
-  }
-  return true;
+// As mbar_try_wait, but the thread may sleep up to SUSPEND_HINT_NS until the
+// phase completes, instead of returning at once: a waiting warp then takes no
+// issue slots from the warps that do the work it waits for.
+constexpr unsigned SUSPEND_HINT_NS = 1000000u;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(SUSPEND_HINT_NS)
+      : "memory");
+  return ok != 0;
 }
 
 // Bulk async global -> shared copy completing on an mbarrier, L2 evict-first.
@@ -169,7 +186,7 @@ constexpr float U32 = 5.9604644775390625e-08f;  // 2^-24, fp32 unit roundoff
 // True when rounding v to bf16 may differ from rounding a value within `bound` of v.
 __device__ __forceinline__ bool bf16_rounding_uncertain(float v, float bound) {
   const unsigned a = __float_as_uint(v) & 0x7fffffffu;
-  const float lo = __uint_as_float(a & 0xffff0000u);            // v truncated to bf16
+  const float lo = __uint_as_float(a & 0xffff0000u);             // v truncated to bf16
   const float mid = __uint_as_float((a & 0xffff0000u) | 0x8000u); // lo + half a bf16 ulp
   return fabsf(__uint_as_float(a) - mid) <= bound || 2.0f * bound >= (mid - lo);
 }
@@ -190,6 +207,59 @@ __device__ __forceinline__ long long conv_index(const StepArgs& a, long long slo
   return a.conv_dim_first ? (slot * C + ch) * SL + j : (slot * SL + j) * C + ch;
 }
 
+
+// Wait for phase `parity` of an mbarrier, giving up after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer();
+  while (!mbar_try_wait_sleep(bar, parity)) {
+    if (global_timer() - t0 > WAIT_LIMIT_NS) return false;
+  }
+  return true;
+}
+
+// z for one channel from this lane's four products (w . f): the fp32 sum over
+// the warp by a 5-level xor butterfly, correctly rounded to bf16.  Every lane
+// returns the same value.  The fp32 path carries run = the sum of |every
+// rounded intermediate|, so |z - exact| <= u (1 + 2u) run; within twice that
+// of a bf16 rounding boundary, the warp redoes the sum with TwoSum (exact
+// pairs hi + lo through the same butterfly) and rounds hi + lo once.
+__device__ __forceinline__ float z_channel(const float w[4], const float4 f) {
+  float p = w[0] * f.x;  // exact: bf16 x bf16
+  float run = 0.0f;
+  p = fmaf(w[1], f.y, p);
+  run += fabsf(p);
+  p = fmaf(w[2], f.z, p);
+  run += fabsf(p);
+  p = fmaf(w[3], f.w, p);
+  run += fabsf(p);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    p += __shfl_xor_sync(0xffffffffu, p, m);
+    run += __shfl_xor_sync(0xffffffffu, run, m);
+    run += fabsf(p);
+  }
+  if (!bf16_rounding_uncertain(p, 2.0f * U32 * run)) return bf_round(p);
+  // exact pairs: a + b = s + e exactly (Knuth's TwoSum)
+  const float pr[4] = {w[0] * f.x, w[1] * f.y, w[2] * f.z, w[3] * f.w};
+  float hi = pr[0], lo = 0.0f;
+#pragma unroll
+  for (int e = 1; e < 4; ++e) {
+    const float s = hi + pr[e], bp = s - hi;
+    lo += (hi - (s - bp)) + (pr[e] - bp);
+    hi = s;
+  }
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    const float ho = __shfl_xor_sync(0xffffffffu, hi, m);
+    const float lo_o = __shfl_xor_sync(0xffffffffu, lo, m);
+    const float s = hi + ho, bp = s - hi;
+    lo = (lo + lo_o) + ((hi - (s - bp)) + (ho - bp));
+    hi = s;
+  }
+  return bf16_round_f64((double)hi + (double)lo);
+}
+
 template <int L>
 __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(const StepArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -198,269 +268,284 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   float* eg = reinterpret_cast<float*>(smem + S::eg);
   float* kh = reinterpret_cast<float*>(smem + S::kh);
   float* qh = reinterpret_cast<float*>(smem + S::qh);
+  float* fa_s = reinterpret_cast<float*>(smem + S::fa);
+  __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(smem + S::fa);  // reuses the f_a space
   __nv_bfloat16* vv = reinterpret_cast<__nv_bfloat16*>(smem + S::vv);
-  __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(smem + S::ob);
+  __nv_bfloat16* gate_s = reinterpret_cast<__nv_bfloat16*>(smem + S::gate);
   float* beta_s = reinterpret_cast<float*>(smem + S::beta);
   float* kq_s = reinterpret_cast<float*>(smem + S::kq);
   int* slot_s = reinterpret_cast<int*>(smem + S::slot);
   int* ctl = reinterpret_cast<int*>(smem + S::ctl);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + S::mbar);
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x % a.heads;
   const long long r = blockIdx.x / a.heads;
   const long long row0 = r * L;
-  const int D = a.D;
+  const int D = a.D, SL = a.W - 1;
 
-  // ---- stage: validate the request, put the start state in flight --------
-  if (tid == 0) {
-    const int* sl = a.slots + row0;
-    int status = 0, start = 0;
-    if (sl[0] == -1) {
-      status = 1;  // padding request
-    } else {
-      int acc = 1;
-      if (a.accepted != nullptr) {
-        acc = a.accepted[r];
-        if (acc < 1 || acc > L) {
-          status = 2;
-          atomicOr(a.err, KDA_ERR_ACCEPTED);
-        }
-      }
-      if (status == 0) {
-        bool bad = false;
+  // ---- round trip 1: everything that needs no other value -------------------
+  int sl[L];
 #pragma unroll
-        for (int t = 0; t < L; ++t) {
-          const int s = sl[t];
-          slot_s[t] = s;
-          bad |= (s < 0) || (s >= a.pool);
-        }
-        if (bad) {
-          status = 2;
-          atomicOr(a.err, KDA_ERR_SLOT);
-        } else {
-          start = sl[acc - 1];
-        }
-      }
-    }
-    ctl[0] = status;
-    ctl[1] = start;
-    ctl[2] = 0;
-    if (status == 0) {
-      const float* src = a.state_pool + ((long long)start * a.heads + h) * STATE_FLOATS;
+  for (int t = 0; t < L; ++t) sl[t] = a.slots[row0 + t];
+  const int acc = (a.accepted != nullptr) ? a.accepted[r] : 1;
+  uint2 fbw[Z_CHANNELS];  // this lane's 4 bf16 of each of the warp's 16 f_b rows
+  {
+    const uint2* fb = reinterpret_cast<const uint2*>(a.f_b + (long long)(h * HD + warp * Z_CHANNELS) * HD) + lane;
 #pragma unroll
-      for (int q = 0; q < QUARTERS; ++q) mbar_init(smem_u32(&mbar[q]), 1);
-      fence_mbar_init();
+    for (int i = 0; i < Z_CHANNELS; ++i) fbw[i] = __ldg(fb + i * (HD / 4));
+  }
+  // f_a and out-gate of the L tokens, two values a thread
+  constexpr int PER_THREAD = (L * HD + THREADS - 1) / THREADS;
+  unsigned short fa_v[PER_THREAD], gate_v[PER_THREAD];  // raw bf16 bits
 #pragma unroll
-      for (int q = 0; q < QUARTERS; ++q) {
-        const uint32_t bar = smem_u32(&mbar[q]);
-        mbar_expect_tx(bar, QUARTER_BYTES);
-        bulk_load(smem_u32(st + q * QUARTER_ROWS * HD), src + q * QUARTER_ROWS * HD, QUARTER_BYTES, bar);
-      }
+  for (int i = 0; i < PER_THREAD; ++i) {
+    const int e = tid + i * THREADS;
+    fa_v[i] = gate_v[i] = 0;
+    if (e < L * HD) {
+      const unsigned short* prow = reinterpret_cast<const unsigned short*>(a.projected + (row0 + e / HD) * a.pitch);
+      fa_v[i] = prow[4 * D + (e % HD)];
+      gate_v[i] = prow[3 * D + h * HD + (e % HD)];
     }
   }
-  __syncthreads();
-  const int status = ctl[0];
-  if (status == 1) {  // padding: zero output rows, no cache traffic
+  float beta_logit = 0.0f;
+  if (tid < L) beta_logit = bf(a.projected[(row0 + tid) * a.pitch + 4 * D + HD + h]);
+
+  // ---- validate (every thread decides the same from the same loaded values) ---
+  int status = TASK_OK, start = sl[0];
+  if (sl[0] == -1) {
+    status = TASK_PADDING;
+  } else if (acc < 1 || acc > L) {
+    status = TASK_SKIP;
+    if (tid == 0) atomicOr(a.err, KDA_ERR_ACCEPTED);
+  } else {
+    bool bad = false;
+#pragma unroll
+    for (int t = 0; t < L; ++t) {
+      bad |= (sl[t] < 0) || (sl[t] >= a.pool);
+      if (t == acc - 1) start = sl[t];
+    }
+    if (bad) {
+      status = TASK_SKIP;
+      if (tid == 0) atomicOr(a.err, KDA_ERR_SLOT);
+    }
+  }
+  if (status == TASK_PADDING) {  // zero output rows, no cache traffic
     for (int i = tid; i < L * HD; i += THREADS)
       a.out[(row0 + i / HD) * D + h * HD + (i % HD)] = __float2bfloat16_rn(0.0f);
     return;
   }
-  if (status != 0) return;
-  const int start = ctl[1];
+  if (status != TASK_OK) return;
 
-  // ---- prologue: f_a staging ------------------------------------------------
-  for (int i = tid; i < L * HD; i += THREADS)
-    ob[i] = a.projected[(row0 + i / HD) * a.pitch + 4 * D + (i % HD)];
-  __syncthreads();
-
-  if (tid < HD) {
-    // z = f_b . f_a for decay channel c of head h, then the lower-bound gate.
-    const int c = tid;
-    const uint4* fbrow = reinterpret_cast<const uint4*>(a.f_b + (long long)(h * HD + c) * HD);
-    float acc[L], run[L];  // the fp32 dot and the sum of |partial sums| (its error bound / u)
+  // ---- round trip 2: the start state (bulk) and the start conv windows -------
+  if (tid == 0) {
+    const float* src = a.state_pool + ((long long)start * a.heads + h) * STATE_FLOATS;
 #pragma unroll
-    for (int t = 0; t < L; ++t) acc[t] = run[t] = 0.0f;
-#pragma unroll 2
-    for (int j8 = 0; j8 < HD / 8; ++j8) {
-      const uint4 w = __ldg(fbrow + j8);
-      const __nv_bfloat16* wb = reinterpret_cast<const __nv_bfloat16*>(&w);
-      float wf[8];
+    for (int q = 0; q < QUARTERS; ++q) mbar_init(smem_u32(&mbar[q]), 1);
+    fence_mbar_init();
 #pragma unroll
-      for (int e = 0; e < 8; ++e) wf[e] = bf(wb[e]);
-#pragma unroll
-      for (int t = 0; t < L; ++t) {
-        const uint4 fa = *reinterpret_cast<const uint4*>(ob + t * HD + j8 * 8);
-        const __nv_bfloat16* fb = reinterpret_cast<const __nv_bfloat16*>(&fa);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          acc[t] = fmaf(wf[e], bf(fb[e]), acc[t]);  // bf16 x bf16 products are exact in fp32
-          run[t] += fabsf(acc[t]);
-        }
-      }
+    for (int q = 0; q < QUARTERS; ++q) {
+      const uint32_t bar = smem_u32(&mbar[q]);
+      mbar_expect_tx(bar, QUARTER_BYTES);
+      bulk_load(smem_u32(st + q * QUARTER_ROWS * HD), src + q * QUARTER_ROWS * HD, QUARTER_BYTES, bar);
     }
+    ctl[0] = 0;
+  }
+#pragma unroll
+  for (int t = 0; t < L; ++t)
+    if (tid == t) slot_s[t] = sl[t];
+#pragma unroll
+  for (int i = 0; i < PER_THREAD; ++i) {
+    const int e = tid + i * THREADS;
+    if (e < L * HD) {
+      fa_s[e] = __uint_as_float((unsigned)fa_v[i] << 16);
+      reinterpret_cast<unsigned short*>(gate_s)[e] = gate_v[i];
+    }
+  }
+  if (tid < L) beta_s[tid] = sigmoidf_(beta_logit);
+  __syncthreads();  // barriers initialised, f_a staged
+
+  // ---- z = f_b . f_a (correctly rounded), lower-bound gate, e^g ---------------
+  {
     const float expA = expf(a.A_log[h]);
-    const float dtc = a.dt_bias[h * HD + c];
-#pragma unroll
-    for (int t = 0; t < L; ++t) {
-      // |acc - exact| <= u (1 + 2u) sum|partials|; margin x2
-      float z;
-      if (!bf16_rounding_uncertain(acc[t], 2.0f * U32 * run[t])) {
-        z = bf_round(acc[t]);
-      } else {
-        // compensated (TwoSum) re-summation: s + e carries the exact dot up to
-        // an error of order n^2 u^2 sum|p|, then one correctly rounded conversion.
-        const __nv_bfloat16* row = a.f_b + (long long)(h * HD + c) * HD;
-        float sum = 0.0f, err = 0.0f;
-        for (int j = 0; j < HD; ++j) {
-          const float p = bf(row[j]) * bf(ob[t * HD + j]);
-          const float nsum = sum + p;
-          const float bp = nsum - sum;
-          err += (sum - (nsum - bp)) + (p - bp);
-          sum = nsum;
-        }
-        z = bf16_round_f64((double)sum + (double)err);
-      }
-      const float g = a.lb * sigmoidf_(expA * (z + dtc));
-      eg[t * HD + c] = expf(g);
-    }
-  } else {
-    // causal depthwise conv of channel i in the head's q, k and v blocks.
-    const int i = tid - HD;
-    const int SL = a.W - 1;
+    const int c0 = warp * Z_CHANNELS;
+    const float dtc = (lane < Z_CHANNELS) ? a.dt_bias[h * HD + c0 + lane] : 0.0f;
 #pragma unroll 1
-    for (int blk = 0; blk < 3; ++blk) {
-      const int ch = blk * D + h * HD + i;
-      float win[3] = {0.0f, 0.0f, 0.0f}, w[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int t = 0; t < L; ++t) {
+      const float4 f = *reinterpret_cast<const float4*>(fa_s + t * HD + lane * 4);
+      float zmine = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 3; ++j)
-        if (j < SL) win[j] = bf(a.conv_state[conv_index(a, start, ch, j)]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (j < a.W) w[j] = bf(a.conv_w[(long long)(blk * a.W + j) * D + h * HD + i]);
-      const float b = a.bias ? bf(a.bias[ch]) : 0.0f;
-      float w_cur = 0.0f;  // the tap on the current token, w[SL]
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (j == SL) w_cur = w[j];
-#pragma unroll
-      for (int t = 0; t < L; ++t) {
-        const float x = bf(a.projected[(row0 + t) * a.pitch + ch]);
-        float y = b, run = 0.0f;  // run: sum of |partial sums|, the fp32 error bound / u
-#pragma unroll
-        for (int j = 0; j < 3; ++j)
-          if (j < SL) {
-            y = fmaf(w[j], win[j], y);
-            run += fabsf(y);
-          }
-        y = fmaf(w_cur, x, y);
-        run += fabsf(y);
-        const float sy = y * sigmoidf_(y);  // SiLU
-        // |sy - silu(exact y)| <= 1.1 u (1+2u) run + 2^-21 |sy| (expf within 2 ulp); margin x2
-        float yb;
-        if (!bf16_rounding_uncertain(sy, 2.0f * (1.1f * U32 * run + 4.0f * U32 * fabsf(sy)))) {
-          yb = bf_round(sy);
-        } else {
-          double yd = (double)b;
-#pragma unroll
-          for (int j = 0; j < 3; ++j)
-            if (j < SL) yd = fma((double)w[j], (double)win[j], yd);
-          yd = fma((double)w_cur, (double)x, yd);
-          yb = bf16_round_f64(yd / (1.0 + exp(-yd)));
-        }
-        if (blk == 0) qh[t * HD + i] = yb;
-        else if (blk == 1) kh[t * HD + i] = yb;
-        else vv[t * HD + i] = __float2bfloat16_rn(yb);
-#pragma unroll
-        for (int j = 0; j < 3; ++j)
-          win[j] = (j + 1 < SL) ? win[j + 1] : (j + 1 == SL ? x : win[j]);
-        const long long dst = slot_s[t];
-#pragma unroll
-        for (int j = 0; j < 3; ++j)
-          if (j < SL) a.conv_state[conv_index(a, dst, ch, j)] = __float2bfloat16_rn(win[j]);
+      for (int i = 0; i < Z_CHANNELS; ++i) {
+        const float wv[4] = {__uint_as_float(fbw[i].x << 16), __uint_as_float(fbw[i].x & 0xffff0000u),
+                             __uint_as_float(fbw[i].y << 16), __uint_as_float(fbw[i].y & 0xffff0000u)};
+        const float z = z_channel(wv, f);
+        if (lane == i) zmine = z;
+      }
+      if (lane < Z_CHANNELS) {
+        const float g = a.lb * sigmoidf_(expA * (zmine + dtc));
+        eg[t * HD + c0 + lane] = expf(g);
       }
     }
   }
-  __syncthreads();
 
-  // ---- l2norm of q and k, k^.q^, beta: one warp per token --------------------
-  const int warp = tid >> 5, lane = tid & 31;
+  // ---- causal conv of the thread's channels (correctly rounded), window stores -
+  // Job j in [0, 384) is channel j % 128 of block j / 128 (q, k, v); thread tid
+  // takes jobs tid and tid + 256.  Its inputs are loaded only now, while the
+  // state copies are still landing, so they are not live during z.
+  constexpr int JOBS = (CONV_JOBS + THREADS - 1) / THREADS;  // 2
+  float x[JOBS][L], w[JOBS][4], b[JOBS], win[JOBS][3];
+#pragma unroll
+  for (int jb = 0; jb < JOBS; ++jb) {
+    const int j = tid + jb * THREADS;
+    if (j < CONV_JOBS) {
+      const int blk = j / HD, c = j % HD, ch = blk * D + h * HD + c;
+#pragma unroll
+      for (int t = 0; t < L; ++t) x[jb][t] = bf(a.projected[(row0 + t) * a.pitch + ch]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w[jb][k] = (k < a.W) ? bf(a.conv_w[(long long)(blk * a.W + k) * D + h * HD + c]) : 0.0f;
+      b[jb] = a.bias ? bf(a.bias[ch]) : 0.0f;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) win[jb][k] = (k < SL) ? bf(a.conv_state[conv_index(a, start, ch, k)]) : 0.0f;
+    }
+  }
+#pragma unroll
+  for (int jb = 0; jb < JOBS; ++jb) {
+    const int j = tid + jb * THREADS;
+    if (j >= CONV_JOBS) continue;
+    const int blk = j / HD, c = j % HD, ch = blk * D + h * HD + c;
+    float wcur = 0.0f;  // the tap on the current token, w[SL]
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (k == SL) wcur = w[jb][k];
+#pragma unroll
+    for (int t = 0; t < L; ++t) {
+      const float xt = x[jb][t];
+      float y = b[jb], run = 0.0f;  // run: sum of |partial sums|, the fp32 error bound / u
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        if (k < SL) {
+          y = fmaf(w[jb][k], win[jb][k], y);
+          run += fabsf(y);
+        }
+      y = fmaf(wcur, xt, y);
+      run += fabsf(y);
+      const float sy = y * sigmoidf_(y);  // SiLU
+      // |sy - silu(exact y)| <= 1.1 u (1+2u) run + 2^-21 |sy| (expf within 2 ulp); margin x2
+      float yb;
+      if (!bf16_rounding_uncertain(sy, 2.0f * (1.1f * U32 * run + 4.0f * U32 * fabsf(sy)))) {
+        yb = bf_round(sy);
+      } else {
+        double yd = (double)b[jb];
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+          if (k < SL) yd = fma((double)w[jb][k], (double)win[jb][k], yd);
+        yd = fma((double)wcur, (double)xt, yd);
+        yb = bf16_round_f64(yd / (1.0 + exp(-yd)));
+      }
+      if (blk == 0) qh[t * HD + c] = yb;
+      else if (blk == 1) kh[t * HD + c] = yb;
+      else vv[t * HD + c] = __float2bfloat16_rn(yb);
+      // shift the window by one and store it into this token's slot
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        win[jb][k] = (k + 1 < SL) ? win[jb][k + 1] : (k + 1 == SL ? xt : win[jb][k]);
+      const long long dst = slot_s[t];
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        if (k < SL) a.conv_state[conv_index(a, dst, ch, k)] = __float2bfloat16_rn(win[jb][k]);
+    }
+  }
+  __syncthreads();  // raw q, k, v and e^g of every channel written
+
+  // ---- l2norm of q and k, k^.q^: one warp per token -----------------------------
   if (warp < L) {
     const int t = warp;
     float4 q = *reinterpret_cast<float4*>(qh + t * HD + lane * 4);
     float4 k = *reinterpret_cast<float4*>(kh + t * HD + lane * 4);
     const float sq = warp_sum(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
     const float sk = warp_sum(k.x * k.x + k.y * k.y + k.z * k.z + k.w * k.w);
-    const float qk = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w);
+    const float sqk = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w);
     const float rq = 1.0f / sqrtf(sq + 1e-6f), rk = 1.0f / sqrtf(sk + 1e-6f);
     const float fq = rq * a.q_scale;
     q.x *= fq; q.y *= fq; q.z *= fq; q.w *= fq;
     k.x *= rk; k.y *= rk; k.z *= rk; k.w *= rk;
     *reinterpret_cast<float4*>(qh + t * HD + lane * 4) = q;
     *reinterpret_cast<float4*>(kh + t * HD + lane * 4) = k;
-    if (lane == 0) {
-      kq_s[t] = qk * fq * rk;
-      beta_s[t] = sigmoidf_(bf(a.projected[(row0 + t) * a.pitch + 4 * D + HD + h]));
-    }
+    if (lane == 0) kq_s[t] = sqk * fq * rk;
   }
   __syncthreads();
 
-  // ---- recurrence: a group of 8 lanes per v row, 16 k values per lane --------
+  // ---- recurrence: 2 passes of 2 quarters; 8 lanes per v row, 16 k values a lane --
   const int sub = lane >> 3, kl = lane & 7;
-  bool any_timeout = false;
+  const int lr = warp * 4 + sub;  // row within a quarter
+  bool timed_out = false;
+  float* dst_row = a.state_pool + ((long long)h * HD + lr) * HD + kl * 4;
 #pragma unroll 1
-  for (int qtr = 0; qtr < QUARTERS; ++qtr) {
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mbar[qtr]), 0));
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mbar[2 * pass]), 0) &&
+                                                mbar_wait_bounded(smem_u32(&mbar[2 * pass + 1]), 0));
     if (!ok) {
-      any_timeout = true;
+      timed_out = true;
       continue;
     }
-    const int v = qtr * QUARTER_ROWS + warp * 4 + sub;
-    float4 s[4];
+    float4 sv[2][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) s[j] = *reinterpret_cast<const float4*>(st + v * HD + j * 32 + kl * 4);
+    for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        sv[qq][j] = *reinterpret_cast<const float4*>(st + ((2 * pass + qq) * QUARTER_ROWS + lr) * HD + j * 32 + kl * 4);
 #pragma unroll 1
     for (int t = 0; t < L; ++t) {
       float4 kv[4];
-      float dk = 0.0f, dq = 0.0f;
+      float dk[2] = {0.0f, 0.0f}, dq[2] = {0.0f, 0.0f};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int k0 = t * HD + j * 32 + kl * 4;
         const float4 e = *reinterpret_cast<const float4*>(eg + k0);
         const float4 qv = *reinterpret_cast<const float4*>(qh + k0);
         kv[j] = *reinterpret_cast<const float4*>(kh + k0);
-        s[j].x *= e.x; s[j].y *= e.y; s[j].z *= e.z; s[j].w *= e.w;
-        dk = fmaf(s[j].x, kv[j].x, dk); dk = fmaf(s[j].y, kv[j].y, dk);
-        dk = fmaf(s[j].z, kv[j].z, dk); dk = fmaf(s[j].w, kv[j].w, dk);
-        dq = fmaf(s[j].x, qv.x, dq); dq = fmaf(s[j].y, qv.y, dq);
-        dq = fmaf(s[j].z, qv.z, dq); dq = fmaf(s[j].w, qv.w, dq);
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          float4& s = sv[qq][j];
+          s.x *= e.x; s.y *= e.y; s.z *= e.z; s.w *= e.w;
+          dk[qq] = fmaf(s.x, kv[j].x, dk[qq]); dk[qq] = fmaf(s.y, kv[j].y, dk[qq]);
+          dk[qq] = fmaf(s.z, kv[j].z, dk[qq]); dk[qq] = fmaf(s.w, kv[j].w, dk[qq]);
+          dq[qq] = fmaf(s.x, qv.x, dq[qq]); dq[qq] = fmaf(s.y, qv.y, dq[qq]);
+          dq[qq] = fmaf(s.z, qv.z, dq[qq]); dq[qq] = fmaf(s.w, qv.w, dq[qq]);
+        }
       }
 #pragma unroll
-      for (int m = 1; m <= 4; m <<= 1) {
-        dk += __shfl_xor_sync(0xffffffffu, dk, m);
-        dq += __shfl_xor_sync(0xffffffffu, dq, m);
-      }
-      const float u = bf(vv[t * HD + v]) - dk;
-      const float bu = beta_s[t] * u;
-      const float o = fmaf(bu, kq_s[t], dq);
-      float* dst = a.state_pool + (((long long)slot_s[t] * a.heads + h) * HD + v) * HD + kl * 4;
+      for (int m = 1; m <= 4; m <<= 1)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        s[j].x = fmaf(bu, kv[j].x, s[j].x); s[j].y = fmaf(bu, kv[j].y, s[j].y);
-        s[j].z = fmaf(bu, kv[j].z, s[j].z); s[j].w = fmaf(bu, kv[j].w, s[j].w);
-        store_streaming(dst + j * 32, s[j]);
+        for (int qq = 0; qq < 2; ++qq) {
+          dk[qq] += __shfl_xor_sync(0xffffffffu, dk[qq], m);
+          dq[qq] += __shfl_xor_sync(0xffffffffu, dq[qq], m);
+        }
+      float* dst = dst_row + (long long)slot_s[t] * a.heads * STATE_FLOATS;
+      const float bt = beta_s[t], kqt = kq_s[t];
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const int v = (2 * pass + qq) * QUARTER_ROWS + lr;
+        const float u = bf(vv[t * HD + v]) - dk[qq];
+        const float bu = bt * u;
+        const float o = fmaf(bu, kqt, dq[qq]);  // S_new^T q^ = S'^T q^ + beta u (k^.q^)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float4& s = sv[qq][j];
+          s.x = fmaf(bu, kv[j].x, s.x); s.y = fmaf(bu, kv[j].y, s.y);
+          s.z = fmaf(bu, kv[j].z, s.z); s.w = fmaf(bu, kv[j].w, s.w);
+          store_streaming(dst + (2 * pass + qq) * QUARTER_ROWS * HD + j * 32, s);
+        }
+        if (kl == 0) ob[t * HD + v] = __float2bfloat16_rn(o);
       }
-      if (kl == 0) ob[t * HD + v] = __float2bfloat16_rn(o);
     }
   }
-  if (any_timeout) {
-    if (lane == 0) {
-      ctl[2] = 1;
-      atomicOr(a.err, KDA_ERR_TIMEOUT);
-    }
+  if (timed_out && lane == 0) {
+    ctl[0] = 1;
+    atomicOr(a.err, KDA_ERR_TIMEOUT);
   }
   __syncthreads();
-  if (ctl[2] != 0) {
+  if (ctl[0] != 0) {
     // Give copies still in flight a second bounded chance to land before the
     // shared memory is released; the outputs of this request stay unwritten.
     if (tid == 0)
@@ -468,7 +553,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     return;
   }
 
-  // ---- gated RMSNorm: one warp per token ---------------------------------------
+  // ---- gated RMSNorm: one warp per token -----------------------------------------
   if (warp < L) {
     const int t = warp;
     float o[4];
@@ -476,11 +561,10 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     for (int e = 0; e < 4; ++e) o[e] = bf(ob[t * HD + lane * 4 + e]);
     const float ss = warp_sum(o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3]);
     const float rstd = 1.0f / sqrtf(ss * (1.0f / HD) + a.eps);
-    const __nv_bfloat16* gate = a.projected + (row0 + t) * a.pitch + 3 * D + h * HD + lane * 4;
     __align__(8) __nv_bfloat16 y[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      y[e] = __float2bfloat16_rn(o[e] * rstd * a.o_norm[lane * 4 + e] * sigmoidf_(bf(gate[e])));
+      y[e] = __float2bfloat16_rn(o[e] * rstd * a.o_norm[lane * 4 + e] * sigmoidf_(bf(gate_s[t * HD + lane * 4 + e])));
     *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
   }
 }
@@ -497,19 +581,8 @@ __global__ void relayout_conv_w(const __nv_bfloat16* in, __nv_bfloat16* out, int
 }
 
 template <int L>
-int smem_bytes() {
-  return Smem<L>::bytes;
-}
-
-template <int L>
 cudaError_t set_smem_attr() {
   return cudaFuncSetAttribute(kda_step_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<L>::bytes);
-}
-
-template <int L>
-cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream) {
-  kda_step_kernel<L><<<(unsigned)ctas, THREADS, Smem<L>::bytes, stream>>>(a);
-  return cudaGetLastError();
 }
 
 cudaError_t set_all_smem_attrs() {
@@ -521,12 +594,24 @@ cudaError_t set_all_smem_attrs() {
   return e;
 }
 
+template <int L>
+cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream) {
+  kda_step_kernel<L><<<(unsigned)ctas, THREADS, Smem<L>::bytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int L>
+const void* kernel_fn() {
+  return reinterpret_cast<const void*>(kda_step_kernel<L>);
+}
+
 bool aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
 }  // namespace
 
 struct kda_handle {
   int device;
+  int sms;  // multiprocessors of the device: one persistent CTA each
   int heads, W;
   __nv_bfloat16* conv_w;
   __nv_bfloat16* bias;
@@ -569,7 +654,7 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
   *out = nullptr;
   if (heads < 1 || conv_width < 2 || conv_width > 4 || !(eps > 0.0f)) return KDA_EINVAL;
   if (!conv_w || !f_b || !A_log || !dt_bias || !o_norm) return KDA_EINVAL;
-  if (!aligned(conv_w, 2) || !aligned(f_b, 2) || !aligned(A_log, 4) || !aligned(dt_bias, 4) ||
+  if (!aligned(conv_w, 2) || !aligned(f_b, 8) || !aligned(A_log, 4) || !aligned(dt_bias, 4) ||
       !aligned(o_norm, 4) || (bias && !aligned(bias, 2)))
     return KDA_EINVAL;
   const long long D = (long long)HD * heads;
@@ -579,6 +664,7 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
   h->lb = gate_lower_bound;
   h->eps = eps;
   cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device);
   const size_t conv_bytes = sizeof(__nv_bfloat16) * 3 * D * conv_width;
   if (e == cudaSuccess) e = cudaMalloc(&h->conv_w, conv_bytes);
   if (e == cudaSuccess && bias) e = cudaMalloc(&h->bias, sizeof(__nv_bfloat16) * 3 * D);
@@ -598,6 +684,7 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
         static_cast<const __nv_bfloat16*>(conv_w), h->conv_w, (int)D, conv_width);
     e = cudaGetLastError();
   }
+
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = set_all_smem_attrs();
   if (e != cudaSuccess) {
@@ -621,8 +708,7 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
   if (!aligned(projected, 2) || !aligned(conv_state, 2) || !aligned(state_pool, 16) || !aligned(slots, 4) ||
       !aligned(out, 8) || (accepted && !aligned(accepted, 4)))
     return KDA_EINVAL;
-  const long long ctas = (rows / L) * h->heads;
-  if (ctas > 0x7fffffffLL) return KDA_EINVAL;
+  if (pool_slots > 0x7fffffffLL || rows > 0x7fffffffLL) return KDA_EINVAL;
 
   StepArgs a;
   a.projected = static_cast<const __nv_bfloat16*>(projected);
@@ -648,6 +734,8 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
   a.W = h->W;
   a.conv_dim_first = conv_dim_first ? 1 : 0;
 
+  const long long ctas = (rows / L) * h->heads;
+  if (ctas > 0x7fffffffLL) return KDA_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   cudaError_t e;
   switch (L) {
@@ -678,14 +766,14 @@ int kda_launch_info(int L, int* threads, int* smem, int* ctas_per_sm) {
   const void* fn = nullptr;
   int bytes = 0;
   switch (L) {
-    case 1: fn = (const void*)kda_step_kernel<1>; bytes = smem_bytes<1>(); break;
-    case 2: fn = (const void*)kda_step_kernel<2>; bytes = smem_bytes<2>(); break;
-    case 3: fn = (const void*)kda_step_kernel<3>; bytes = smem_bytes<3>(); break;
-    case 4: fn = (const void*)kda_step_kernel<4>; bytes = smem_bytes<4>(); break;
-    case 5: fn = (const void*)kda_step_kernel<5>; bytes = smem_bytes<5>(); break;
-    case 6: fn = (const void*)kda_step_kernel<6>; bytes = smem_bytes<6>(); break;
-    case 7: fn = (const void*)kda_step_kernel<7>; bytes = smem_bytes<7>(); break;
-    default: fn = (const void*)kda_step_kernel<8>; bytes = smem_bytes<8>(); break;
+    case 1: fn = kernel_fn<1>(); bytes = Smem<1>::bytes; break;
+    case 2: fn = kernel_fn<2>(); bytes = Smem<2>::bytes; break;
+    case 3: fn = kernel_fn<3>(); bytes = Smem<3>::bytes; break;
+    case 4: fn = kernel_fn<4>(); bytes = Smem<4>::bytes; break;
+    case 5: fn = kernel_fn<5>(); bytes = Smem<5>::bytes; break;
+    case 6: fn = kernel_fn<6>(); bytes = Smem<6>::bytes; break;
+    case 7: fn = kernel_fn<7>(); bytes = Smem<7>::bytes; break;
+    default: fn = kernel_fn<8>(); bytes = Smem<8>::bytes; break;
   }
   if (threads) *threads = THREADS;
   if (smem) *smem = bytes;
