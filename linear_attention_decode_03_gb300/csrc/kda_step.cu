@@ -218,46 +218,77 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity)
   return true;
 }
 
-// z for one channel from this lane's four products (w . f): the fp32 sum over
-// the warp by a 5-level xor butterfly, correctly rounded to bf16.  Every lane
-// returns the same value.  The fp32 path carries run = the sum of |every
-// rounded intermediate|, so |z - exact| <= u (1 + 2u) run; within twice that
-// of a bf16 rounding boundary, the warp redoes the sum with TwoSum (exact
-// pairs hi + lo through the same butterfly) and rounds hi + lo once.
-__device__ __forceinline__ float z_channel(const float w[4], const float4 f) {
-  float p = w[0] * f.x;  // exact: bf16 x bf16
-  float run = 0.0f;
-  p = fmaf(w[1], f.y, p);
-  run += fabsf(p);
-  p = fmaf(w[2], f.z, p);
-  run += fabsf(p);
-  p = fmaf(w[3], f.w, p);
-  run += fabsf(p);
+// z for the warp's 16 channels, correctly rounded to bf16.  Lane l holds four
+// exact products (bf16 x bf16) of every channel in w[i] . f; a transposed
+// xor butterfly (reduce-scatter over lane bits 4..1, then a final xor-1 add)
+// leaves channel l >> 1 on lanes l and l ^ 1.  Each fp32 add carries run, the
+// sum of |every rounded intermediate| of that channel, so that
+// |z - exact| <= u (1 + 2u) run.  Channels whose bound straddles a bf16
+// rounding boundary are summed again exactly (TwoSum pairs hi + lo over the
+// whole warp) and rounded once; that decision is warp-uniform per channel.
+__device__ __forceinline__ float z_channels(const uint2 (&fbw)[Z_CHANNELS], const float4 f, int lane) {
+  float p[Z_CHANNELS], run[Z_CHANNELS];
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
-    p += __shfl_xor_sync(0xffffffffu, p, m);
-    run += __shfl_xor_sync(0xffffffffu, run, m);
-    run += fabsf(p);
+  for (int i = 0; i < Z_CHANNELS; ++i) {
+    const float w0 = __uint_as_float(fbw[i].x << 16), w1 = __uint_as_float(fbw[i].x & 0xffff0000u);
+    const float w2 = __uint_as_float(fbw[i].y << 16), w3 = __uint_as_float(fbw[i].y & 0xffff0000u);
+    float q = w0 * f.x;
+    q = fmaf(w1, f.y, q);
+    float rr = fabsf(q);
+    q = fmaf(w2, f.z, q);
+    rr += fabsf(q);
+    q = fmaf(w3, f.w, q);
+    rr += fabsf(q);
+    p[i] = q;
+    run[i] = rr;
   }
-  if (!bf16_rounding_uncertain(p, 2.0f * U32 * run)) return bf_round(p);
-  // exact pairs: a + b = s + e exactly (Knuth's TwoSum)
-  const float pr[4] = {w[0] * f.x, w[1] * f.y, w[2] * f.z, w[3] * f.w};
-  float hi = pr[0], lo = 0.0f;
+  // reduce-scatter: at offset m the lane keeps the upper or lower half of its channels
 #pragma unroll
-  for (int e = 1; e < 4; ++e) {
-    const float s = hi + pr[e], bp = s - hi;
-    lo += (hi - (s - bp)) + (pr[e] - bp);
-    hi = s;
-  }
+  for (int n = Z_CHANNELS, m = 16; n >= 2; n >>= 1, m >>= 1) {
+    const bool upper = (lane & m) != 0;
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
-    const float ho = __shfl_xor_sync(0xffffffffu, hi, m);
-    const float lo_o = __shfl_xor_sync(0xffffffffu, lo, m);
-    const float s = hi + ho, bp = s - hi;
-    lo = (lo + lo_o) + ((hi - (s - bp)) + (ho - bp));
-    hi = s;
+    for (int k = 0; k < n / 2; ++k) {
+      const float send = upper ? p[k] : p[k + n / 2], keep = upper ? p[k + n / 2] : p[k];
+      const float rsend = upper ? run[k] : run[k + n / 2], rkeep = upper ? run[k + n / 2] : run[k];
+      p[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+      run[k] = rkeep + __shfl_xor_sync(0xffffffffu, rsend, m) + fabsf(p[k]);
+    }
   }
-  return bf16_round_f64((double)hi + (double)lo);
+  float z = p[0] + __shfl_xor_sync(0xffffffffu, p[0], 1);
+  const float bound = 2.0f * U32 * (run[0] + __shfl_xor_sync(0xffffffffu, run[0], 1) + fabsf(z));
+  const bool unsure = bf16_rounding_uncertain(z, bound);
+  unsigned redo = __ballot_sync(0xffffffffu, unsure) & 0x55555555u;  // one bit per channel (even lanes)
+  z = bf_round(z);
+  while (redo) {
+    const int c = (__ffs(redo) - 1) >> 1;
+    redo &= redo - 1;
+    // exact pairs: a + b = s + e exactly (Knuth's TwoSum)
+    uint2 wc = fbw[0];  // row c, selected without indexing the register array
+#pragma unroll
+    for (int i = 1; i < Z_CHANNELS; ++i)
+      if (i == c) wc = fbw[i];
+    const float w0 = __uint_as_float(wc.x << 16), w1 = __uint_as_float(wc.x & 0xffff0000u);
+    const float w2 = __uint_as_float(wc.y << 16), w3 = __uint_as_float(wc.y & 0xffff0000u);
+    const float pr[4] = {w0 * f.x, w1 * f.y, w2 * f.z, w3 * f.w};
+    float hi = pr[0], lo = 0.0f;
+#pragma unroll
+    for (int e = 1; e < 4; ++e) {
+      const float s = hi + pr[e], bp = s - hi;
+      lo += (hi - (s - bp)) + (pr[e] - bp);
+      hi = s;
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      const float ho = __shfl_xor_sync(0xffffffffu, hi, m);
+      const float lo_o = __shfl_xor_sync(0xffffffffu, lo, m);
+      const float s = hi + ho, bp = s - hi;
+      lo = (lo + lo_o) + ((hi - (s - bp)) + (ho - bp));
+      hi = s;
+    }
+    const float exact = bf16_round_f64((double)hi + (double)lo);
+    if ((lane >> 1) == c) z = exact;
+  }
+  return z;  // channel lane >> 1
 }
 
 template <int L>
@@ -369,21 +400,14 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   {
     const float expA = expf(a.A_log[h]);
     const int c0 = warp * Z_CHANNELS;
-    const float dtc = (lane < Z_CHANNELS) ? a.dt_bias[h * HD + c0 + lane] : 0.0f;
+    const float dtc = a.dt_bias[h * HD + c0 + (lane >> 1)];
 #pragma unroll 1
     for (int t = 0; t < L; ++t) {
       const float4 f = *reinterpret_cast<const float4*>(fa_s + t * HD + lane * 4);
-      float zmine = 0.0f;
-#pragma unroll
-      for (int i = 0; i < Z_CHANNELS; ++i) {
-        const float wv[4] = {__uint_as_float(fbw[i].x << 16), __uint_as_float(fbw[i].x & 0xffff0000u),
-                             __uint_as_float(fbw[i].y << 16), __uint_as_float(fbw[i].y & 0xffff0000u)};
-        const float z = z_channel(wv, f);
-        if (lane == i) zmine = z;
-      }
-      if (lane < Z_CHANNELS) {
-        const float g = a.lb * sigmoidf_(expA * (zmine + dtc));
-        eg[t * HD + c0 + lane] = expf(g);
+      const float z = z_channels(fbw, f, lane);  // channel c0 + (lane >> 1)
+      if ((lane & 1) == 0) {
+        const float g = a.lb * sigmoidf_(expA * (z + dtc));
+        eg[t * HD + c0 + (lane >> 1)] = expf(g);
       }
     }
   }
