@@ -44,6 +44,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
 _LIB_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_LIB_DIR, "libkda_oracle.so")
+# A test that plants a mistake in the oracle (tests/test_oracle_mutations.py)
+# points this variable at a mutated build; nothing else sets it.
+_LIB_OVERRIDE = os.environ.get("KDA_ORACLE_LIB_OVERRIDE")
 _lib = None
 
 
@@ -65,7 +68,7 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
+        lib = ctypes.CDLL(_LIB_OVERRIDE or build())
         lib.kda_oracle_step.restype = ctypes.c_int
         lib.kda_oracle_bf16_round.restype = ctypes.c_uint16
         lib.kda_oracle_bf16_round.argtypes = [ctypes.c_double]

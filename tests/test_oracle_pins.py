@@ -319,6 +319,42 @@ def test_written_slots_padding_and_errors(run):
     assert np.all(out[2:] == 0) and np.any(out[:2] != 0)   # rows of requests 1..3 stay zero
 
 
+def test_column_split_per_head(run):
+    """The packed row: beta logits at 4D + 128 + h, one per head; q and k of
+    head h at blocks 0 and 1 (PreparedKda._operands column split)."""
+    si, pool, conv = _decode_case(heads=3, seed=24)
+    D, H = si.workload.dim, si.workload.heads
+    logits = [BF16_NEG_INF, BF16_POS_INF, np.uint16(0)]
+    for h in range(H):
+        si.projected[:, 4 * D + HEAD_DIM + h] = logits[h]
+    cw = np.zeros_like(si.weights.conv_w)
+    cw[:, 0, 3] = 0x3F80                                   # identity taps
+    *_, dg = run(oracle_weights(si, conv_w=cw), si.projected, conv, pool, si.slots, 1, None, act="none", diag=True)
+    assert np.array_equal(dg[:, :, -1], np.tile([0.0, 1.0, 0.5], (si.workload.rows, 1)))
+    for h in range(H):
+        xq = bf16_value(si.projected[:, head_cols(D, 0, h)])
+        xk = bf16_value(si.projected[:, head_cols(D, 1, h)])
+        qh, kh = dg[:, h, :HEAD_DIM], dg[:, h, HEAD_DIM:2 * HEAD_DIM]
+        np.testing.assert_allclose(qh, xq / np.linalg.norm(xq, axis=1, keepdims=True) * HEAD_DIM ** -0.5,
+                                   rtol=1e-6, atol=1e-9)
+        np.testing.assert_allclose(kh, xk / np.linalg.norm(xk, axis=1, keepdims=True), rtol=1e-6, atol=1e-9)
+
+
+def test_padding_alone_sets_no_error(run):
+    """A padding request (slot -1 first) is not an error: no error bits, zero
+    output rows, no cache written; the other requests run normally."""
+    R, L = 3, 2
+    si = case(heads=1, requests=R, L=L, pool=10, seed=25, accepted=[1, 2, 2])
+    slots = si.slots.reshape(R, L).copy()
+    slots[1, :] = -1
+    pool, conv = si.full_state_pool(), si.full_conv_state()
+    out, nconv, npool, err = run(oracle_weights(si), si.projected, conv, pool, slots.reshape(-1), L, si.accepted)
+    assert err == 0
+    assert np.all(out[L:2 * L] == 0) and np.all(out[:L] != 0) and np.all(out[2 * L:] != 0)
+    written = {s for s in range(10) if not np.array_equal(npool[s].view(np.uint32), pool[s].view(np.uint32))}
+    assert written == set(int(s) for s in slots[[0, 2]].reshape(-1))
+
+
 def test_c_matches_numpy_on_random_shapes():
     rng = np.random.default_rng(5)
     for trial in range(6):
