@@ -44,6 +44,56 @@ L2_BYTES = 129 * 1024 * 1024
 HEAD_DIM = 128
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kda_step_kernel_dram_traffic.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "linear_attention_decode_03_gb300", "csrc", "kda_step.cu"),
+                  os.path.join(ROOT, "include", "kda.h")]
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes (read + write) per launch that an ncu capture recorded for
+    this workload, or None when there is none or the kernel source changed
+    since (the summary stores the hash of the sources it was taken on)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    src_hash, per_wl = None, {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 2 and parts[0] == "source_sha256":
+                src_hash = parts[1]
+            elif len(parts) == 3 and parts[0] == "traffic":
+                per_wl[parts[1]] = int(parts[2])
+    if src_hash != kernel_source_hash():
+        return None
+    return per_wl.get(workload)
+
+
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise max of per-rank values (identity on one process)."""
+    if dist is None:
+        return list(values)
+    import torch
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(world: int, rows: int, steps: int, elapsed_ms: float) -> float:
+    """Tokens per second of all replicas, timed by the slowest rank."""
+    return world * rows * steps / (elapsed_ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -355,18 +405,14 @@ def main():
     if dw.prep.check() != 0:
         raise RuntimeError("device error bits set during the e2e steps")
 
-    # max over ranks
-    if dist is not None:
-        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dist, device)
 
     if rank != 0:
         dist.destroy_process_group()
         return
 
     ms_step = elapsed_ms / args.steps
-    tokens_per_s = world * w.rows * args.steps / (elapsed_ms / 1e3)
+    tokens_per_s = whole_job_rate(world, w.rows, args.steps, elapsed_ms)
     peak, peak_kind = load_peaks()
     achieved = all_b / (ms_step / 1e3) / 1e9
     state_gbs = state_b / (ms_step / 1e3) / 1e9
@@ -376,10 +422,10 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload_config(w, args),
         "state_gbs": state_gbs, "state_frac_of_peak": state_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "kda_step_kernel",
+                     "traffic": measured_traffic(w.name), "kernel": "kda_step_kernel",
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
-        "e2e": {"value": world * w.rows * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(world, w.rows, e2e_steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(t_host0, t_host1),
