@@ -14,16 +14,17 @@
 //   * round trip 1 (issued at entry, by every thread, with no dependence):
 //       the request's slots / accepted, this warp's 16 rows of the head's f_b
 //       (256 contiguous bytes a row, 8 bytes a lane), the f_a, out-gate and
-//       beta values, the q/k/v inputs and conv taps of the thread's channels.
+//       beta values, the q/k/v inputs, conv taps and bias of the thread's
+//       channels.
 //   * round trip 2 (once the slots are in): thread 0 validates them and puts
 //       the 64 KiB start state of (slot, head) in flight as four 16 KiB bulk
 //       async copies (cp.async.bulk, L2 evict-first) on four mbarriers; every
 //       thread loads the start conv windows of its channels.
-//   * while the state lands: z = f_b . f_a per warp (16 channels, 4 products
-//       a lane and a 5-level xor butterfly that also carries the fp32 error
-//       bound), the lower-bound gate and e^g; the causal conv of the q, k, v
-//       channels over the L tokens (window stores into slots[r, t]); one warp
-//       per token l2-normalises q and k and forms k^.q^ and beta.
+//   * while the state lands: the causal conv of the q, k, v channels over the
+//       L tokens (window stores into slots[r, t]); z = f_b . f_a per warp (16
+//       channels, 4 products a lane, a transposed xor butterfly over the warp,
+//       and a closed-form bound on its fp32 error), the lower-bound gate and
+//       e^g; one warp per token l2-normalises q and k and forms k^.q^ and beta.
 //   * recurrence: two passes over pairs of 32-row quarters of the state
 //       (rows = v; each pass waits on its two copies); a group of 8 lanes owns
 //       one v row of each quarter, 16 k values per lane in registers across
@@ -33,8 +34,8 @@
 // The bf16 hand-offs (conv outputs, z) are rounded correctly: each fp32 value
 // carries a bound on its error and is recomputed exactly (fp64, or a
 // compensated TwoSum butterfly) when the bound straddles a bf16 rounding
-// boundary.  Every wait is bounded (1 s of %globaltimer); a wait that gives up
-// sets KDA_ERR_TIMEOUT and the request's outputs are not written.
+// boundary.  Every wait is bounded (about 1 s of SM clock cycles); a wait that
+// gives up sets KDA_ERR_TIMEOUT and the request's outputs are not written.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -53,7 +54,7 @@ constexpr int STATE_BYTES = STATE_FLOATS * 4;  // 64 KiB
 constexpr int QUARTERS = 4;
 constexpr int QUARTER_ROWS = HD / QUARTERS;    // 32 v rows
 constexpr int QUARTER_BYTES = STATE_BYTES / QUARTERS;
-constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;
+constexpr long long WAIT_LIMIT_CYCLES = 2000000000ll;  // ~1 s at 2 GHz
 
 enum { TASK_OK = 0, TASK_PADDING = 1, TASK_SKIP = 2 };
 
@@ -69,6 +70,7 @@ struct StepArgs {
   const __nv_bfloat16* conv_w;  // prepared [3][W][D]
   const __nv_bfloat16* bias;    // [3D] or null
   const __nv_bfloat16* f_b;     // [D][128]
+  const float* fb_norm;         // [D] Euclidean norm of each f_b row, rounded up
   const float* A_log;           // [H]
   const float* dt_bias;         // [D]
   const float* o_norm;          // [128]
@@ -100,12 +102,6 @@ __device__ __forceinline__ float bf_round(float x) { return __bfloat162float(__f
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_timer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
@@ -167,6 +163,27 @@ __device__ __forceinline__ void store_streaming(float* p, float4 v) {
                : "memory");
 }
 
+// Packed fp32 pair arithmetic (two lanes of work per instruction on sm_100+),
+// with the operands passed as plain registers.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
@@ -208,68 +225,79 @@ __device__ __forceinline__ long long conv_index(const StepArgs& a, long long slo
 }
 
 
-// Wait for phase `parity` of an mbarrier, giving up after WAIT_LIMIT_NS.
+// Wait for phase `parity` of an mbarrier, giving up after WAIT_LIMIT_CYCLES SM
+// clock cycles (about a second; the SM cycle counter is far cheaper to read
+// than %globaltimer).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer();
+  const long long c0 = clock64();
   while (!mbar_try_wait_sleep(bar, parity)) {
-    if (global_timer() - t0 > WAIT_LIMIT_NS) return false;
+    if (clock64() - c0 > WAIT_LIMIT_CYCLES) return false;
   }
   return true;
 }
 
-// z for the warp's 16 channels, correctly rounded to bf16.  Lane l holds four
-// exact products (bf16 x bf16) of every channel in w[i] . f; a transposed
-// xor butterfly (reduce-scatter over lane bits 4..1, then a final xor-1 add)
-// leaves channel l >> 1 on lanes l and l ^ 1.  Each fp32 add carries run, the
-// sum of |every rounded intermediate| of that channel, so that
-// |z - exact| <= u (1 + 2u) run.  Channels whose bound straddles a bf16
-// rounding boundary are summed again exactly (TwoSum pairs hi + lo over the
-// whole warp) and rounded once; that decision is warp-uniform per channel.
-__device__ __forceinline__ float z_channels(const uint2 (&fbw)[Z_CHANNELS], const float4 f, int lane) {
-  float p[Z_CHANNELS], run[Z_CHANNELS];
+// z for the warp's 16 channels, correctly rounded to bf16.  Lane l holds, in
+// fbw[i], its four bf16 of the f_b row of channel i ^ m with m = (l >> 1) & 15,
+// and forms four exact products (bf16 x bf16) per channel.  A transposed xor
+// butterfly then halves the channel set at lane offsets 16, 8, 4, 2 -- with
+// that storage order every lane keeps the lower half of its array and sends
+// the upper half -- and a final xor-1 add leaves channel l >> 1 on lanes l and
+// l ^ 1.  Each channel's sum takes 3 roundings inside a lane and 5 tree
+// levels; the results of one level add up to at most sum|p_j| (1 + O(u)), so
+// |z - exact| <= 8 u (1 + O(u)) sum|p_j| <= 8 u (1 + O(u)) |f_b row|_2 |f_a|_2
+// (Cauchy-Schwarz).  `bound` is twice that, from upper bounds of the two
+// norms.  Channels whose bound straddles a bf16 rounding boundary are summed
+// again exactly (TwoSum pairs hi + lo over the whole warp) and rounded once;
+// that decision is warp-uniform per channel.
+__device__ __forceinline__ float z_channels(const uint2 (&fbw)[Z_CHANNELS], const float4 f, float bound, int lane) {
+  const float2 fx = make_float2(f.x, f.x), fy = make_float2(f.y, f.y);
+  const float2 fz = make_float2(f.z, f.z), fw = make_float2(f.w, f.w);
+  static_assert(Z_CHANNELS == 16, "the butterfly below is written out for 16 channels");
+  float p[Z_CHANNELS];
 #pragma unroll
-  for (int i = 0; i < Z_CHANNELS; ++i) {
-    const float w0 = __uint_as_float(fbw[i].x << 16), w1 = __uint_as_float(fbw[i].x & 0xffff0000u);
-    const float w2 = __uint_as_float(fbw[i].y << 16), w3 = __uint_as_float(fbw[i].y & 0xffff0000u);
-    float q = w0 * f.x;
-    q = fmaf(w1, f.y, q);
-    float rr = fabsf(q);
-    q = fmaf(w2, f.z, q);
-    rr += fabsf(q);
-    q = fmaf(w3, f.w, q);
-    rr += fabsf(q);
-    p[i] = q;
-    run[i] = rr;
+  for (int i = 0; i < Z_CHANNELS; i += 2) {
+    const uint2 a0 = fbw[i], a1 = fbw[i + 1];
+    const float2 w0 = make_float2(__uint_as_float(a0.x << 16), __uint_as_float(a1.x << 16));
+    const float2 w1 = make_float2(__uint_as_float(a0.x & 0xffff0000u), __uint_as_float(a1.x & 0xffff0000u));
+    const float2 w2 = make_float2(__uint_as_float(a0.y << 16), __uint_as_float(a1.y << 16));
+    const float2 w3 = make_float2(__uint_as_float(a0.y & 0xffff0000u), __uint_as_float(a1.y & 0xffff0000u));
+    float2 q = mul2(w0, fx);  // exact
+    q = fma2(w1, fy, q);
+    q = fma2(w2, fz, q);
+    q = fma2(w3, fw, q);
+    p[i] = q.x;
+    p[i + 1] = q.y;
   }
-  // reduce-scatter: at offset m the lane keeps the upper or lower half of its channels
 #pragma unroll
-  for (int n = Z_CHANNELS, m = 16; n >= 2; n >>= 1, m >>= 1) {
-    const bool upper = (lane & m) != 0;
+  for (int k = 0; k < 8; ++k) p[k] += __shfl_xor_sync(0xffffffffu, p[k + 8], 16);
 #pragma unroll
-    for (int k = 0; k < n / 2; ++k) {
-      const float send = upper ? p[k] : p[k + n / 2], keep = upper ? p[k + n / 2] : p[k];
-      const float rsend = upper ? run[k] : run[k + n / 2], rkeep = upper ? run[k + n / 2] : run[k];
-      p[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-      run[k] = rkeep + __shfl_xor_sync(0xffffffffu, rsend, m) + fabsf(p[k]);
-    }
-  }
+  for (int k = 0; k < 4; ++k) p[k] += __shfl_xor_sync(0xffffffffu, p[k + 4], 8);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) p[k] += __shfl_xor_sync(0xffffffffu, p[k + 2], 4);
+  p[0] += __shfl_xor_sync(0xffffffffu, p[1], 2);
   float z = p[0] + __shfl_xor_sync(0xffffffffu, p[0], 1);
-  const float bound = 2.0f * U32 * (run[0] + __shfl_xor_sync(0xffffffffu, run[0], 1) + fabsf(z));
   const bool unsure = bf16_rounding_uncertain(z, bound);
   unsigned redo = __ballot_sync(0xffffffffu, unsure) & 0x55555555u;  // one bit per channel (even lanes)
   z = bf_round(z);
+  const int mperm = (lane >> 1) & (Z_CHANNELS - 1);
   while (redo) {
     const int c = (__ffs(redo) - 1) >> 1;
     redo &= redo - 1;
-    // exact pairs: a + b = s + e exactly (Knuth's TwoSum)
-    uint2 wc = fbw[0];  // row c, selected without indexing the register array
+    // row of channel c: fbw[c ^ mperm], picked by masks so that the register
+    // array is never indexed at run time (that would move it to local memory)
+    const int idx = c ^ mperm;
+    uint2 wc = make_uint2(0u, 0u);
 #pragma unroll
-    for (int i = 1; i < Z_CHANNELS; ++i)
-      if (i == c) wc = fbw[i];
+    for (int i = 0; i < Z_CHANNELS; ++i) {
+      const unsigned msk = 0u - (unsigned)(i == idx);
+      wc.x |= fbw[i].x & msk;
+      wc.y |= fbw[i].y & msk;
+    }
     const float w0 = __uint_as_float(wc.x << 16), w1 = __uint_as_float(wc.x & 0xffff0000u);
     const float w2 = __uint_as_float(wc.y << 16), w3 = __uint_as_float(wc.y & 0xffff0000u);
     const float pr[4] = {w0 * f.x, w1 * f.y, w2 * f.z, w3 * f.w};
+    // exact pairs: a + b = s + e exactly (Knuth's TwoSum)
     float hi = pr[0], lo = 0.0f;
 #pragma unroll
     for (int e = 1; e < 4; ++e) {
@@ -321,10 +349,12 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   for (int t = 0; t < L; ++t) sl[t] = a.slots[row0 + t];
   const int acc = (a.accepted != nullptr) ? a.accepted[r] : 1;
   uint2 fbw[Z_CHANNELS];  // this lane's 4 bf16 of each of the warp's 16 f_b rows
+  const float fbn = a.fb_norm[h * HD + warp * Z_CHANNELS + (lane >> 1)];  // |f_b row|_2, rounded up
   {
     const uint2* fb = reinterpret_cast<const uint2*>(a.f_b + (long long)(h * HD + warp * Z_CHANNELS) * HD) + lane;
+    const int mperm = (lane >> 1) & (Z_CHANNELS - 1);  // storage order of z_channels
 #pragma unroll
-    for (int i = 0; i < Z_CHANNELS; ++i) fbw[i] = __ldg(fb + i * (HD / 4));
+    for (int i = 0; i < Z_CHANNELS; ++i) fbw[i] = __ldg(fb + (i ^ mperm) * (HD / 4));
   }
   // f_a and out-gate of the L tokens, two values a thread
   constexpr int PER_THREAD = (L * HD + THREADS - 1) / THREADS;
@@ -342,8 +372,25 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   float beta_logit = 0.0f;
   if (tid < L) beta_logit = bf(a.projected[(row0 + tid) * a.pitch + 4 * D + HD + h]);
 
+  // conv inputs of the thread's channels: job j in [0, 384) is channel j % 128
+  // of block j / 128 (q, k, v); thread tid takes jobs tid and tid + 256
+  constexpr int JOBS = (CONV_JOBS + THREADS - 1) / THREADS;  // 2
+  float x[JOBS][L], w[JOBS][4], b[JOBS];
+#pragma unroll
+  for (int jb = 0; jb < JOBS; ++jb) {
+    const int j = tid + jb * THREADS;
+    if (j < CONV_JOBS) {
+      const int blk = j / HD, c = j % HD, ch = blk * D + h * HD + c;
+#pragma unroll
+      for (int t = 0; t < L; ++t) x[jb][t] = bf(a.projected[(row0 + t) * a.pitch + ch]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w[jb][k] = (k < a.W) ? bf(a.conv_w[(long long)(blk * a.W + k) * D + h * HD + c]) : 0.0f;
+      b[jb] = a.bias ? bf(a.bias[ch]) : 0.0f;
+    }
+  }
+
   // ---- validate (every thread decides the same from the same loaded values) ---
-  int status = TASK_OK, start = sl[0];
+  int status = TASK_OK, start = 0;
   if (sl[0] == -1) {
     status = TASK_PADDING;
   } else if (acc < 1 || acc > L) {
@@ -354,7 +401,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
     for (int t = 0; t < L; ++t) {
       bad |= (sl[t] < 0) || (sl[t] >= a.pool);
-      if (t == acc - 1) start = sl[t];
+      start |= sl[t] & (0 - (int)(t == acc - 1));  // sl[acc - 1] without a run-time index
     }
     if (bad) {
       status = TASK_SKIP;
@@ -382,6 +429,17 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     }
     ctl[0] = 0;
   }
+  // the start conv windows of the thread's channels, in flight with the state
+  float win[JOBS][3];
+#pragma unroll
+  for (int jb = 0; jb < JOBS; ++jb) {
+    const int j = tid + jb * THREADS;
+    if (j < CONV_JOBS) {
+      const int ch = (j / HD) * D + h * HD + (j % HD);
+#pragma unroll
+      for (int k = 0; k < 3; ++k) win[jb][k] = (k < SL) ? bf(a.conv_state[conv_index(a, start, ch, k)]) : 0.0f;
+    }
+  }
 #pragma unroll
   for (int t = 0; t < L; ++t)
     if (tid == t) slot_s[t] = sl[t];
@@ -394,44 +452,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     }
   }
   if (tid < L) beta_s[tid] = sigmoidf_(beta_logit);
-  __syncthreads();  // barriers initialised, f_a staged
-
-  // ---- z = f_b . f_a (correctly rounded), lower-bound gate, e^g ---------------
-  {
-    const float expA = expf(a.A_log[h]);
-    const int c0 = warp * Z_CHANNELS;
-    const float dtc = a.dt_bias[h * HD + c0 + (lane >> 1)];
-#pragma unroll 1
-    for (int t = 0; t < L; ++t) {
-      const float4 f = *reinterpret_cast<const float4*>(fa_s + t * HD + lane * 4);
-      const float z = z_channels(fbw, f, lane);  // channel c0 + (lane >> 1)
-      if ((lane & 1) == 0) {
-        const float g = a.lb * sigmoidf_(expA * (z + dtc));
-        eg[t * HD + c0 + (lane >> 1)] = expf(g);
-      }
-    }
-  }
+  __syncthreads();  // barriers initialised, f_a and slots staged
 
   // ---- causal conv of the thread's channels (correctly rounded), window stores -
-  // Job j in [0, 384) is channel j % 128 of block j / 128 (q, k, v); thread tid
-  // takes jobs tid and tid + 256.  Its inputs are loaded only now, while the
-  // state copies are still landing, so they are not live during z.
-  constexpr int JOBS = (CONV_JOBS + THREADS - 1) / THREADS;  // 2
-  float x[JOBS][L], w[JOBS][4], b[JOBS], win[JOBS][3];
-#pragma unroll
-  for (int jb = 0; jb < JOBS; ++jb) {
-    const int j = tid + jb * THREADS;
-    if (j < CONV_JOBS) {
-      const int blk = j / HD, c = j % HD, ch = blk * D + h * HD + c;
-#pragma unroll
-      for (int t = 0; t < L; ++t) x[jb][t] = bf(a.projected[(row0 + t) * a.pitch + ch]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) w[jb][k] = (k < a.W) ? bf(a.conv_w[(long long)(blk * a.W + k) * D + h * HD + c]) : 0.0f;
-      b[jb] = a.bias ? bf(a.bias[ch]) : 0.0f;
-#pragma unroll
-      for (int k = 0; k < 3; ++k) win[jb][k] = (k < SL) ? bf(a.conv_state[conv_index(a, start, ch, k)]) : 0.0f;
-    }
-  }
+  // It runs before z: its inputs arrived with round trips 1 and 2, which the
+  // recurrence waits for anyway, and they are dead before z needs registers.
 #pragma unroll
   for (int jb = 0; jb < JOBS; ++jb) {
     const int j = tid + jb * THREADS;
@@ -479,6 +504,26 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         if (k < SL) a.conv_state[conv_index(a, dst, ch, k)] = __float2bfloat16_rn(win[jb][k]);
     }
   }
+  // ---- z = f_b . f_a (correctly rounded), lower-bound gate, e^g ---------------
+  {
+    const float expA = expf(a.A_log[h]);
+    const int c0 = warp * Z_CHANNELS;
+    const float dtc = a.dt_bias[h * HD + c0 + (lane >> 1)];
+#pragma unroll 1
+    for (int t = 0; t < L; ++t) {
+      const float4 f = *reinterpret_cast<const float4*>(fa_s + t * HD + lane * 4);
+      // |f_a|_2 of token t, rounded up: the fp32 sum of 128 squares is within
+      // 2^-17 relative of exact, the root within half an ulp
+      const float fnorm = sqrtf(warp_sum(f.x * f.x + f.y * f.y + f.z * f.z + f.w * f.w)) * (1.0f + 0x1p-12f);
+      const float bound = 16.0f * U32 * (1.0f + 0x1p-10f) * fbn * fnorm;
+      const float z = z_channels(fbw, f, bound, lane);  // channel c0 + (lane >> 1)
+      if ((lane & 1) == 0) {
+        const float g = a.lb * sigmoidf_(expA * (z + dtc));
+        eg[t * HD + c0 + (lane >> 1)] = expf(g);
+      }
+    }
+  }
+
   __syncthreads();  // raw q, k, v and e^g of every channel written
 
   // ---- l2norm of q and k, k^.q^: one warp per token -----------------------------
@@ -512,31 +557,46 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       timed_out = true;
       continue;
     }
-    float4 sv[2][4];
+    // two rows (one per quarter of the pass), 16 k values each as 8 float2 pairs
+    float2 sv[2][8];
 #pragma unroll
     for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        sv[qq][j] = *reinterpret_cast<const float4*>(st + ((2 * pass + qq) * QUARTER_ROWS + lr) * HD + j * 32 + kl * 4);
+      for (int j = 0; j < 4; ++j) {
+        const float4 x = *reinterpret_cast<const float4*>(st + ((2 * pass + qq) * QUARTER_ROWS + lr) * HD + j * 32 + kl * 4);
+        sv[qq][2 * j] = make_float2(x.x, x.y);
+        sv[qq][2 * j + 1] = make_float2(x.z, x.w);
+      }
 #pragma unroll 1
     for (int t = 0; t < L; ++t) {
-      float4 kv[4];
-      float dk[2] = {0.0f, 0.0f}, dq[2] = {0.0f, 0.0f};
+      float2 kv[8], dk2[2], dq2[2];
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) dk2[qq] = dq2[qq] = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int k0 = t * HD + j * 32 + kl * 4;
         const float4 e = *reinterpret_cast<const float4*>(eg + k0);
         const float4 qv = *reinterpret_cast<const float4*>(qh + k0);
-        kv[j] = *reinterpret_cast<const float4*>(kh + k0);
+        const float4 k4 = *reinterpret_cast<const float4*>(kh + k0);
+        const float2 e0 = make_float2(e.x, e.y), e1 = make_float2(e.z, e.w);
+        const float2 q0 = make_float2(qv.x, qv.y), q1 = make_float2(qv.z, qv.w);
+        kv[2 * j] = make_float2(k4.x, k4.y);
+        kv[2 * j + 1] = make_float2(k4.z, k4.w);
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
-          float4& s = sv[qq][j];
-          s.x *= e.x; s.y *= e.y; s.z *= e.z; s.w *= e.w;
-          dk[qq] = fmaf(s.x, kv[j].x, dk[qq]); dk[qq] = fmaf(s.y, kv[j].y, dk[qq]);
-          dk[qq] = fmaf(s.z, kv[j].z, dk[qq]); dk[qq] = fmaf(s.w, kv[j].w, dk[qq]);
-          dq[qq] = fmaf(s.x, qv.x, dq[qq]); dq[qq] = fmaf(s.y, qv.y, dq[qq]);
-          dq[qq] = fmaf(s.z, qv.z, dq[qq]); dq[qq] = fmaf(s.w, qv.w, dq[qq]);
+          sv[qq][2 * j] = mul2(sv[qq][2 * j], e0);  // S' = diag(e^g) S
+          sv[qq][2 * j + 1] = mul2(sv[qq][2 * j + 1], e1);
+          dk2[qq] = fma2(sv[qq][2 * j], kv[2 * j], dk2[qq]);
+          dk2[qq] = fma2(sv[qq][2 * j + 1], kv[2 * j + 1], dk2[qq]);
+          dq2[qq] = fma2(sv[qq][2 * j], q0, dq2[qq]);
+          dq2[qq] = fma2(sv[qq][2 * j + 1], q1, dq2[qq]);
         }
+      }
+      float dk[2], dq[2];
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        dk[qq] = dk2[qq].x + dk2[qq].y;
+        dq[qq] = dq2[qq].x + dq2[qq].y;
       }
 #pragma unroll
       for (int m = 1; m <= 4; m <<= 1)
@@ -553,12 +613,13 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         const float u = bf(vv[t * HD + v]) - dk[qq];
         const float bu = bt * u;
         const float o = fmaf(bu, kqt, dq[qq]);  // S_new^T q^ = S'^T q^ + beta u (k^.q^)
+        const float2 bu2 = make_float2(bu, bu);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float4& s = sv[qq][j];
-          s.x = fmaf(bu, kv[j].x, s.x); s.y = fmaf(bu, kv[j].y, s.y);
-          s.z = fmaf(bu, kv[j].z, s.z); s.w = fmaf(bu, kv[j].w, s.w);
-          store_streaming(dst + (2 * pass + qq) * QUARTER_ROWS * HD + j * 32, s);
+          sv[qq][2 * j] = fma2(bu2, kv[2 * j], sv[qq][2 * j]);  // S += beta k^ u^T
+          sv[qq][2 * j + 1] = fma2(bu2, kv[2 * j + 1], sv[qq][2 * j + 1]);
+          store_streaming(dst + (2 * pass + qq) * QUARTER_ROWS * HD + j * 32,
+                          make_float4(sv[qq][2 * j].x, sv[qq][2 * j].y, sv[qq][2 * j + 1].x, sv[qq][2 * j + 1].y));
         }
         if (kl == 0) ob[t * HD + v] = __float2bfloat16_rn(o);
       }
@@ -604,6 +665,18 @@ __global__ void relayout_conv_w(const __nv_bfloat16* in, __nv_bfloat16* out, int
   }
 }
 
+// Euclidean norm of each 128-wide bf16 row, in fp64, rounded up to fp32.
+__global__ void row_norms(const __nv_bfloat16* m, float* norms, int rows) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= rows) return;
+  double ss = 0.0;
+  for (int j = 0; j < HD; ++j) {
+    const double v = (double)__bfloat162float(m[(long long)i * HD + j]);
+    ss = fma(v, v, ss);
+  }
+  norms[i] = __double2float_ru(__dsqrt_ru(ss));
+}
+
 template <int L>
 cudaError_t set_smem_attr() {
   return cudaFuncSetAttribute(kda_step_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<L>::bytes);
@@ -640,6 +713,7 @@ struct kda_handle {
   __nv_bfloat16* conv_w;
   __nv_bfloat16* bias;
   __nv_bfloat16* f_b;
+  float* fb_norm;
   float* A_log;
   float* dt_bias;
   float* o_norm;
@@ -664,6 +738,7 @@ void kda_destroy(kda_handle* h) {
   cudaFree(h->conv_w);
   cudaFree(h->bias);
   cudaFree(h->f_b);
+  cudaFree(h->fb_norm);
   cudaFree(h->A_log);
   cudaFree(h->dt_bias);
   cudaFree(h->o_norm);
@@ -693,6 +768,7 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
   if (e == cudaSuccess) e = cudaMalloc(&h->conv_w, conv_bytes);
   if (e == cudaSuccess && bias) e = cudaMalloc(&h->bias, sizeof(__nv_bfloat16) * 3 * D);
   if (e == cudaSuccess) e = cudaMalloc(&h->f_b, sizeof(__nv_bfloat16) * D * HD);
+  if (e == cudaSuccess) e = cudaMalloc(&h->fb_norm, sizeof(float) * D);
   if (e == cudaSuccess) e = cudaMalloc(&h->A_log, sizeof(float) * heads);
   if (e == cudaSuccess) e = cudaMalloc(&h->dt_bias, sizeof(float) * D);
   if (e == cudaSuccess) e = cudaMalloc(&h->o_norm, sizeof(float) * HD);
@@ -709,6 +785,10 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
     e = cudaGetLastError();
   }
 
+  if (e == cudaSuccess) {
+    row_norms<<<(unsigned)((D + 255) / 256), 256>>>(h->f_b, h->fb_norm, (int)D);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = set_all_smem_attrs();
   if (e != cudaSuccess) {
@@ -746,6 +826,7 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
   a.conv_w = h->conv_w;
   a.bias = h->bias;
   a.f_b = h->f_b;
+  a.fb_norm = h->fb_norm;
   a.A_log = h->A_log;
   a.dt_bias = h->dt_bias;
   a.o_norm = h->o_norm;
