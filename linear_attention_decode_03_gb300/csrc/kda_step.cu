@@ -157,6 +157,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, unsigne
       : "memory");
 }
 
+// Bulk async shared -> global copy (one bulk group per call site commit).
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, unsigned bytes) {
+  unsigned long long policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+               "r"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void store_streaming(float* p, float4 v) {
   asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
                "f"(v.w)
@@ -217,6 +230,21 @@ __device__ __forceinline__ float bf16_round_f64(double x) {
   unsigned b = __float_as_uint(f);
   if ((double)f != x) b |= 1u;
   return __bfloat162float(__float2bfloat16_rn(__uint_as_float(b)));
+}
+
+// bf16 (ties to even) of hi + lo, an unevaluated fp32 pair.  TwoSum first
+// makes it s + e with s = fl(hi + lo) and |e| <= ulp(s) / 2.  Then s and s + e
+// round alike unless s is itself a bf16 midpoint: any other fp32 value is at
+// least one fp32 ulp from every midpoint, which e cannot cross.  At a midpoint
+// the sign of e picks the neighbour, and e = 0 leaves the tie to even.
+__device__ __forceinline__ float bf16_round_pair(float hi, float lo) {
+  const float s = hi + lo, bp = s - hi;
+  const float e = (hi - (s - bp)) + (lo - bp);
+  const unsigned a = __float_as_uint(s);
+  if ((a & 0xffffu) != 0x8000u || e == 0.0f) return bf_round(s);
+  const float down = __uint_as_float(a & 0xffff0000u);            // toward zero
+  const float up = __uint_as_float((a & 0xffff0000u) + 0x10000u);  // away from zero
+  return ((e > 0.0f) == (s > 0.0f)) ? up : down;
 }
 
 __device__ __forceinline__ long long conv_index(const StepArgs& a, long long slot, int ch, int j) {
@@ -313,7 +341,7 @@ __device__ __forceinline__ float z_channels(const uint2 (&fbw)[Z_CHANNELS], cons
       lo = (lo + lo_o) + ((hi - (s - bp)) + (ho - bp));
       hi = s;
     }
-    const float exact = bf16_round_f64((double)hi + (double)lo);
+    const float exact = bf16_round_pair(hi, lo);
     if ((lane >> 1) == c) z = exact;
   }
   return z;  // channel lane >> 1
@@ -553,10 +581,8 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   for (int pass = 0; pass < 2; ++pass) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mbar[2 * pass]), 0) &&
                                                 mbar_wait_bounded(smem_u32(&mbar[2 * pass + 1]), 0));
-    if (!ok) {
-      timed_out = true;
-      continue;
-    }
+    if (!ok) timed_out = true;
+    if (ok) {
     // two rows (one per quarter of the pass), 16 k values each as 8 float2 pairs
     float2 sv[2][8];
 #pragma unroll
@@ -618,10 +644,32 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         for (int j = 0; j < 4; ++j) {
           sv[qq][2 * j] = fma2(bu2, kv[2 * j], sv[qq][2 * j]);  // S += beta k^ u^T
           sv[qq][2 * j + 1] = fma2(bu2, kv[2 * j + 1], sv[qq][2 * j + 1]);
-          store_streaming(dst + (2 * pass + qq) * QUARTER_ROWS * HD + j * 32,
-                          make_float4(sv[qq][2 * j].x, sv[qq][2 * j].y, sv[qq][2 * j + 1].x, sv[qq][2 * j + 1].y));
+          const float4 row4 = make_float4(sv[qq][2 * j].x, sv[qq][2 * j].y, sv[qq][2 * j + 1].x, sv[qq][2 * j + 1].y);
+          if constexpr (L == 1) {
+            // decode: back into the shared-memory state; TMA stores the quarter
+            *reinterpret_cast<float4*>(st + ((2 * pass + qq) * QUARTER_ROWS + lr) * HD + j * 32 + kl * 4) = row4;
+          } else {
+            store_streaming(dst + (2 * pass + qq) * QUARTER_ROWS * HD + j * 32, row4);
+          }
         }
         if (kl == 0) ob[t * HD + v] = __float2bfloat16_rn(o);
+      }
+    }
+    }  // ok
+    if constexpr (L == 1) {
+      // Every thread reaches this barrier, timed out or not; the quarters go out
+      // only when no warp of the CTA timed out.
+      fence_proxy_async();  // this thread's shared-memory writes -> async proxy
+      if (timed_out && lane == 0) ctl[0] = 1;
+      __syncthreads();
+      if (tid == 0 && ctl[0] == 0) {
+        float* gdst = a.state_pool + ((long long)slot_s[0] * a.heads + h) * STATE_FLOATS;
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const int q = 2 * pass + qq;
+          bulk_store(gdst + q * QUARTER_ROWS * HD, smem_u32(st + q * QUARTER_ROWS * HD), QUARTER_BYTES);
+        }
+        bulk_commit();
       }
     }
   }
@@ -633,8 +681,10 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   if (ctl[0] != 0) {
     // Give copies still in flight a second bounded chance to land before the
     // shared memory is released; the outputs of this request stay unwritten.
-    if (tid == 0)
+    if (tid == 0) {
       for (int q = 0; q < QUARTERS; ++q) (void)mbar_wait_bounded(smem_u32(&mbar[q]), 0);
+      if constexpr (L == 1) bulk_wait_read();
+    }
     return;
   }
 
@@ -651,6 +701,9 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     for (int e = 0; e < 4; ++e)
       y[e] = __float2bfloat16_rn(o[e] * rstd * a.o_norm[lane * 4 + e] * sigmoidf_(bf(gate_s[t * HD + lane * 4 + e])));
     *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
+  }
+  if constexpr (L == 1) {
+    if (tid == 0) bulk_wait_read();  // shared memory stays until the bulk stores have read it
   }
 }
 
