@@ -288,7 +288,7 @@ def workload_config(w: I.Workload, args):
             "rows": w.rows, "pool_slots": w.pool, "conv_width": w.width, "state_bytes_per_step": state,
             "algorithmic_bytes_per_step": allb,
             "l2": ("inputs larger than L2 (%.0f MB of state per step)" % (state / 1e6)) if big
-            else "L2 flushed between timed steps (256 MiB write, outside the per-step events)",
+            else "L2 flushed between timed steps (256 MiB write, then 256 MiB read; outside the per-step events)",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
 
@@ -332,7 +332,11 @@ def main():
     dw = DeviceWorkload(si, device)
     state_b, all_b = algorithmic_bytes(w)
     flush = state_b <= L2_BYTES
+    # L2 flush between timed steps: write a buffer larger than L2, then read a
+    # second one so that the written lines are back in HBM (clean) before the
+    # step starts instead of being written back during it
     scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device) if flush else None
+    scratch_rd = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device) if flush else None
     stream = torch.cuda.current_stream(device)
 
     def barrier():
@@ -355,6 +359,7 @@ def main():
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         for i in range(args.steps):
             scratch.fill_(float(i))
+            scratch_rd.sum()
             starts[i].record(stream)
             dw.step()
             ends[i].record(stream)

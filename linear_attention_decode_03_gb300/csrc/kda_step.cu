@@ -48,7 +48,6 @@ constexpr int HD = 128;                        // head dim (k and v)
 constexpr int THREADS = 256;                   // 8 warps
 constexpr int WARPS = THREADS / 32;
 constexpr int Z_CHANNELS = HD / WARPS;         // 16 decay channels a warp
-constexpr int CONV_JOBS = 3 * HD;              // q, k, v channels of the head
 constexpr int STATE_FLOATS = HD * HD;          // one (slot, head) state
 constexpr int STATE_BYTES = STATE_FLOATS * 4;  // 64 KiB
 constexpr int QUARTERS = 4;
@@ -86,10 +85,11 @@ struct Smem {
   static constexpr int eg = state + STATE_BYTES;      // float [L][128]    e^g
   static constexpr int kh = eg + L * HD * 4;          // float [L][128]    k, then k^
   static constexpr int qh = kh + L * HD * 4;          // float [L][128]    q, then q^
-  static constexpr int fa = qh + L * HD * 4;          // float [L][128]    f_a; later bf16 o
-  static constexpr int vv = fa + L * HD * 4;          // bf16  [L][128]    v
+  static constexpr int fa = qh + L * HD * 4;          // bf16  [L][128]    f_a; later o
+  static constexpr int vv = fa + L * HD * 2;          // bf16  [L][128]    v
   static constexpr int gate = vv + L * HD * 2;        // bf16  [L][128]    out-gate
-  static constexpr int beta = gate + L * HD * 2;      // float [L]
+  static constexpr int fnp = gate + L * HD * 2;       // float [L][4]      partial sums of f_a^2
+  static constexpr int beta = fnp + 16 * L;           // float [L]
   static constexpr int kq = beta + 4 * L;             // float [L]         k^.q^
   static constexpr int slot = kq + 4 * L;             // int   [L]         slots[r, t]
   static constexpr int ctl = slot + 4 * L;            // int   [2]         timeout flag
@@ -265,86 +265,168 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity)
   return true;
 }
 
-// z for the warp's 16 channels, correctly rounded to bf16.  Lane l holds, in
-// fbw[i], its four bf16 of the f_b row of channel i ^ m with m = (l >> 1) & 15,
-// and forms four exact products (bf16 x bf16) per channel.  A transposed xor
-// butterfly then halves the channel set at lane offsets 16, 8, 4, 2 -- with
-// that storage order every lane keeps the lower half of its array and sends
-// the upper half -- and a final xor-1 add leaves channel l >> 1 on lanes l and
-// l ^ 1.  Each channel's sum takes 3 roundings inside a lane and 5 tree
-// levels; the results of one level add up to at most sum|p_j| (1 + O(u)), so
-// |z - exact| <= 8 u (1 + O(u)) sum|p_j| <= 8 u (1 + O(u)) |f_b row|_2 |f_a|_2
-// (Cauchy-Schwarz).  `bound` is twice that, from upper bounds of the two
-// norms.  Channels whose bound straddles a bf16 rounding boundary are summed
-// again exactly (TwoSum pairs hi + lo over the whole warp) and rounded once;
-// that decision is warp-uniform per channel.
-__device__ __forceinline__ float z_channels(const uint2 (&fbw)[Z_CHANNELS], const float4 f, float bound, int lane) {
-  const float2 fx = make_float2(f.x, f.x), fy = make_float2(f.y, f.y);
-  const float2 fz = make_float2(f.z, f.z), fw = make_float2(f.w, f.w);
-  static_assert(Z_CHANNELS == 16, "the butterfly below is written out for 16 channels");
-  float p[Z_CHANNELS];
+// Mixed-precision fused multiply-adds (sm_100+): bf16 operands, fp32 sum.
+// The bf16 x bf16 product is exact in fp32, so each call rounds once, as
+// fmaf on the widened operands would, without converting them first.
+__device__ __forceinline__ void fma_bf16_pair(unsigned a, unsigned b, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(a), "r"(b));
+}
+// As above for one product, the operands picked from halves AH / BH of packed words.
+template <int AH, int BH>
+__device__ __forceinline__ float fma_bf16(unsigned a, unsigned b, float c) {
+  if constexpr (AH == 0 && BH == 0)
+    asm("{\n\t.reg .b16 x0, x1, y0, y1;\n\tmov.b32 {x0, x1}, %1;\n\tmov.b32 {y0, y1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, x0, y0, %0;\n\t}" : "+f"(c) : "r"(a), "r"(b));
+  else if constexpr (AH == 0 && BH == 1)
+    asm("{\n\t.reg .b16 x0, x1, y0, y1;\n\tmov.b32 {x0, x1}, %1;\n\tmov.b32 {y0, y1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, x0, y1, %0;\n\t}" : "+f"(c) : "r"(a), "r"(b));
+  else if constexpr (AH == 1 && BH == 0)
+    asm("{\n\t.reg .b16 x0, x1, y0, y1;\n\tmov.b32 {x0, x1}, %1;\n\tmov.b32 {y0, y1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, x1, y0, %0;\n\t}" : "+f"(c) : "r"(a), "r"(b));
+  else
+    asm("{\n\t.reg .b16 x0, x1, y0, y1;\n\tmov.b32 {x0, x1}, %1;\n\tmov.b32 {y0, y1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, x1, y1, %0;\n\t}" : "+f"(c) : "r"(a), "r"(b));
+  return c;
+}
+__device__ __forceinline__ float bf_bits(unsigned short x) { return __uint_as_float((unsigned)x << 16); }
+__device__ __forceinline__ float bf_lo(unsigned w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ---- z = f_b . f_a ------------------------------------------------------------
+// Lane l of warp w: group g = l >> 3 owns channels 16 w + 4 g + r (r = 0..3),
+// kl = l & 7 owns k = 64 m + 8 kl + (0..7) (m = 0, 1); fbw[r][m] holds those
+// 8 bf16 of the f_b row of channel r.  The lane sums the 16 exact products of
+// each channel in two fp32 chains (even / odd k) and adds them; a reduce-
+// scatter over the group's 8 lanes (offsets 4 and 2) and a full add at offset
+// 1 leave channel row (l >> 1) & 3 on lanes l and l ^ 1.  No product passes
+// more than 8 roundings in the lane and 3 in the tree, so
+//   |z - exact| <= gamma_11 sum|p_j| <= 11 u (1 + 2^-10) |f_b row|_2 |f_a|_2
+// (Cauchy-Schwarz, u = 2^-24); the bound used is 12 u (1 + 2^-10) times upper
+// bounds of the two norms.
+__device__ __forceinline__ void z_partials(const uint4 (&fbw)[4][2], const uint4 f0, const uint4 f1, float (&acc)[4]) {
 #pragma unroll
-  for (int i = 0; i < Z_CHANNELS; i += 2) {
-    const uint2 a0 = fbw[i], a1 = fbw[i + 1];
-    const float2 w0 = make_float2(__uint_as_float(a0.x << 16), __uint_as_float(a1.x << 16));
-    const float2 w1 = make_float2(__uint_as_float(a0.x & 0xffff0000u), __uint_as_float(a1.x & 0xffff0000u));
-    const float2 w2 = make_float2(__uint_as_float(a0.y << 16), __uint_as_float(a1.y << 16));
-    const float2 w3 = make_float2(__uint_as_float(a0.y & 0xffff0000u), __uint_as_float(a1.y & 0xffff0000u));
-    float2 q = mul2(w0, fx);  // exact
-    q = fma2(w1, fy, q);
-    q = fma2(w2, fz, q);
-    q = fma2(w3, fw, q);
-    p[i] = q.x;
-    p[i + 1] = q.y;
+  for (int r = 0; r < 4; ++r) {
+    float lo = 0.0f, hi = 0.0f;
+    fma_bf16_pair(fbw[r][0].x, f0.x, lo, hi);
+    fma_bf16_pair(fbw[r][0].y, f0.y, lo, hi);
+    fma_bf16_pair(fbw[r][0].z, f0.z, lo, hi);
+    fma_bf16_pair(fbw[r][0].w, f0.w, lo, hi);
+    fma_bf16_pair(fbw[r][1].x, f1.x, lo, hi);
+    fma_bf16_pair(fbw[r][1].y, f1.y, lo, hi);
+    fma_bf16_pair(fbw[r][1].z, f1.z, lo, hi);
+    fma_bf16_pair(fbw[r][1].w, f1.w, lo, hi);
+    acc[r] = lo + hi;
+  }
+}
+
+__device__ __forceinline__ float z_reduce(const float (&acc)[4], int lane) {
+  const bool b2 = (lane & 4) != 0, b1 = (lane & 2) != 0;
+  float k0 = b2 ? acc[2] : acc[0], k1 = b2 ? acc[3] : acc[1];
+  const float s0 = b2 ? acc[0] : acc[2], s1 = b2 ? acc[1] : acc[3];
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 4);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 4);
+  float r = b1 ? k1 : k0;
+  const float s = b1 ? k0 : k1;
+  r += __shfl_xor_sync(0xffffffffu, s, 2);
+  return r + __shfl_xor_sync(0xffffffffu, r, 1);
+}
+
+// z of one channel row of each lane group (the lane's 16 bf16 of it in w0, w1,
+// of f_a in f0, f1), from its exact products summed as TwoSum pairs (Knuth)
+// in the lane and across the group's 8 lanes; the pair hi + lo then rounds to
+// the correctly rounded bf16 of z.  Every lane of the warp calls it together.
+__device__ __forceinline__ float z_exact(const uint4 w0, const uint4 w1, const uint4 f0, const uint4 f1) {
+  const unsigned w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  const unsigned fv[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+  float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float p = (j & 1) ? bf_hi(w[j >> 1]) * bf_hi(fv[j >> 1]) : bf_lo(w[j >> 1]) * bf_lo(fv[j >> 1]);
+    const float s = hi + p, bp = s - hi;
+    lo += (hi - (s - bp)) + (p - bp);
+    hi = s;
   }
 #pragma unroll
-  for (int k = 0; k < 8; ++k) p[k] += __shfl_xor_sync(0xffffffffu, p[k + 8], 16);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) p[k] += __shfl_xor_sync(0xffffffffu, p[k + 4], 8);
-#pragma unroll
-  for (int k = 0; k < 2; ++k) p[k] += __shfl_xor_sync(0xffffffffu, p[k + 2], 4);
-  p[0] += __shfl_xor_sync(0xffffffffu, p[1], 2);
-  float z = p[0] + __shfl_xor_sync(0xffffffffu, p[0], 1);
-  const bool unsure = bf16_rounding_uncertain(z, bound);
-  unsigned redo = __ballot_sync(0xffffffffu, unsure) & 0x55555555u;  // one bit per channel (even lanes)
-  z = bf_round(z);
-  const int mperm = (lane >> 1) & (Z_CHANNELS - 1);
-  while (redo) {
-    const int c = (__ffs(redo) - 1) >> 1;
-    redo &= redo - 1;
-    // row of channel c: fbw[c ^ mperm], picked by masks so that the register
-    // array is never indexed at run time (that would move it to local memory)
-    const int idx = c ^ mperm;
-    uint2 wc = make_uint2(0u, 0u);
-#pragma unroll
-    for (int i = 0; i < Z_CHANNELS; ++i) {
-      const unsigned msk = 0u - (unsigned)(i == idx);
-      wc.x |= fbw[i].x & msk;
-      wc.y |= fbw[i].y & msk;
-    }
-    const float w0 = __uint_as_float(wc.x << 16), w1 = __uint_as_float(wc.x & 0xffff0000u);
-    const float w2 = __uint_as_float(wc.y << 16), w3 = __uint_as_float(wc.y & 0xffff0000u);
-    const float pr[4] = {w0 * f.x, w1 * f.y, w2 * f.z, w3 * f.w};
-    // exact pairs: a + b = s + e exactly (Knuth's TwoSum)
-    float hi = pr[0], lo = 0.0f;
-#pragma unroll
-    for (int e = 1; e < 4; ++e) {
-      const float s = hi + pr[e], bp = s - hi;
-      lo += (hi - (s - bp)) + (pr[e] - bp);
-      hi = s;
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-      const float ho = __shfl_xor_sync(0xffffffffu, hi, m);
-      const float lo_o = __shfl_xor_sync(0xffffffffu, lo, m);
-      const float s = hi + ho, bp = s - hi;
-      lo = (lo + lo_o) + ((hi - (s - bp)) + (ho - bp));
-      hi = s;
-    }
-    const float exact = bf16_round_pair(hi, lo);
-    if ((lane >> 1) == c) z = exact;
+  for (int m = 1; m <= 4; m <<= 1) {
+    const float ho = __shfl_xor_sync(0xffffffffu, hi, m);
+    const float lo_o = __shfl_xor_sync(0xffffffffu, lo, m);
+    const float s = hi + ho, bp = s - hi;
+    lo = (lo + lo_o) + ((hi - (s - bp)) + (ho - bp));
+    hi = s;
   }
-  return z;  // channel lane >> 1
+  return bf16_round_pair(hi, lo);
+}
+
+// Row rs of fbw, picked by masks so that fbw is never indexed at run time (that
+// would move it to local memory).
+__device__ __forceinline__ void fb_row(const uint4 (&fbw)[4][2], int rs, uint4& w0, uint4& w1) {
+  w0 = w1 = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const unsigned msk = 0u - (unsigned)(r == rs);
+    w0.x |= fbw[r][0].x & msk; w0.y |= fbw[r][0].y & msk; w0.z |= fbw[r][0].z & msk; w0.w |= fbw[r][0].w & msk;
+    w1.x |= fbw[r][1].x & msk; w1.y |= fbw[r][1].y & msk; w1.z |= fbw[r][1].z & msk; w1.w |= fbw[r][1].w & msk;
+  }
+}
+
+// ---- causal conv ----------------------------------------------------------------
+// bf16 of SiLU(b + sum_k w_k s_k) from fp64 (exact products and sums of four
+// bf16 pairs; the SiLU's own fp64 error is far below a bf16 half ulp):
+// the rare path taken when the fp32 value is too close to a rounding boundary.
+__device__ __forceinline__ float silu_bf16_exact(float b, unsigned wp0, unsigned wp1, unsigned s01, unsigned s23) {
+  double y = (double)b;
+  y = fma((double)bf_lo(wp0), (double)bf_lo(s01), y);
+  y = fma((double)bf_hi(wp0), (double)bf_hi(s01), y);
+  y = fma((double)bf_lo(wp1), (double)bf_lo(s23), y);
+  y = fma((double)bf_hi(wp1), (double)bf_hi(s23), y);
+  return bf16_round_f64(y / (1.0 + exp(-y)));
+}
+// The same out of line: with many tokens the unrolled conv is long enough for
+// instruction fetch to matter, and the rare path is better kept out of it.
+__device__ __noinline__ float silu_bf16_exact_ool(float b, unsigned wp0, unsigned wp1, unsigned s01, unsigned s23) {
+  return silu_bf16_exact(b, wp0, wp1, s01, s23);
+}
+
+// One channel over up to N tokens [t0, t0 + n): position p of the channel's
+// input sequence is window slot p - (3 - SL) for p < 3 (the window right-
+// aligned) and x_{p-3} from p = 3 on; taps are right-aligned in w[0..4) (zero
+// taps in front when W < 4), so that y_t = b + sum_k w[k] seq(t + k).  The
+// lane holds positions t0 .. t0 + N + 2 as raw bf16 bits, two to a word.
+template <int N>
+struct ConvLane {
+  static constexpr int WORDS = (N + 4) / 2;
+  unsigned sp[WORDS];  // position t0 + i in half i & 1 of word i >> 1
+  unsigned wp[2];      // taps, w[k] in half k & 1 of word k >> 1
+  float b;
+  __device__ __forceinline__ void set(int i, unsigned short v) {  // i compile-time after unrolling
+    sp[i >> 1] = (i & 1) ? ((sp[i >> 1] & 0xffffu) | ((unsigned)v << 16)) : ((sp[i >> 1] & 0xffff0000u) | v);
+  }
+  __device__ __forceinline__ unsigned short get(int i) const {
+    return (unsigned short)((i & 1) ? (sp[i >> 1] >> 16) : (sp[i >> 1] & 0xffffu));
+  }
+  __device__ __forceinline__ unsigned short tap(int k) const {
+    return (unsigned short)((k & 1) ? (wp[k >> 1] >> 16) : (wp[k >> 1] & 0xffffu));
+  }
+};
+
+// y = b + sum_k w[k] seq(i + k) for the lane's token i, each step rounded
+// once; run collects |partial sums| (the fp32 error bound / u).
+template <int I, int N>
+__device__ __forceinline__ float conv_dot(const ConvLane<N>& q, float& run) {
+  float y = q.b;
+  y = fma_bf16<0, (I & 1)>(q.wp[0], q.sp[I >> 1], y);
+  run = fabsf(y);
+  y = fma_bf16<1, ((I + 1) & 1)>(q.wp[0], q.sp[(I + 1) >> 1], y);
+  run += fabsf(y);
+  y = fma_bf16<0, ((I + 2) & 1)>(q.wp[1], q.sp[(I + 2) >> 1], y);
+  run += fabsf(y);
+  y = fma_bf16<1, ((I + 3) & 1)>(q.wp[1], q.sp[(I + 3) >> 1], y);
+  run += fabsf(y);
+  return y;
 }
 
 template <int L>
@@ -355,10 +437,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   float* eg = reinterpret_cast<float*>(smem + S::eg);
   float* kh = reinterpret_cast<float*>(smem + S::kh);
   float* qh = reinterpret_cast<float*>(smem + S::qh);
-  float* fa_s = reinterpret_cast<float*>(smem + S::fa);
+  unsigned short* fa_b = reinterpret_cast<unsigned short*>(smem + S::fa);
   __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(smem + S::fa);  // reuses the f_a space
   __nv_bfloat16* vv = reinterpret_cast<__nv_bfloat16*>(smem + S::vv);
   __nv_bfloat16* gate_s = reinterpret_cast<__nv_bfloat16*>(smem + S::gate);
+  float* fnp = reinterpret_cast<float*>(smem + S::fnp);
   float* beta_s = reinterpret_cast<float*>(smem + S::beta);
   float* kq_s = reinterpret_cast<float*>(smem + S::kq);
   int* slot_s = reinterpret_cast<int*>(smem + S::slot);
@@ -376,17 +459,22 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
   for (int t = 0; t < L; ++t) sl[t] = a.slots[row0 + t];
   const int acc = (a.accepted != nullptr) ? a.accepted[r] : 1;
-  uint2 fbw[Z_CHANNELS];  // this lane's 4 bf16 of each of the warp's 16 f_b rows
-  const float fbn = a.fb_norm[h * HD + warp * Z_CHANNELS + (lane >> 1)];  // |f_b row|_2, rounded up
+  // z operands of the lane's 4 channels (see z_partials)
+  const int zc = warp * Z_CHANNELS + (lane >> 3) * 4 + ((lane >> 1) & 3);  // channel of the lane's z
+  uint4 fbw[4][2];
   {
-    const uint2* fb = reinterpret_cast<const uint2*>(a.f_b + (long long)(h * HD + warp * Z_CHANNELS) * HD) + lane;
-    const int mperm = (lane >> 1) & (Z_CHANNELS - 1);  // storage order of z_channels
+    const uint4* fb = reinterpret_cast<const uint4*>(a.f_b + (long long)(h * HD + warp * Z_CHANNELS + (lane >> 3) * 4) * HD);
 #pragma unroll
-    for (int i = 0; i < Z_CHANNELS; ++i) fbw[i] = __ldg(fb + (i ^ mperm) * (HD / 4));
+    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+      for (int m = 0; m < 2; ++m) fbw[rr][m] = __ldg(fb + rr * (HD / 8) + m * 8 + (lane & 7));
   }
-  // f_a and out-gate of the L tokens, two values a thread
+  const float fbn = a.fb_norm[h * HD + zc];  // |f_b row|_2, rounded up
+  const float dtc = a.dt_bias[h * HD + zc];
+  const float a_log = a.A_log[h];
+  // f_a and out-gate of the L tokens, raw bf16
   constexpr int PER_THREAD = (L * HD + THREADS - 1) / THREADS;
-  unsigned short fa_v[PER_THREAD], gate_v[PER_THREAD];  // raw bf16 bits
+  unsigned short fa_v[PER_THREAD], gate_v[PER_THREAD];
 #pragma unroll
   for (int i = 0; i < PER_THREAD; ++i) {
     const int e = tid + i * THREADS;
@@ -400,21 +488,40 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   float beta_logit = 0.0f;
   if (tid < L) beta_logit = bf(a.projected[(row0 + tid) * a.pitch + 4 * D + HD + h]);
 
-  // conv inputs of the thread's channels: job j in [0, 384) is channel j % 128
-  // of block j / 128 (q, k, v); thread tid takes jobs tid and tid + 256
-  constexpr int JOBS = (CONV_JOBS + THREADS - 1) / THREADS;  // 2
-  float x[JOBS][L], w[JOBS][4], b[JOBS];
+  // conv work: channel c of the head; the first half of the CTA takes q and k
+  // over tokens [0, A) and v over [0, B), the second half q and k over [A, L)
+  // and v over [B, L) (A = ceil(L/2), B = floor(L/2)): 1.5 L outputs a thread
+  // for even L.
+  constexpr int CA = (L + 1) / 2, CB = L / 2;
+  const int c = tid & (HD - 1);
+  const bool second = tid >= HD;
+  // first token and token count of kind 0, 1 (q, k) and 2 (v)
+  auto conv_t0 = [&](int kind) { return (kind < 2) ? (second ? CA : 0) : (second ? CB : 0); };
+  auto conv_n = [&](int kind) { return (kind < 2) ? (second ? L - CA : CA) : (second ? L - CB : CB); };
+  const unsigned short* proj16 = reinterpret_cast<const unsigned short*>(a.projected);
+  ConvLane<CA> cv[3];
 #pragma unroll
-  for (int jb = 0; jb < JOBS; ++jb) {
-    const int j = tid + jb * THREADS;
-    if (j < CONV_JOBS) {
-      const int blk = j / HD, c = j % HD, ch = blk * D + h * HD + c;
+  for (int kind = 0; kind < 3; ++kind) {
+    ConvLane<CA>& q = cv[kind];
+    const int t0 = conv_t0(kind), n = conv_n(kind);
+    const int ch = kind * D + h * HD + c;
 #pragma unroll
-      for (int t = 0; t < L; ++t) x[jb][t] = bf(a.projected[(row0 + t) * a.pitch + ch]);
+    for (int w = 0; w < ConvLane<CA>::WORDS; ++w) q.sp[w] = 0u;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) w[jb][k] = (k < a.W) ? bf(a.conv_w[(long long)(blk * a.W + k) * D + h * HD + c]) : 0.0f;
-      b[jb] = a.bias ? bf(a.bias[ch]) : 0.0f;
+    for (int i = 0; i < CA + 3; ++i) {
+      const int t = t0 + i - 3;  // token whose x sits at position t0 + i
+      if (t >= 0 && t < L && i < n + 3) q.set(i, proj16[(row0 + t) * a.pitch + ch]);
     }
+    const unsigned short* cw = reinterpret_cast<const unsigned short*>(a.conv_w) + (long long)kind * a.W * D + h * HD + c;
+    unsigned short w4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = k - (3 - SL);  // tap index, right-aligned
+      w4[k] = (j >= 0) ? cw[(long long)j * D] : (unsigned short)0;
+    }
+    q.wp[0] = w4[0] | ((unsigned)w4[1] << 16);
+    q.wp[1] = w4[2] | ((unsigned)w4[3] << 16);
+    q.b = a.bias ? bf(a.bias[ch]) : 0.0f;
   }
 
   // ---- validate (every thread decides the same from the same loaded values) ---
@@ -457,15 +564,17 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     }
     ctl[0] = 0;
   }
-  // the start conv windows of the thread's channels, in flight with the state
-  float win[JOBS][3];
+  // window values at seq positions < 3 (window slot j = position - (3 - SL))
 #pragma unroll
-  for (int jb = 0; jb < JOBS; ++jb) {
-    const int j = tid + jb * THREADS;
-    if (j < CONV_JOBS) {
-      const int ch = (j / HD) * D + h * HD + (j % HD);
+  for (int kind = 0; kind < 3; ++kind) {
+    ConvLane<CA>& q = cv[kind];
+    const int t0 = conv_t0(kind), n = conv_n(kind);
+    const int ch = kind * D + h * HD + c;
 #pragma unroll
-      for (int k = 0; k < 3; ++k) win[jb][k] = (k < SL) ? bf(a.conv_state[conv_index(a, start, ch, k)]) : 0.0f;
+    for (int i = 0; i < 3; ++i) {
+      const int j = t0 + i - (3 - SL);
+      if (t0 + i < 3 && j >= 0 && n > 0)
+        q.set(i, reinterpret_cast<const unsigned short*>(a.conv_state)[conv_index(a, start, ch, j)]);
     }
   }
 #pragma unroll
@@ -474,80 +583,109 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
   for (int i = 0; i < PER_THREAD; ++i) {
     const int e = tid + i * THREADS;
-    if (e < L * HD) {
-      fa_s[e] = __uint_as_float((unsigned)fa_v[i] << 16);
+    if ((tid & ~31) + i * THREADS < L * HD) {  // warp-uniform
+      fa_b[e] = fa_v[i];
       reinterpret_cast<unsigned short*>(gate_s)[e] = gate_v[i];
+      // squares of f_a: one partial sum per (token, 32 channels)
+      const float f = bf_bits(fa_v[i]);
+      const float sq = warp_sum(f * f);
+      if (lane == 0) fnp[(e / HD) * 4 + (e % HD) / 32] = sq;
     }
   }
   if (tid < L) beta_s[tid] = sigmoidf_(beta_logit);
-  __syncthreads();  // barriers initialised, f_a and slots staged
+  __syncthreads();  // barriers initialised, f_a, its squares and the slots staged
 
   // ---- causal conv of the thread's channels (correctly rounded), window stores -
   // It runs before z: its inputs arrived with round trips 1 and 2, which the
   // recurrence waits for anyway, and they are dead before z needs registers.
+  {
+    const long long C3 = 3LL * D;
 #pragma unroll
-  for (int jb = 0; jb < JOBS; ++jb) {
-    const int j = tid + jb * THREADS;
-    if (j >= CONV_JOBS) continue;
-    const int blk = j / HD, c = j % HD, ch = blk * D + h * HD + c;
-    float wcur = 0.0f;  // the tap on the current token, w[SL]
+    for (int kind = 0; kind < 3; ++kind) {
+      const ConvLane<CA>& q = cv[kind];
+      const int t0 = conv_t0(kind), n = conv_n(kind);
+      const int ch = kind * D + h * HD + c;
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (k == SL) wcur = w[jb][k];
-#pragma unroll
-    for (int t = 0; t < L; ++t) {
-      const float xt = x[jb][t];
-      float y = b[jb], run = 0.0f;  // run: sum of |partial sums|, the fp32 error bound / u
-#pragma unroll
-      for (int k = 0; k < 3; ++k)
-        if (k < SL) {
-          y = fmaf(w[jb][k], win[jb][k], y);
-          run += fabsf(y);
+      for (int i = 0; i < CA; ++i) {
+        if (i >= n) continue;
+        const int t = t0 + i;
+        float run;  // sum of |partial sums|, the fp32 error bound / u
+        float y;
+        switch (i) {  // compile-time after unrolling
+          case 0: y = conv_dot<0>(q, run); break;
+          case 1: y = conv_dot<1>(q, run); break;
+          case 2: y = conv_dot<2>(q, run); break;
+          default: y = conv_dot<3>(q, run); break;
         }
-      y = fmaf(wcur, xt, y);
-      run += fabsf(y);
-      const float sy = y * sigmoidf_(y);  // SiLU
-      // |sy - silu(exact y)| <= 1.1 u (1+2u) run + 2^-21 |sy| (expf within 2 ulp); margin x2
-      float yb;
-      if (!bf16_rounding_uncertain(sy, 2.0f * (1.1f * U32 * run + 4.0f * U32 * fabsf(sy)))) {
-        yb = bf_round(sy);
-      } else {
-        double yd = (double)b[jb];
+        const float sy = y * sigmoidf_(y);  // SiLU
+        // |sy - silu(exact y)| <= 1.1 u (1+2u) run + 2^-21 |sy| (expf within 2 ulp); margin x2
+        float yb;
+        if (!bf16_rounding_uncertain(sy, 2.0f * (1.1f * U32 * run + 4.0f * U32 * fabsf(sy)))) {
+          yb = bf_round(sy);
+        } else {
+          const unsigned s01 = q.get(i) | ((unsigned)q.get(i + 1) << 16);
+          const unsigned s23 = q.get(i + 2) | ((unsigned)q.get(i + 3) << 16);
+          if constexpr (L > 4) yb = silu_bf16_exact_ool(q.b, q.wp[0], q.wp[1], s01, s23);
+          else yb = silu_bf16_exact(q.b, q.wp[0], q.wp[1], s01, s23);
+        }
+        if (kind == 0) qh[t * HD + c] = yb;
+        else if (kind == 1) kh[t * HD + c] = yb;
+        else vv[t * HD + c] = __float2bfloat16_rn(yb);
+        // the window after token t: inputs at seq positions t + 1 .. t + 3, of
+        // which the last SL go to window slots 0 .. SL - 1 of slots[r, t]
+        const long long slot = slot_s[t];
+        const long long base = a.conv_dim_first ? (slot * C3 + ch) * SL : slot * SL * C3 + ch;
+        const long long step = a.conv_dim_first ? 1 : C3;
+        unsigned short* cs = reinterpret_cast<unsigned short*>(a.conv_state);
 #pragma unroll
-        for (int k = 0; k < 3; ++k)
-          if (k < SL) yd = fma((double)w[jb][k], (double)win[jb][k], yd);
-        yd = fma((double)wcur, (double)xt, yd);
-        yb = bf16_round_f64(yd / (1.0 + exp(-yd)));
+        for (int p = 1; p <= 3; ++p) {
+          const int j = p - 4 + SL;
+          if (j >= 0) cs[base + j * step] = q.get(i + p);
+        }
       }
-      if (blk == 0) qh[t * HD + c] = yb;
-      else if (blk == 1) kh[t * HD + c] = yb;
-      else vv[t * HD + c] = __float2bfloat16_rn(yb);
-      // shift the window by one and store it into this token's slot
-#pragma unroll
-      for (int k = 0; k < 3; ++k)
-        win[jb][k] = (k + 1 < SL) ? win[jb][k + 1] : (k + 1 == SL ? xt : win[jb][k]);
-      const long long dst = slot_s[t];
-#pragma unroll
-      for (int k = 0; k < 3; ++k)
-        if (k < SL) a.conv_state[conv_index(a, dst, ch, k)] = __float2bfloat16_rn(win[jb][k]);
     }
   }
   // ---- z = f_b . f_a (correctly rounded), lower-bound gate, e^g ---------------
   {
-    const float expA = expf(a.A_log[h]);
-    const int c0 = warp * Z_CHANNELS;
-    const float dtc = a.dt_bias[h * HD + c0 + (lane >> 1)];
+    const float expA = expf(a_log);
 #pragma unroll 1
-    for (int t = 0; t < L; ++t) {
-      const float4 f = *reinterpret_cast<const float4*>(fa_s + t * HD + lane * 4);
-      // |f_a|_2 of token t, rounded up: the fp32 sum of 128 squares is within
+    for (int t = 0; t < L; t += 2) {
+      const bool pair = (t + 1 < L);
+      const uint4* f0 = reinterpret_cast<const uint4*>(fa_b + t * HD);
+      float p0[4];
+      z_partials(fbw, f0[lane & 7], f0[8 + (lane & 7)], p0);
+      float z = z_reduce(p0, lane);
+      int tt = t;
+      if (pair) {
+        const uint4* f1 = reinterpret_cast<const uint4*>(fa_b + (t + 1) * HD);
+        float p1[4];
+        z_partials(fbw, f1[lane & 7], f1[8 + (lane & 7)], p1);
+        const float z1 = z_reduce(p1, lane);
+        if (lane & 1) {  // odd lanes finish token t + 1, even lanes token t
+          z = z1;
+          tt = t + 1;
+        }
+      }
+      // |f_a|_2 of token tt, rounded up: the fp32 sum of 128 squares is within
       // 2^-17 relative of exact, the root within half an ulp
-      const float fnorm = sqrtf(warp_sum(f.x * f.x + f.y * f.y + f.z * f.z + f.w * f.w)) * (1.0f + 0x1p-12f);
-      const float bound = 16.0f * U32 * (1.0f + 0x1p-10f) * fbn * fnorm;
-      const float z = z_channels(fbw, f, bound, lane);  // channel c0 + (lane >> 1)
-      if ((lane & 1) == 0) {
+      const float4 np = *reinterpret_cast<const float4*>(fnp + tt * 4);
+      const float fnorm = sqrtf((np.x + np.y) + (np.z + np.w)) * (1.0f + 0x1p-12f);
+      const float bound = 12.0f * U32 * (1.0f + 0x1p-10f) * fbn * fnorm;
+      const bool unsure = bf16_rounding_uncertain(z, bound);
+      unsigned redo = __ballot_sync(0xffffffffu, unsure) & (pair ? 0xffffffffu : 0x55555555u);
+      z = bf_round(z);
+      while (redo) {
+        const int li = __ffs(redo) - 1;
+        redo &= redo - 1;
+        const uint4* fr = reinterpret_cast<const uint4*>(fa_b + (pair ? t + (li & 1) : t) * HD);
+        uint4 w0, w1;
+        fb_row(fbw, (li >> 1) & 3, w0, w1);
+        const float ex = z_exact(w0, w1, fr[lane & 7], fr[8 + (lane & 7)]);
+        if (lane == li) z = ex;
+      }
+      if (pair || (lane & 1) == 0) {
         const float g = a.lb * sigmoidf_(expA * (z + dtc));
-        eg[t * HD + c0 + (lane >> 1)] = expf(g);
+        eg[tt * HD + zc] = expf(g);
       }
     }
   }
@@ -575,6 +713,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   // ---- recurrence: 2 passes of 2 quarters; 8 lanes per v row, 16 k values a lane --
   const int sub = lane >> 3, kl = lane & 7;
   const int lr = warp * 4 + sub;  // row within a quarter
+  const bool b2 = (kl & 4) != 0, b1 = (kl & 2) != 0;
   bool timed_out = false;
   float* dst_row = a.state_pool + ((long long)h * HD + lr) * HD + kl * 4;
 #pragma unroll 1
@@ -593,6 +732,8 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         sv[qq][2 * j] = make_float2(x.x, x.y);
         sv[qq][2 * j + 1] = make_float2(x.z, x.w);
       }
+    // the row of the value this lane ends up with after the reduce-scatter
+    const int vq = (2 * pass + (b1 ? 1 : 0)) * QUARTER_ROWS + lr;
 #pragma unroll 1
     for (int t = 0; t < L; ++t) {
       float2 kv[8], dk2[2], dq2[2];
@@ -618,27 +759,30 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
           dq2[qq] = fma2(sv[qq][2 * j + 1], q1, dq2[qq]);
         }
       }
-      float dk[2], dq[2];
-#pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        dk[qq] = dk2[qq].x + dk2[qq].y;
-        dq[qq] = dq2[qq].x + dq2[qq].y;
-      }
-#pragma unroll
-      for (int m = 1; m <= 4; m <<= 1)
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          dk[qq] += __shfl_xor_sync(0xffffffffu, dk[qq], m);
-          dq[qq] += __shfl_xor_sync(0xffffffffu, dq[qq], m);
-        }
+      // reduce-scatter of S'^T k^ and S'^T q^ of both rows over the row's 8
+      // lanes: lane kl ends with S'^T k^ (kl < 4) or S'^T q^ (kl >= 4) of row
+      // qq = (kl >> 1) & 1, on lanes kl and kl ^ 1
+      const float dk0 = dk2[0].x + dk2[0].y, dk1 = dk2[1].x + dk2[1].y;
+      const float dq0 = dq2[0].x + dq2[0].y, dq1 = dq2[1].x + dq2[1].y;
+      float k0 = b2 ? dq0 : dk0, k1 = b2 ? dq1 : dk1;
+      const float s0 = b2 ? dk0 : dq0, s1 = b2 ? dk1 : dq1;
+      k0 += __shfl_xor_sync(0xffffffffu, s0, 4);
+      k1 += __shfl_xor_sync(0xffffffffu, s1, 4);
+      float rv = b1 ? k1 : k0;
+      const float sx = b1 ? k0 : k1;
+      rv += __shfl_xor_sync(0xffffffffu, sx, 2);
+      rv += __shfl_xor_sync(0xffffffffu, rv, 1);
+      // beta u = beta (v - S'^T k^) on the lanes that hold S'^T k^, then to all
+      const float bt = beta_s[t];
+      const float bu_own = bt * (bf(vv[t * HD + vq]) - rv);
+      const float bu0 = __shfl_sync(0xffffffffu, bu_own, lane & ~7);
+      const float bu1 = __shfl_sync(0xffffffffu, bu_own, (lane & ~7) | 2);
+      if (kl == 4 || kl == 6)  // S_new^T q^ = S'^T q^ + beta u (k^.q^)
+        ob[t * HD + vq] = __float2bfloat16_rn(fmaf(b1 ? bu1 : bu0, kq_s[t], rv));
       float* dst = dst_row + (long long)slot_s[t] * a.heads * STATE_FLOATS;
-      const float bt = beta_s[t], kqt = kq_s[t];
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
-        const int v = (2 * pass + qq) * QUARTER_ROWS + lr;
-        const float u = bf(vv[t * HD + v]) - dk[qq];
-        const float bu = bt * u;
-        const float o = fmaf(bu, kqt, dq[qq]);  // S_new^T q^ = S'^T q^ + beta u (k^.q^)
+        const float bu = qq ? bu1 : bu0;
         const float2 bu2 = make_float2(bu, bu);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -652,7 +796,6 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
             store_streaming(dst + (2 * pass + qq) * QUARTER_ROWS * HD + j * 32, row4);
           }
         }
-        if (kl == 0) ob[t * HD + v] = __float2bfloat16_rn(o);
       }
     }
     }  // ok
