@@ -203,7 +203,13 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+// Sigmoid from the fast intrinsics: __expf is within 2 + 1.173 |x| ulp and
+// __fdividef within 2 ulp (CUDA's documented bounds), so with the rounding of
+// 1 + e^-x the result is within 2.35 |x| u + 2^-21 + u relative (u = 2^-24).
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// sqrt(s) for s >= 0 within 2^-21 relative (rsqrtf is within 2 ulp).
+__device__ __forceinline__ float sqrt_fast(float s) { return s > 0.0f ? s * rsqrtf(s) : 0.0f; }
 
 // ---- correctly rounded bf16 hand-offs ------------------------------------
 // The conv outputs (q, k, v) and z = f_b . f_a are handed on as bf16.  They
@@ -247,10 +253,13 @@ __device__ __forceinline__ float bf16_round_pair(float hi, float lo) {
   return ((e > 0.0f) == (s > 0.0f)) ? up : down;
 }
 
-__device__ __forceinline__ long long conv_index(const StepArgs& a, long long slot, int ch, int j) {
-  const int C = 3 * a.D, SL = a.W - 1;
-  return a.conv_dim_first ? (slot * C + ch) * SL + j : (slot * SL + j) * C + ch;
+// Element (slot, ch, j) of the conv cache is at conv_base + j * conv_step.
+__device__ __forceinline__ long long conv_base(const StepArgs& a, long long slot, int ch) {
+  const long long C = 3LL * a.D;
+  const int SL = a.W - 1;
+  return a.conv_dim_first ? (slot * C + ch) * SL : slot * SL * C + ch;
 }
+__device__ __forceinline__ long long conv_step(const StepArgs& a) { return a.conv_dim_first ? 1 : 3LL * a.D; }
 
 
 // Wait for phase `parity` of an mbarrier, giving up after WAIT_LIMIT_CYCLES SM
@@ -361,29 +370,53 @@ __device__ __forceinline__ float z_exact(const uint4 w0, const uint4 w1, const u
   return bf16_round_pair(hi, lo);
 }
 
-// Row rs of fbw, picked by masks so that fbw is never indexed at run time (that
-// would move it to local memory).
+// Row rs of fbw, picked by selects so that fbw is never indexed at run time
+// (that would move it to local memory).
+__device__ __forceinline__ unsigned pick4(int rs, unsigned a, unsigned b, unsigned c, unsigned d) {
+  return rs < 2 ? (rs == 0 ? a : b) : (rs == 2 ? c : d);
+}
 __device__ __forceinline__ void fb_row(const uint4 (&fbw)[4][2], int rs, uint4& w0, uint4& w1) {
-  w0 = w1 = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const unsigned msk = 0u - (unsigned)(r == rs);
-    w0.x |= fbw[r][0].x & msk; w0.y |= fbw[r][0].y & msk; w0.z |= fbw[r][0].z & msk; w0.w |= fbw[r][0].w & msk;
-    w1.x |= fbw[r][1].x & msk; w1.y |= fbw[r][1].y & msk; w1.z |= fbw[r][1].z & msk; w1.w |= fbw[r][1].w & msk;
-  }
+  w0.x = pick4(rs, fbw[0][0].x, fbw[1][0].x, fbw[2][0].x, fbw[3][0].x);
+  w0.y = pick4(rs, fbw[0][0].y, fbw[1][0].y, fbw[2][0].y, fbw[3][0].y);
+  w0.z = pick4(rs, fbw[0][0].z, fbw[1][0].z, fbw[2][0].z, fbw[3][0].z);
+  w0.w = pick4(rs, fbw[0][0].w, fbw[1][0].w, fbw[2][0].w, fbw[3][0].w);
+  w1.x = pick4(rs, fbw[0][1].x, fbw[1][1].x, fbw[2][1].x, fbw[3][1].x);
+  w1.y = pick4(rs, fbw[0][1].y, fbw[1][1].y, fbw[2][1].y, fbw[3][1].y);
+  w1.z = pick4(rs, fbw[0][1].z, fbw[1][1].z, fbw[2][1].z, fbw[3][1].z);
+  w1.w = pick4(rs, fbw[0][1].w, fbw[1][1].w, fbw[2][1].w, fbw[3][1].w);
 }
 
 // ---- causal conv ----------------------------------------------------------------
-// bf16 of SiLU(b + sum_k w_k s_k) from fp64 (exact products and sums of four
-// bf16 pairs; the SiLU's own fp64 error is far below a bf16 half ulp):
-// the rare path taken when the fp32 value is too close to a rounding boundary.
+// bf16 of SiLU(y), y = b + sum_k w_k s_k (four bf16 pairs), for the rare case in
+// which the fast fp32 value lies too close to a rounding boundary.  First in
+// fp32: y exactly as the pair s + e (TwoSum over the exact products), the
+// sigmoid from expf (within 2 ulp) and an IEEE division; that settles most
+// cases.  The rest go to fp64 (exact products and sums; the SiLU's own fp64
+// error is far below a bf16 half ulp), which is slow on this part.
 __device__ __forceinline__ float silu_bf16_exact(float b, unsigned wp0, unsigned wp1, unsigned s01, unsigned s23) {
-  double y = (double)b;
-  y = fma((double)bf_lo(wp0), (double)bf_lo(s01), y);
-  y = fma((double)bf_hi(wp0), (double)bf_hi(s01), y);
-  y = fma((double)bf_lo(wp1), (double)bf_lo(s23), y);
-  y = fma((double)bf_hi(wp1), (double)bf_hi(s23), y);
-  return bf16_round_f64(y / (1.0 + exp(-y)));
+  const float p[4] = {bf_lo(wp0) * bf_lo(s01), bf_hi(wp0) * bf_hi(s01), bf_lo(wp1) * bf_lo(s23),
+                      bf_hi(wp1) * bf_hi(s23)};  // exact
+  float sum = b, err = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float t = sum + p[k], bp = t - sum;
+    err += (sum - (t - bp)) + (p[k] - bp);
+    sum = t;
+  }
+  const float y = sum + err;  // within u |y| (1 + 4u) of the exact sum
+  const float sg = 1.0f / (1.0f + expf(-y));
+  const float sy = fmaf(sum, sg, err * sg);
+  // sigmoid: 2^-22 (expf) + u (1 + e^-y) + u (division) + |y| u (the error of
+  // y, through sigma' / sigma = 1 - sigma); the product one more u:
+  // |sy - silu(exact y)| <= (2^-22 + 3u + |y| u) |sy|; margin x2
+  if (fabsf(y) < 80.0f && !bf16_rounding_uncertain(sy, 2.0f * (0x1p-22f + (3.0f + fabsf(y)) * U32) * fabsf(sy)))
+    return bf_round(sy);
+  double yd = (double)b;
+  yd = fma((double)bf_lo(wp0), (double)bf_lo(s01), yd);
+  yd = fma((double)bf_hi(wp0), (double)bf_hi(s01), yd);
+  yd = fma((double)bf_lo(wp1), (double)bf_lo(s23), yd);
+  yd = fma((double)bf_hi(wp1), (double)bf_hi(s23), yd);
+  return bf16_round_f64(yd / (1.0 + exp(-yd)));
 }
 // The same out of line: with many tokens the unrolled conv is long enough for
 // instruction fetch to matter, and the rare path is better kept out of it.
@@ -512,12 +545,12 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       const int t = t0 + i - 3;  // token whose x sits at position t0 + i
       if (t >= 0 && t < L && i < n + 3) q.set(i, proj16[(row0 + t) * a.pitch + ch]);
     }
-    const unsigned short* cw = reinterpret_cast<const unsigned short*>(a.conv_w) + (long long)kind * a.W * D + h * HD + c;
+    const unsigned short* cw = reinterpret_cast<const unsigned short*>(a.conv_w) + kind * a.W * D + h * HD + c;
     unsigned short w4[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int j = k - (3 - SL);  // tap index, right-aligned
-      w4[k] = (j >= 0) ? cw[(long long)j * D] : (unsigned short)0;
+      w4[k] = (j >= 0) ? cw[j * D] : (unsigned short)0;
     }
     q.wp[0] = w4[0] | ((unsigned)w4[1] << 16);
     q.wp[1] = w4[2] | ((unsigned)w4[3] << 16);
@@ -565,16 +598,19 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     ctl[0] = 0;
   }
   // window values at seq positions < 3 (window slot j = position - (3 - SL))
+  {
+    const long long cstep = conv_step(a);
 #pragma unroll
-  for (int kind = 0; kind < 3; ++kind) {
-    ConvLane<CA>& q = cv[kind];
-    const int t0 = conv_t0(kind), n = conv_n(kind);
-    const int ch = kind * D + h * HD + c;
+    for (int kind = 0; kind < 3; ++kind) {
+      ConvLane<CA>& q = cv[kind];
+      const int t0 = conv_t0(kind), n = conv_n(kind);
+      const unsigned short* cs = reinterpret_cast<const unsigned short*>(a.conv_state) +
+                                 conv_base(a, start, kind * D + h * HD + c);
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const int j = t0 + i - (3 - SL);
-      if (t0 + i < 3 && j >= 0 && n > 0)
-        q.set(i, reinterpret_cast<const unsigned short*>(a.conv_state)[conv_index(a, start, ch, j)]);
+      for (int i = 0; i < 3; ++i) {
+        const int j = t0 + i - (3 - SL);
+        if (t0 + i < 3 && j >= 0 && n > 0) q.set(i, cs[j * cstep]);
+      }
     }
   }
 #pragma unroll
@@ -592,14 +628,14 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       if (lane == 0) fnp[(e / HD) * 4 + (e % HD) / 32] = sq;
     }
   }
-  if (tid < L) beta_s[tid] = sigmoidf_(beta_logit);
+  if (tid < L) beta_s[tid] = sigmoid_fast(beta_logit);
   __syncthreads();  // barriers initialised, f_a, its squares and the slots staged
 
   // ---- causal conv of the thread's channels (correctly rounded), window stores -
   // It runs before z: its inputs arrived with round trips 1 and 2, which the
   // recurrence waits for anyway, and they are dead before z needs registers.
   {
-    const long long C3 = 3LL * D;
+    const long long cstep = conv_step(a);
 #pragma unroll
     for (int kind = 0; kind < 3; ++kind) {
       const ConvLane<CA>& q = cv[kind];
@@ -617,10 +653,12 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
           case 2: y = conv_dot<2>(q, run); break;
           default: y = conv_dot<3>(q, run); break;
         }
-        const float sy = y * sigmoidf_(y);  // SiLU
-        // |sy - silu(exact y)| <= 1.1 u (1+2u) run + 2^-21 |sy| (expf within 2 ulp); margin x2
+        const float sy = y * sigmoid_fast(y);  // SiLU
+        // |y - exact| <= 1.1 u run and SiLU' <= 1.1; the sigmoid and the
+        // product add at most (2.35 |y| u + 2^-21 + 2u) |sy|:
+        // |sy - silu(exact y)| <= 1.21 u run + (2.5 u |y| + 2^-20) |sy|; margin x2
         float yb;
-        if (!bf16_rounding_uncertain(sy, 2.0f * (1.1f * U32 * run + 4.0f * U32 * fabsf(sy)))) {
+        if (!bf16_rounding_uncertain(sy, 2.0f * (1.21f * U32 * run + (2.5f * U32 * fabsf(y) + 0x1p-20f) * fabsf(sy)))) {
           yb = bf_round(sy);
         } else {
           const unsigned s01 = q.get(i) | ((unsigned)q.get(i + 1) << 16);
@@ -633,14 +671,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         else vv[t * HD + c] = __float2bfloat16_rn(yb);
         // the window after token t: inputs at seq positions t + 1 .. t + 3, of
         // which the last SL go to window slots 0 .. SL - 1 of slots[r, t]
-        const long long slot = slot_s[t];
-        const long long base = a.conv_dim_first ? (slot * C3 + ch) * SL : slot * SL * C3 + ch;
-        const long long step = a.conv_dim_first ? 1 : C3;
-        unsigned short* cs = reinterpret_cast<unsigned short*>(a.conv_state);
+        unsigned short* cs = reinterpret_cast<unsigned short*>(a.conv_state) + conv_base(a, slot_s[t], ch);
 #pragma unroll
         for (int p = 1; p <= 3; ++p) {
           const int j = p - 4 + SL;
-          if (j >= 0) cs[base + j * step] = q.get(i + p);
+          if (j >= 0) cs[j * cstep] = q.get(i + p);
         }
       }
     }
@@ -667,9 +702,9 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         }
       }
       // |f_a|_2 of token tt, rounded up: the fp32 sum of 128 squares is within
-      // 2^-17 relative of exact, the root within half an ulp
+      // 2^-17 relative of exact, its root within 2^-18 + 2^-21
       const float4 np = *reinterpret_cast<const float4*>(fnp + tt * 4);
-      const float fnorm = sqrtf((np.x + np.y) + (np.z + np.w)) * (1.0f + 0x1p-12f);
+      const float fnorm = sqrt_fast((np.x + np.y) + (np.z + np.w)) * (1.0f + 0x1p-12f);
       const float bound = 12.0f * U32 * (1.0f + 0x1p-10f) * fbn * fnorm;
       const bool unsure = bf16_rounding_uncertain(z, bound);
       unsigned redo = __ballot_sync(0xffffffffu, unsure) & (pair ? 0xffffffffu : 0x55555555u);
@@ -684,8 +719,8 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         if (lane == li) z = ex;
       }
       if (pair || (lane & 1) == 0) {
-        const float g = a.lb * sigmoidf_(expA * (z + dtc));
-        eg[tt * HD + zc] = expf(g);
+        const float g = a.lb * sigmoid_fast(expA * (z + dtc));
+        eg[tt * HD + zc] = __expf(g);
       }
     }
   }
@@ -700,7 +735,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     const float sq = warp_sum(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
     const float sk = warp_sum(k.x * k.x + k.y * k.y + k.z * k.z + k.w * k.w);
     const float sqk = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w);
-    const float rq = 1.0f / sqrtf(sq + 1e-6f), rk = 1.0f / sqrtf(sk + 1e-6f);
+    const float rq = rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
     const float fq = rq * a.q_scale;
     q.x *= fq; q.y *= fq; q.z *= fq; q.w *= fq;
     k.x *= rk; k.y *= rk; k.z *= rk; k.w *= rk;
@@ -838,11 +873,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[e] = bf(ob[t * HD + lane * 4 + e]);
     const float ss = warp_sum(o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3]);
-    const float rstd = 1.0f / sqrtf(ss * (1.0f / HD) + a.eps);
+    const float rstd = rsqrtf(ss * (1.0f / HD) + a.eps);
     __align__(8) __nv_bfloat16 y[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      y[e] = __float2bfloat16_rn(o[e] * rstd * a.o_norm[lane * 4 + e] * sigmoidf_(bf(gate_s[t * HD + lane * 4 + e])));
+      y[e] = __float2bfloat16_rn(o[e] * rstd * a.o_norm[lane * 4 + e] * sigmoid_fast(bf(gate_s[t * HD + lane * 4 + e])));
     *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
   }
   if constexpr (L == 1) {
