@@ -66,7 +66,7 @@ struct StepArgs {
   const int* slots;
   const int* accepted;
   __nv_bfloat16* out;
-  const __nv_bfloat16* conv_w;  // prepared [3][W][D]
+  const uint2* conv_w;          // prepared [3D]: the W taps right-aligned in 4, two bf16 a word
   const __nv_bfloat16* bias;    // [3D] or null
   const __nv_bfloat16* f_b;     // [D][128]
   const float* fb_norm;         // [D] Euclidean norm of each f_b row, rounded up
@@ -434,10 +434,7 @@ struct ConvLane {
   static constexpr int WORDS = (N + 4) / 2;
   unsigned sp[WORDS];  // position t0 + i in half i & 1 of word i >> 1
   unsigned wp[2];      // taps, w[k] in half k & 1 of word k >> 1
-  float b;
-  __device__ __forceinline__ void set(int i, unsigned short v) {  // i compile-time after unrolling
-    sp[i >> 1] = (i & 1) ? ((sp[i >> 1] & 0xffffu) | ((unsigned)v << 16)) : ((sp[i >> 1] & 0xffff0000u) | v);
-  }
+  unsigned short bb;   // bias
   __device__ __forceinline__ unsigned short get(int i) const {
     return (unsigned short)((i & 1) ? (sp[i >> 1] >> 16) : (sp[i >> 1] & 0xffffu));
   }
@@ -450,7 +447,7 @@ struct ConvLane {
 // once; run collects |partial sums| (the fp32 error bound / u).
 template <int I, int N>
 __device__ __forceinline__ float conv_dot(const ConvLane<N>& q, float& run) {
-  float y = q.b;
+  float y = bf_bits(q.bb);
   y = fma_bf16<0, (I & 1)>(q.wp[0], q.sp[I >> 1], y);
   run = fabsf(y);
   y = fma_bf16<1, ((I + 1) & 1)>(q.wp[0], q.sp[(I + 1) >> 1], y);
@@ -531,30 +528,13 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   // first token and token count of kind 0, 1 (q, k) and 2 (v)
   auto conv_t0 = [&](int kind) { return (kind < 2) ? (second ? CA : 0) : (second ? CB : 0); };
   auto conv_n = [&](int kind) { return (kind < 2) ? (second ? L - CA : CA) : (second ? L - CB : CB); };
-  const unsigned short* proj16 = reinterpret_cast<const unsigned short*>(a.projected);
   ConvLane<CA> cv[3];
 #pragma unroll
   for (int kind = 0; kind < 3; ++kind) {
-    ConvLane<CA>& q = cv[kind];
-    const int t0 = conv_t0(kind), n = conv_n(kind);
-    const int ch = kind * D + h * HD + c;
-#pragma unroll
-    for (int w = 0; w < ConvLane<CA>::WORDS; ++w) q.sp[w] = 0u;
-#pragma unroll
-    for (int i = 0; i < CA + 3; ++i) {
-      const int t = t0 + i - 3;  // token whose x sits at position t0 + i
-      if (t >= 0 && t < L && i < n + 3) q.set(i, proj16[(row0 + t) * a.pitch + ch]);
-    }
-    const unsigned short* cw = reinterpret_cast<const unsigned short*>(a.conv_w) + kind * a.W * D + h * HD + c;
-    unsigned short w4[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int j = k - (3 - SL);  // tap index, right-aligned
-      w4[k] = (j >= 0) ? cw[j * D] : (unsigned short)0;
-    }
-    q.wp[0] = w4[0] | ((unsigned)w4[1] << 16);
-    q.wp[1] = w4[2] | ((unsigned)w4[3] << 16);
-    q.b = a.bias ? bf(a.bias[ch]) : 0.0f;
+    const uint2 wt = a.conv_w[kind * D + h * HD + c];
+    cv[kind].wp[0] = wt.x;
+    cv[kind].wp[1] = wt.y;
+    cv[kind].bb = a.bias ? reinterpret_cast<const unsigned short*>(a.bias)[kind * D + h * HD + c] : (unsigned short)0;
   }
 
   // ---- validate (every thread decides the same from the same loaded values) ---
@@ -583,36 +563,52 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   }
   if (status != TASK_OK) return;
 
-  // ---- round trip 2: the start state (bulk) and the start conv windows -------
-  if (tid == 0) {
-    const float* src = a.state_pool + ((long long)start * a.heads + h) * STATE_FLOATS;
-#pragma unroll
-    for (int q = 0; q < QUARTERS; ++q) mbar_init(smem_u32(&mbar[q]), 1);
-    fence_mbar_init();
-#pragma unroll
-    for (int q = 0; q < QUARTERS; ++q) {
-      const uint32_t bar = smem_u32(&mbar[q]);
-      mbar_expect_tx(bar, QUARTER_BYTES);
-      bulk_load(smem_u32(st + q * QUARTER_ROWS * HD), src + q * QUARTER_ROWS * HD, QUARTER_BYTES, bar);
-    }
-    ctl[0] = 0;
-  }
-  // window values at seq positions < 3 (window slot j = position - (3 - SL))
+  // ---- round trip 2: the conv inputs, then the start state (bulk) -------------
+  // The conv inputs of the thread's tokens (projected x from position 3 on, the
+  // start window below it) go out first so that they do not queue behind the
+  // state's bulk copies; they are packed once the copies are issued.
+  unsigned short xin[3][CA + 3];
   {
+    const unsigned short* proj16 = reinterpret_cast<const unsigned short*>(a.projected);
+    const unsigned short* cs16 = reinterpret_cast<const unsigned short*>(a.conv_state);
     const long long cstep = conv_step(a);
 #pragma unroll
     for (int kind = 0; kind < 3; ++kind) {
-      ConvLane<CA>& q = cv[kind];
       const int t0 = conv_t0(kind), n = conv_n(kind);
-      const unsigned short* cs = reinterpret_cast<const unsigned short*>(a.conv_state) +
-                                 conv_base(a, start, kind * D + h * HD + c);
+      const int ch = kind * D + h * HD + c;
+      const unsigned short* cs = cs16 + conv_base(a, start, ch);
 #pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        const int j = t0 + i - (3 - SL);
-        if (t0 + i < 3 && j >= 0 && n > 0) q.set(i, cs[j * cstep]);
+      for (int i = 0; i < CA + 3; ++i) {
+        const int pos = t0 + i;  // sequence position; pos - 3 < t0 + n <= L
+        unsigned short v = 0;
+        if (n > 0 && i < n + 3) {
+          if (pos >= 3) v = proj16[(row0 + pos - 3) * a.pitch + ch];
+          else if (pos - (3 - SL) >= 0) v = cs[(pos - (3 - SL)) * cstep];
+        }
+        xin[kind][i] = v;
       }
     }
   }
+  // Decode (many CTAs a SM, one after another) puts the state in flight at
+  // once; verify (often a single wave of CTAs, all in this phase together)
+  // first waits for the conv inputs, which would otherwise queue behind every
+  // CTA's state copies, and has its conv and gates to cover the state's latency.
+  auto issue_state = [&]() {
+    if (tid == 0) {
+      const float* src = a.state_pool + ((long long)start * a.heads + h) * STATE_FLOATS;
+#pragma unroll
+      for (int q = 0; q < QUARTERS; ++q) mbar_init(smem_u32(&mbar[q]), 1);
+      fence_mbar_init();
+#pragma unroll
+      for (int q = 0; q < QUARTERS; ++q) {
+        const uint32_t bar = smem_u32(&mbar[q]);
+        mbar_expect_tx(bar, QUARTER_BYTES);
+        bulk_load(smem_u32(st + q * QUARTER_ROWS * HD), src + q * QUARTER_ROWS * HD, QUARTER_BYTES, bar);
+      }
+      ctl[0] = 0;
+    }
+  };
+  if constexpr (L == 1) issue_state();
 #pragma unroll
   for (int t = 0; t < L; ++t)
     if (tid == t) slot_s[t] = sl[t];
@@ -629,6 +625,16 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     }
   }
   if (tid < L) beta_s[tid] = sigmoid_fast(beta_logit);
+#pragma unroll
+  for (int kind = 0; kind < 3; ++kind)
+#pragma unroll
+    for (int w = 0; w < ConvLane<CA>::WORDS; ++w)
+      cv[kind].sp[w] = xin[kind][2 * w] | ((2 * w + 1 < CA + 3) ? ((unsigned)xin[kind][2 * w + 1] << 16) : 0u);
+  if constexpr (L > 1) {
+    // thread 0 issues the copies only once its own conv inputs are in
+    asm volatile("" ::"r"(cv[0].sp[0] | cv[1].sp[0] | cv[2].sp[0]));
+    issue_state();
+  }
   __syncthreads();  // barriers initialised, f_a, its squares and the slots staged
 
   // ---- causal conv of the thread's channels (correctly rounded), window stores -
@@ -663,8 +669,8 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         } else {
           const unsigned s01 = q.get(i) | ((unsigned)q.get(i + 1) << 16);
           const unsigned s23 = q.get(i + 2) | ((unsigned)q.get(i + 3) << 16);
-          if constexpr (L > 4) yb = silu_bf16_exact_ool(q.b, q.wp[0], q.wp[1], s01, s23);
-          else yb = silu_bf16_exact(q.b, q.wp[0], q.wp[1], s01, s23);
+          if constexpr (L > 4) yb = silu_bf16_exact_ool(bf_bits(q.bb), q.wp[0], q.wp[1], s01, s23);
+          else yb = silu_bf16_exact(bf_bits(q.bb), q.wp[0], q.wp[1], s01, s23);
         }
         if (kind == 0) qh[t * HD + c] = yb;
         else if (kind == 1) kh[t * HD + c] = yb;
@@ -745,90 +751,109 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   }
   __syncthreads();
 
-  // ---- recurrence: 2 passes of 2 quarters; 8 lanes per v row, 16 k values a lane --
-  const int sub = lane >> 3, kl = lane & 7;
-  const int lr = warp * 4 + sub;  // row within a quarter
-  const bool b2 = (kl & 4) != 0, b1 = (kl & 2) != 0;
+  // ---- recurrence: 2 passes of 2 quarters; 16 lanes per v row, 8 k values a lane --
+  // Lane l: half hs = l >> 4 of the warp, kl = l & 15 owns k = 64 m + 4 kl + (0..3)
+  // (m = 0, 1); in pass p the thread holds rows 64 p + 32 (r >> 1) + 16 (r & 1) +
+  // 2 warp + hs (r = 0..3), i.e. one row of each quarter half.  A warp half
+  // reads each k-slice of e^g, q^, k^ once per token.
+  const int hs = lane >> 4, kl = lane & 15;
+  const int rbase = warp * 2 + hs;
+  const bool b3 = (kl & 8) != 0, b2 = (kl & 4) != 0, b1 = (kl & 2) != 0;
+  const int rsel = (b2 ? 2 : 0) + (b1 ? 1 : 0);  // row of the value this lane ends with
   bool timed_out = false;
-  float* dst_row = a.state_pool + ((long long)h * HD + lr) * HD + kl * 4;
+  float* dst_k = a.state_pool + (long long)h * STATE_FLOATS + kl * 4;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mbar[2 * pass]), 0) &&
                                                 mbar_wait_bounded(smem_u32(&mbar[2 * pass + 1]), 0));
     if (!ok) timed_out = true;
     if (ok) {
-    // two rows (one per quarter of the pass), 16 k values each as 8 float2 pairs
-    float2 sv[2][8];
+    // 4 rows, 8 k values each as 4 float2 pairs
+    float2 sv[4][4];
 #pragma unroll
-    for (int qq = 0; qq < 2; ++qq)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 x = *reinterpret_cast<const float4*>(st + ((2 * pass + qq) * QUARTER_ROWS + lr) * HD + j * 32 + kl * 4);
-        sv[qq][2 * j] = make_float2(x.x, x.y);
-        sv[qq][2 * j + 1] = make_float2(x.z, x.w);
+      for (int m = 0; m < 2; ++m) {
+        const int row = pass * 64 + (r >> 1) * 32 + (r & 1) * 16 + rbase;
+        const float4 x = *reinterpret_cast<const float4*>(st + row * HD + m * 64 + kl * 4);
+        sv[r][2 * m] = make_float2(x.x, x.y);
+        sv[r][2 * m + 1] = make_float2(x.z, x.w);
       }
-    // the row of the value this lane ends up with after the reduce-scatter
-    const int vq = (2 * pass + (b1 ? 1 : 0)) * QUARTER_ROWS + lr;
+    const int vq = pass * 64 + (rsel >> 1) * 32 + (rsel & 1) * 16 + rbase;  // row of this lane's value
 #pragma unroll 1
     for (int t = 0; t < L; ++t) {
-      float2 kv[8], dk2[2], dq2[2];
+      float2 kv[4], dk2[4], dq2[4];
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) dk2[qq] = dq2[qq] = make_float2(0.0f, 0.0f);
+      for (int r = 0; r < 4; ++r) dk2[r] = dq2[r] = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int k0 = t * HD + j * 32 + kl * 4;
+      for (int m = 0; m < 2; ++m) {
+        const int k0 = t * HD + m * 64 + kl * 4;
         const float4 e = *reinterpret_cast<const float4*>(eg + k0);
         const float4 qv = *reinterpret_cast<const float4*>(qh + k0);
         const float4 k4 = *reinterpret_cast<const float4*>(kh + k0);
         const float2 e0 = make_float2(e.x, e.y), e1 = make_float2(e.z, e.w);
         const float2 q0 = make_float2(qv.x, qv.y), q1 = make_float2(qv.z, qv.w);
-        kv[2 * j] = make_float2(k4.x, k4.y);
-        kv[2 * j + 1] = make_float2(k4.z, k4.w);
+        kv[2 * m] = make_float2(k4.x, k4.y);
+        kv[2 * m + 1] = make_float2(k4.z, k4.w);
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          sv[qq][2 * j] = mul2(sv[qq][2 * j], e0);  // S' = diag(e^g) S
-          sv[qq][2 * j + 1] = mul2(sv[qq][2 * j + 1], e1);
-          dk2[qq] = fma2(sv[qq][2 * j], kv[2 * j], dk2[qq]);
-          dk2[qq] = fma2(sv[qq][2 * j + 1], kv[2 * j + 1], dk2[qq]);
-          dq2[qq] = fma2(sv[qq][2 * j], q0, dq2[qq]);
-          dq2[qq] = fma2(sv[qq][2 * j + 1], q1, dq2[qq]);
+        for (int r = 0; r < 4; ++r) {
+          sv[r][2 * m] = mul2(sv[r][2 * m], e0);  // S' = diag(e^g) S
+          sv[r][2 * m + 1] = mul2(sv[r][2 * m + 1], e1);
+          dk2[r] = fma2(sv[r][2 * m], kv[2 * m], dk2[r]);
+          dk2[r] = fma2(sv[r][2 * m + 1], kv[2 * m + 1], dk2[r]);
+          dq2[r] = fma2(sv[r][2 * m], q0, dq2[r]);
+          dq2[r] = fma2(sv[r][2 * m + 1], q1, dq2[r]);
         }
       }
-      // reduce-scatter of S'^T k^ and S'^T q^ of both rows over the row's 8
-      // lanes: lane kl ends with S'^T k^ (kl < 4) or S'^T q^ (kl >= 4) of row
-      // qq = (kl >> 1) & 1, on lanes kl and kl ^ 1
-      const float dk0 = dk2[0].x + dk2[0].y, dk1 = dk2[1].x + dk2[1].y;
-      const float dq0 = dq2[0].x + dq2[0].y, dq1 = dq2[1].x + dq2[1].y;
-      float k0 = b2 ? dq0 : dk0, k1 = b2 ? dq1 : dk1;
-      const float s0 = b2 ? dk0 : dq0, s1 = b2 ? dk1 : dq1;
-      k0 += __shfl_xor_sync(0xffffffffu, s0, 4);
-      k1 += __shfl_xor_sync(0xffffffffu, s1, 4);
-      float rv = b1 ? k1 : k0;
-      const float sx = b1 ? k0 : k1;
-      rv += __shfl_xor_sync(0xffffffffu, sx, 2);
+      // reduce-scatter of S'^T k^ and S'^T q^ of the 4 rows over the row's 16
+      // lanes (offsets 8, 4, 2, then a full add at 1): lane kl ends with
+      // S'^T k^ (kl < 8) or S'^T q^ (kl >= 8) of row rsel, on lanes kl and kl ^ 1
+      float v8[8];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        v8[r] = dk2[r].x + dk2[r].y;
+        v8[4 + r] = dq2[r].x + dq2[r].y;
+      }
+      float w4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float keep = b3 ? v8[4 + i] : v8[i], send = b3 ? v8[i] : v8[4 + i];
+        w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+      float w2[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float keep = b2 ? w4[2 + i] : w4[i], send = b2 ? w4[i] : w4[2 + i];
+        w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+      float rv = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
       rv += __shfl_xor_sync(0xffffffffu, rv, 1);
-      // beta u = beta (v - S'^T k^) on the lanes that hold S'^T k^, then to all
+      // beta u = beta (v - S'^T k^) on the lanes holding S'^T k^, then to the half
       const float bt = beta_s[t];
       const float bu_own = bt * (bf(vv[t * HD + vq]) - rv);
-      const float bu0 = __shfl_sync(0xffffffffu, bu_own, lane & ~7);
-      const float bu1 = __shfl_sync(0xffffffffu, bu_own, (lane & ~7) | 2);
-      if (kl == 4 || kl == 6)  // S_new^T q^ = S'^T q^ + beta u (k^.q^)
-        ob[t * HD + vq] = __float2bfloat16_rn(fmaf(b1 ? bu1 : bu0, kq_s[t], rv));
-      float* dst = dst_row + (long long)slot_s[t] * a.heads * STATE_FLOATS;
+      const int src = lane & 16;
+      float bu[4];
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        const float bu = qq ? bu1 : bu0;
-        const float2 bu2 = make_float2(bu, bu);
+      for (int r = 0; r < 4; ++r) bu[r] = __shfl_sync(0xffffffffu, bu_own, src | (2 * r));
+      if (b3 && (kl & 1) == 0) {  // S_new^T q^ = S'^T q^ + beta u (k^.q^)
+        const float bur = b2 ? (b1 ? bu[3] : bu[2]) : (b1 ? bu[1] : bu[0]);
+        ob[t * HD + vq] = __float2bfloat16_rn(fmaf(bur, kq_s[t], rv));
+      }
+      float* dst = dst_k + (long long)slot_s[t] * a.heads * STATE_FLOATS;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          sv[qq][2 * j] = fma2(bu2, kv[2 * j], sv[qq][2 * j]);  // S += beta k^ u^T
-          sv[qq][2 * j + 1] = fma2(bu2, kv[2 * j + 1], sv[qq][2 * j + 1]);
-          const float4 row4 = make_float4(sv[qq][2 * j].x, sv[qq][2 * j].y, sv[qq][2 * j + 1].x, sv[qq][2 * j + 1].y);
+      for (int r = 0; r < 4; ++r) {
+        const int row = pass * 64 + (r >> 1) * 32 + (r & 1) * 16 + rbase;
+        const float2 bu2 = make_float2(bu[r], bu[r]);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          sv[r][2 * m] = fma2(bu2, kv[2 * m], sv[r][2 * m]);  // S += beta k^ u^T
+          sv[r][2 * m + 1] = fma2(bu2, kv[2 * m + 1], sv[r][2 * m + 1]);
+          const float4 row4 = make_float4(sv[r][2 * m].x, sv[r][2 * m].y, sv[r][2 * m + 1].x, sv[r][2 * m + 1].y);
           if constexpr (L == 1) {
             // decode: back into the shared-memory state; TMA stores the quarter
-            *reinterpret_cast<float4*>(st + ((2 * pass + qq) * QUARTER_ROWS + lr) * HD + j * 32 + kl * 4) = row4;
+            *reinterpret_cast<float4*>(st + row * HD + m * 64 + kl * 4) = row4;
           } else {
-            store_streaming(dst + (2 * pass + qq) * QUARTER_ROWS * HD + j * 32, row4);
+            store_streaming(dst + row * HD + m * 64, row4);
           }
         }
       }
@@ -885,15 +910,19 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   }
 }
 
-// [3D, 1, W] -> [3, W, D] (decode_conv_weight on the PreparedKda page).
-__global__ void relayout_conv_w(const __nv_bfloat16* in, __nv_bfloat16* out, int D, int W) {
-  const long long n = 3LL * D * W;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const long long ch = i / W;  // source channel in [0, 3D)
-    const int j = (int)(i % W);
-    const long long blk = ch / D, c = ch % D;
-    out[(blk * W + j) * D + c] = in[i];
+// [3D, 1, W] -> [3D] of 4 taps right-aligned (zeros in front when W < 4),
+// two bf16 a word: one 8-byte load gives a channel all its taps (the
+// PreparedKda page re-lays the weight out once, in decode_conv_weight).
+__global__ void pack_conv_w(const unsigned short* in, uint2* out, long long channels, int W) {
+  const long long ch = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (ch >= channels) return;
+  unsigned short t[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int j = k - (4 - W);
+    t[k] = (j >= 0) ? in[ch * W + j] : (unsigned short)0;
   }
+  out[ch] = make_uint2(t[0] | ((unsigned)t[1] << 16), t[2] | ((unsigned)t[3] << 16));
 }
 
 // Euclidean norm of each 128-wide bf16 row, in fp64, rounded up to fp32.
@@ -941,7 +970,7 @@ struct kda_handle {
   int device;
   int sms;  // multiprocessors of the device: one persistent CTA each
   int heads, W;
-  __nv_bfloat16* conv_w;
+  uint2* conv_w;
   __nv_bfloat16* bias;
   __nv_bfloat16* f_b;
   float* fb_norm;
@@ -995,7 +1024,7 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
   h->eps = eps;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device);
-  const size_t conv_bytes = sizeof(__nv_bfloat16) * 3 * D * conv_width;
+  const size_t conv_bytes = sizeof(uint2) * 3 * D;
   if (e == cudaSuccess) e = cudaMalloc(&h->conv_w, conv_bytes);
   if (e == cudaSuccess && bias) e = cudaMalloc(&h->bias, sizeof(__nv_bfloat16) * 3 * D);
   if (e == cudaSuccess) e = cudaMalloc(&h->f_b, sizeof(__nv_bfloat16) * D * HD);
@@ -1011,8 +1040,8 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
   if (e == cudaSuccess) e = cudaMemcpy(h->dt_bias, dt_bias, sizeof(float) * D, cudaMemcpyDeviceToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->o_norm, o_norm, sizeof(float) * HD, cudaMemcpyDeviceToDevice);
   if (e == cudaSuccess) {
-    relayout_conv_w<<<(unsigned)((3 * D * conv_width + 255) / 256), 256>>>(
-        static_cast<const __nv_bfloat16*>(conv_w), h->conv_w, (int)D, conv_width);
+    pack_conv_w<<<(unsigned)((3 * D + 255) / 256), 256>>>(static_cast<const unsigned short*>(conv_w), h->conv_w,
+                                                          3 * D, conv_width);
     e = cudaGetLastError();
   }
 
