@@ -37,6 +37,7 @@
 // boundary.  Every wait is bounded (about 1 s of SM clock cycles); a wait that
 // gives up sets KDA_ERR_TIMEOUT and the request's outputs are not written.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -87,7 +88,7 @@ struct Smem {
   static constexpr int qh = kh + L * HD * 4;          // float [L][128]    q, then q^
   static constexpr int fa = qh + L * HD * 4;          // bf16  [L][128]    f_a; later o
   static constexpr int vv = fa + L * HD * 2;          // bf16  [L][128]    v
-  static constexpr int gate = vv + L * HD * 2;        // bf16  [L][128]    out-gate
+  static constexpr int gate = vv + L * HD * 2;        // fp16  [L][128]    sigmoid(out-gate)
   static constexpr int fnp = gate + L * HD * 2;       // float [L][4]      partial sums of f_a^2
   static constexpr int beta = fnp + 16 * L;           // float [L]
   static constexpr int kq = beta + 4 * L;             // float [L]         k^.q^
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   unsigned short* fa_b = reinterpret_cast<unsigned short*>(smem + S::fa);
   __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(smem + S::fa);  // reuses the f_a space
   __nv_bfloat16* vv = reinterpret_cast<__nv_bfloat16*>(smem + S::vv);
-  __nv_bfloat16* gate_s = reinterpret_cast<__nv_bfloat16*>(smem + S::gate);
+  __half* gsig_s = reinterpret_cast<__half*>(smem + S::gate);  // sigmoid of the out-gate
   float* fnp = reinterpret_cast<float*>(smem + S::fnp);
   float* beta_s = reinterpret_cast<float*>(smem + S::beta);
   float* kq_s = reinterpret_cast<float*>(smem + S::kq);
@@ -617,7 +618,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     const int e = tid + i * THREADS;
     if ((tid & ~31) + i * THREADS < L * HD) {  // warp-uniform
       fa_b[e] = fa_v[i];
-      reinterpret_cast<unsigned short*>(gate_s)[e] = gate_v[i];
+      gsig_s[e] = __float2half_rn(sigmoid_fast(bf_bits(gate_v[i])));  // within 2^-11 relative; the output is bf16
       // squares of f_a: one partial sum per (token, 32 channels)
       const float f = bf_bits(fa_v[i]);
       const float sq = warp_sum(f * f);
@@ -876,6 +877,8 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       }
     }
   }
+  // the RMSNorm weights of this lane, in flight across the barrier
+  const float4 onw = (warp < L) ? *reinterpret_cast<const float4*>(a.o_norm + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
   if (timed_out && lane == 0) {
     ctl[0] = 1;
     atomicOr(a.err, KDA_ERR_TIMEOUT);
@@ -899,10 +902,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     for (int e = 0; e < 4; ++e) o[e] = bf(ob[t * HD + lane * 4 + e]);
     const float ss = warp_sum(o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3]);
     const float rstd = rsqrtf(ss * (1.0f / HD) + a.eps);
+    const float wn[4] = {onw.x, onw.y, onw.z, onw.w};
     __align__(8) __nv_bfloat16 y[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      y[e] = __float2bfloat16_rn(o[e] * rstd * a.o_norm[lane * 4 + e] * sigmoid_fast(bf(gate_s[t * HD + lane * 4 + e])));
+      y[e] = __float2bfloat16_rn(o[e] * rstd * wn[e] * __half2float(gsig_s[t * HD + lane * 4 + e]));
     *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
   }
   if constexpr (L == 1) {
