@@ -70,9 +70,11 @@ typedef struct kda_handle kda_handle;
 
 /*
  * kda_prepare -- copy the layer's weights into handle-owned device buffers,
- * re-laying out the conv weight [3D, 1, W] into [3, W, D] (q, k, v blocks,
- * taps outer, channel contiguous), as PreparedKda.__init__ /
- * decode_conv_weight do ("...cutedsl.kda.prepared" page).
+ * re-laying out the conv weight [3D, 1, W] so that each channel's W taps sit
+ * right-aligned in four bf16 (one 8-byte word a channel), as PreparedKda.__init__
+ * re-lays its conv weight out once for its kernel (decode_conv_weight,
+ * "...cutedsl.kda.prepared" page), and taking the Euclidean norm of each f_b
+ * row.
  *
  *   heads             H >= 1 (D = 128 H)
  *   conv_width        W in 2..4
