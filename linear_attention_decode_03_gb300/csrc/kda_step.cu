@@ -405,10 +405,11 @@ __device__ __forceinline__ float silu_bf16_exact(float b, unsigned wp0, unsigned
     sum = t;
   }
   const float y = sum + err;  // within u |y| (1 + 4u) of the exact sum
-  const float sg = 1.0f / (1.0f + expf(-y));
+  const float d = 1.0f + expf(-y);
+  float sg = __frcp_rn(d);
   const float sy = fmaf(sum, sg, err * sg);
-  // sigmoid: 2^-22 (expf) + u (1 + e^-y) + u (division) + |y| u (the error of
-  // y, through sigma' / sigma = 1 - sigma); the product one more u:
+  // sigmoid: 2^-22 (expf) + u (1 + e^-y) + u (the reciprocal) + |y| u (the
+  // error of y, through sigma' / sigma = 1 - sigma); the product one more u:
   // |sy - silu(exact y)| <= (2^-22 + 3u + |y| u) |sy|; margin x2
   if (fabsf(y) < 80.0f && !bf16_rounding_uncertain(sy, 2.0f * (0x1p-22f + (3.0f + fabsf(y)) * U32) * fabsf(sy)))
     return bf_round(sy);
@@ -417,7 +418,7 @@ __device__ __forceinline__ float silu_bf16_exact(float b, unsigned wp0, unsigned
   yd = fma((double)bf_hi(wp0), (double)bf_hi(s01), yd);
   yd = fma((double)bf_lo(wp1), (double)bf_lo(s23), yd);
   yd = fma((double)bf_hi(wp1), (double)bf_hi(s23), yd);
-  return bf16_round_f64(yd / (1.0 + exp(-yd)));
+  return bf16_round_f64(yd * __drcp_rn(1.0 + exp(-yd)));  // y / (1 + e^-y) within 2 fp64 ulp
 }
 // The same out of line: with many tokens the unrolled conv is long enough for
 // instruction fetch to matter, and the rare path is better kept out of it.
