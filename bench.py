@@ -162,7 +162,7 @@ class DeviceWorkload:
     """One workload's inputs resident on the device (pools sentinel-filled,
     read slots filled from the seeded generator)."""
 
-    def __init__(self, si: I.StepInputs, device):
+    def __init__(self, si: I.StepInputs, device, gate_mode: int = 0):
         import torch
         import linear_attention_decode_03_gb300 as kda
 
@@ -177,7 +177,7 @@ class DeviceWorkload:
         self.prep = kda.PreparedKda(bf16(wt.conv_w), None if wt.bias is None else bf16(wt.bias), bf16(wt.f_b),
                                     torch.from_numpy(wt.A_log).to(device), torch.from_numpy(wt.dt_bias).to(device),
                                     torch.from_numpy(wt.o_norm).to(device), gate_lower_bound=wt.gate_lower_bound,
-                                    eps=wt.eps, conv_dim_first=True)
+                                    eps=wt.eps, conv_dim_first=True, gate_mode=gate_mode)
         self.projected = bf16(si.projected)
         self.state = torch.empty((w.pool, w.heads, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=device)
         self.state.view(torch.int32).fill_(int(I.STATE_SENTINEL.view(np.int32)))
@@ -289,7 +289,8 @@ def workload_config(w: I.Workload, args):
             "algorithmic_bytes_per_step": allb,
             "l2": ("inputs larger than L2 (%.0f MB of state per step)" % (state / 1e6)) if big
             else "L2 flushed between timed steps (256 MiB write, then 256 MiB read; outside the per-step events)",
-            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+            "parallelism": "replicas" if args.gpus > 1 else "single GPU",
+            "gate": getattr(args, "gate_mode", "sigmoid")}
 
 
 # -------------------------------------------------------------------- main
@@ -302,6 +303,8 @@ def main():
     ap.add_argument("--workload", default="large_decode", choices=sorted(I.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--gate-mode", choices=["sigmoid", "softplus"], default="sigmoid",
+                    help="decay gate form (kda_set_gate_mode); the default is the reading the step follows")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = I.WORKLOADS[args.workload]
@@ -329,7 +332,7 @@ def main():
     kda.load_library()
 
     si = I.make_step_inputs(w)
-    dw = DeviceWorkload(si, device)
+    dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1)
     state_b, all_b = algorithmic_bytes(w)
     flush = state_b <= L2_BYTES
     # L2 flush between timed steps: write a buffer larger than L2, then read a

@@ -128,6 +128,19 @@ int kda_step(kda_handle* handle, const void* projected, long long rows, long lon
  */
 int kda_check(kda_handle* handle, void* cuda_stream, unsigned* device_flags);
 
+/*
+ * kda_set_gate_mode -- choose the decay gate the handle's steps compute.  The
+ * K1 page names a "lower-bound gate" and PreparedKda takes gate_lower_bound
+ * (lb) without giving the formula, so both forms it admits are offered:
+ *   KDA_GATE_SIGMOID  (default)  g = lb * sigmoid(e^{A_log[h]} (z + dt_bias[c])), in (lb, 0)
+ *   KDA_GATE_SOFTPLUS            g = max(-e^{A_log[h]} softplus(z + dt_bias[c]), lb), in [lb, 0)
+ * Applies to steps enqueued after the call.  Returns KDA_OK, or KDA_EINVAL
+ * for a NULL handle or an unknown mode.  No CUDA call.
+ */
+#define KDA_GATE_SIGMOID 0
+#define KDA_GATE_SOFTPLUS 1
+int kda_set_gate_mode(kda_handle* handle, int mode);
+
 /* kda_destroy -- free the handle's device buffers (synchronises the device). NULL is a no-op. */
 void kda_destroy(kda_handle* handle);
 

@@ -8,7 +8,7 @@ missing or fails to load, every call raises.
 
 Low-level functions carry the C names (:func:`kda_prepare`, :func:`kda_step`,
 :func:`kda_check`, :func:`kda_destroy`, :func:`kda_strerror`,
-:func:`kda_launch_info`) and take raw device pointers.  :class:`PreparedKda`
+:func:`kda_launch_info`, :func:`kda_set_gate_mode`) and take raw device pointers.  :class:`PreparedKda`
 mirrors the PreparedKda wrapper on the
 "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.prepared" page:
 weights prepared once, then ``run(projected, out, caches=..., slots=...,
@@ -25,14 +25,15 @@ from ._build import LIB_PATH, build
 
 __all__ = [
     "KdaError", "build", "load_library", "kda_prepare", "kda_step", "kda_check", "kda_destroy",
-    "kda_strerror", "kda_launch_info", "PreparedKda", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
-    "KDA_ERR_TIMEOUT", "KDA_MAX_TOKENS", "HEAD_DIM",
+    "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "PreparedKda", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
+    "KDA_ERR_TIMEOUT", "KDA_MAX_TOKENS", "KDA_GATE_SIGMOID", "KDA_GATE_SOFTPLUS", "HEAD_DIM",
 ]
 
 HEAD_DIM = 128
 KDA_OK, KDA_EINVAL, KDA_ECUDA = 0, -1, -2
 KDA_ERR_SLOT, KDA_ERR_ACCEPTED, KDA_ERR_TIMEOUT = 1, 2, 4
 KDA_MAX_TOKENS = 8
+KDA_GATE_SIGMOID, KDA_GATE_SOFTPLUS = 0, 1
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -64,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_strerror.restype = ctypes.c_char_p
     lib.kda_launch_info.argtypes = [i32, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
     lib.kda_launch_info.restype = i32
+    lib.kda_set_gate_mode.argtypes = [vp, i32]
+    lib.kda_set_gate_mode.restype = i32
     _lib = lib
     return lib
 
@@ -90,6 +93,13 @@ def kda_step(handle: int, projected: int, rows: int, pitch: int, conv_state: int
                                  state_pool, pool_slots, slots, L, accepted or None, out, stream or None)
     if rc != KDA_OK:
         raise KdaError("kda_step", rc)
+
+
+def kda_set_gate_mode(handle: int, mode: int) -> None:
+    """KDA_GATE_SIGMOID (default) or KDA_GATE_SOFTPLUS for the handle's later steps."""
+    rc = load_library().kda_set_gate_mode(handle, int(mode))
+    if rc != KDA_OK:
+        raise KdaError("kda_set_gate_mode", rc)
 
 
 def kda_check(handle: int, stream: int = 0) -> int:
@@ -131,11 +141,13 @@ class PreparedKda:
 
     ``conv_w`` [3D, 1, W] bf16, ``conv_bias`` [3D] bf16 or None, ``f_b`` [D, 128]
     bf16, ``A_log`` [H] f32, ``dt_bias`` [D] f32, ``o_norm`` [128] f32 (cast
-    to fp32 as the page's __init__ does).
+    to fp32 as the page's __init__ does).  ``gate_mode`` picks the decay gate
+    (``KDA_GATE_SIGMOID``, the default, or ``KDA_GATE_SOFTPLUS``; see
+    ``include/kda.h``).
     """
 
     def __init__(self, conv_w, conv_bias, f_b, A_log, dt_bias, o_norm, *, gate_lower_bound: float = -5.0,
-                 eps: float = 1e-6, conv_dim_first: bool = True):
+                 eps: float = 1e-6, conv_dim_first: bool = True, gate_mode: int = KDA_GATE_SIGMOID):
         import torch
 
         self.heads = int(A_log.numel())
@@ -159,6 +171,8 @@ class PreparedKda:
             self.handle = kda_prepare(self.heads, self.width, cw.data_ptr(), bias_ptr, fb.data_ptr(),
                                       al.data_ptr(), dt.data_ptr(), on.data_ptr(), float(gate_lower_bound),
                                       float(eps))
+            if gate_mode != KDA_GATE_SIGMOID:
+                kda_set_gate_mode(self.handle, gate_mode)
 
     def run(self, projected, out, *, caches, slots, accepted=None, stream=None):
         """One step.  ``caches`` = (conv_state, state_pool); decode when

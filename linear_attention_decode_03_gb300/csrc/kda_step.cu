@@ -77,6 +77,7 @@ struct StepArgs {
   unsigned* err;
   float lb, eps, q_scale;
   int heads, D, W, conv_dim_first;
+  int gate_mode;  // KDA_GATE_SIGMOID or KDA_GATE_SOFTPLUS
 };
 
 // Shared-memory carve-up for L tokens (byte offsets from the dynamic base).
@@ -208,6 +209,9 @@ __device__ __forceinline__ float warp_sum(float x) {
 // __fdividef within 2 ulp (CUDA's documented bounds), so with the rounding of
 // 1 + e^-x the result is within 2.35 |x| u + 2^-21 + u relative (u = 2^-24).
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// softplus(x) = log(1 + e^x) = max(x, 0) + log(1 + e^-|x|), fast intrinsics.
+__device__ __forceinline__ float softplus_fast(float x) { return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x))); }
 
 // sqrt(s) for s >= 0 within 2^-21 relative (rsqrtf is within 2 ulp).
 __device__ __forceinline__ float sqrt_fast(float s) { return s > 0.0f ? s * rsqrtf(s) : 0.0f; }
@@ -727,7 +731,9 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         if (lane == li) z = ex;
       }
       if (pair || (lane & 1) == 0) {
-        const float g = a.lb * sigmoid_fast(expA * (z + dtc));
+        const float x = z + dtc;
+        const float g = (a.gate_mode == KDA_GATE_SOFTPLUS) ? fmaxf(-expA * softplus_fast(x), a.lb)
+                                                          : a.lb * sigmoid_fast(expA * x);
         eg[tt * HD + zc] = __expf(g);
       }
     }
@@ -984,6 +990,7 @@ struct kda_handle {
   float* o_norm;
   unsigned* err;
   float lb, eps;
+  int gate_mode;
 };
 
 extern "C" {
@@ -1026,6 +1033,7 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
   h->heads = heads;
   h->W = conv_width;
   h->lb = gate_lower_bound;
+  h->gate_mode = KDA_GATE_SIGMOID;
   h->eps = eps;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device);
@@ -1097,6 +1105,7 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
   a.o_norm = h->o_norm;
   a.err = h->err;
   a.lb = h->lb;
+  a.gate_mode = h->gate_mode;
   a.eps = h->eps;
   a.q_scale = 0.08838834764831845f;  // 128^-0.5
   a.heads = h->heads;
@@ -1119,6 +1128,12 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
     default: e = launch<8>(a, ctas, s); break;
   }
   return e == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+int kda_set_gate_mode(kda_handle* h, int mode) {
+  if (h == nullptr || (mode != KDA_GATE_SIGMOID && mode != KDA_GATE_SOFTPLUS)) return KDA_EINVAL;
+  h->gate_mode = mode;
+  return KDA_OK;
 }
 
 int kda_check(kda_handle* h, void* cuda_stream, unsigned* device_flags) {

@@ -111,8 +111,10 @@ def bf16_round(x: float) -> int:
 
 
 def step(w: Weights, projected, conv_state, state_pool, slots, L: int, accepted=None, *,
-         dim_first: bool = True, act: str = "silu", diag: bool = False):
+         dim_first: bool = True, act: str = "silu", gate_mode: int = 0, diag: bool = False):
     """One decode (accepted None, L = 1) or verify step of the C oracle.
+
+    gate_mode 0: g = lb * sigmoid(e^A (z + dt)); 1: g = max(-e^A softplus(z + dt), lb).
 
     conv_state and state_pool are copied, not modified.  Returns
     ``(out, conv_state, state_pool, err[, diag])`` where ``diag`` is
@@ -140,7 +142,7 @@ def step(w: Weights, projected, conv_state, state_pool, slots, L: int, accepted=
     rc = lib.kda_oracle_step(
         ctypes.c_int(heads), ctypes.c_int(w.width), _ptr(conv_w), _ptr(bias), _ptr(f_b),
         _ptr(A_log), _ptr(dt_bias), _ptr(o_norm), ctypes.c_float(w.gate_lower_bound),
-        ctypes.c_float(w.eps), ctypes.c_int(1 if act == "silu" else 0), _ptr(projected),
+        ctypes.c_float(w.eps), ctypes.c_int(1 if act == "silu" else 0), ctypes.c_int(int(gate_mode)), _ptr(projected),
         ctypes.c_int64(rows), ctypes.c_int64(pitch), _ptr(conv_state), ctypes.c_int(1 if dim_first else 0),
         _ptr(state_pool), ctypes.c_int64(pool), _ptr(slots), ctypes.c_int(L), _ptr(acc), _ptr(out),
         ctypes.byref(err), _ptr(dg),

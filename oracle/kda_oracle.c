@@ -26,7 +26,9 @@
  *
  * Readings taken where the pages are silent (each one is listed in the
  * design notes of the repository):
- *  - gate:  g = lb * sigmoid(exp(A_log[h]) * (z + dt_bias[c])), range (lb, 0).
+ *  - gate:  g = lb * sigmoid(exp(A_log[h]) * (z + dt_bias[c])), range (lb, 0)
+ *           (gate_mode 0, the reading taken); gate_mode 1 is the other form the
+ *           pages leave open: g = max(-exp(A_log[h]) * softplus(z + dt_bias[c]), lb).
  *  - conv:  causal depthwise, tap W-1 multiplies the current token, window
  *           oldest first; activation SiLU (act = 1) or none (act = 0, pins).
  *  - l2norm: x / sqrt(sum x^2 + 1e-6); q is scaled by 128^-0.5 afterwards.
@@ -85,6 +87,7 @@ static uint16_t bf16_round(double x) {
 static double bf16_rounded(double x) { return bf16_value(bf16_round(x)); }
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
 
 /* Exported so that tests can pin the rounding rule itself. */
 uint16_t kda_oracle_bf16_round(double x) { return bf16_round(x); }
@@ -99,6 +102,7 @@ uint16_t kda_oracle_bf16_round(double x) { return bf16_round(x); }
  *   A_log             [H] fp32;  dt_bias [D] fp32;  o_norm [128] fp32
  *   lb, eps           gate lower bound and o_norm epsilon (fp32 scalars)
  *   act               1 = SiLU after the conv (the model), 0 = none (pins only)
+ *   gate_mode         0 = lb * sigmoid form, 1 = clamped softplus form (see above)
  *   projected         [rows, pitch] bf16: cols [0,3D) q|k|v, [3D,4D) out-gate,
  *                     [4D, 4D+128) f_a, [4D+128, 4D+128+H) beta
  *   conv_state        bf16 [pool, 3D, W-1] (dim_first) or [pool, W-1, 3D]; updated
@@ -114,7 +118,7 @@ uint16_t kda_oracle_bf16_round(double x) { return bf16_round(x); }
  */
 int kda_oracle_step(int heads, int W, const uint16_t *conv_w, const uint16_t *bias,
                     const uint16_t *f_b, const float *A_log, const float *dt_bias,
-                    const float *o_norm, float lb, float eps, int act,
+                    const float *o_norm, float lb, float eps, int act, int gate_mode,
                     const uint16_t *projected, int64_t rows, int64_t pitch,
                     uint16_t *conv_state, int dim_first, float *state_pool, int64_t pool,
                     const int32_t *slots, int L, const int32_t *accepted, uint16_t *out,
@@ -194,7 +198,10 @@ int kda_oracle_step(int heads, int W, const uint16_t *conv_w, const uint16_t *bi
                     z += bf16_value(f_b[c * HEAD_DIM + j]) * bf16_value(prow[4 * D + j]);
                 z = bf16_rounded(z);
                 const int64_t h = c / HEAD_DIM;
-                g[t * D + c] = (double)lb * sigmoid(exp((double)A_log[h]) * (z + (double)dt_bias[c]));
+                if (gate_mode == 0)
+                    g[t * D + c] = (double)lb * sigmoid(exp((double)A_log[h]) * (z + (double)dt_bias[c]));
+                else
+                    g[t * D + c] = fmax(-exp((double)A_log[h]) * softplus(z + dt_bias[c]), (double)lb);
             }
             for (int64_t h = 0; h < heads; ++h)
                 beta[t * heads + h] = sigmoid(bf16_value(prow[4 * D + HEAD_DIM + h]));

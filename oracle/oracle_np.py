@@ -54,7 +54,7 @@ def _sigmoid(x):
 
 
 def step(w, projected, conv_state, state_pool, slots, L, accepted=None, *, dim_first=True,
-         act="silu", diag=False):
+         act="silu", gate_mode=0, diag=False):
     """Same contract as ``oracle.step`` (the C oracle); inputs are not modified."""
     projected = np.asarray(projected, dtype=np.uint16)
     rows, pitch = projected.shape
@@ -109,7 +109,10 @@ def step(w, projected, conv_state, state_pool, slots, L, accepted=None, *, dim_f
             conv_v[req_slots[t]] = f64_to_bf16(seq[t + 1:t + 1 + SL].T)
 
         z = _bf16_round_value(P[:, 4 * D:4 * D + HEAD_DIM] @ f_b.T)          # [L, D]
-        g = lb * _sigmoid(np.repeat(np.exp(A), HEAD_DIM) * (z + dt))          # [L, D]
+        if gate_mode == 0:
+            g = lb * _sigmoid(np.repeat(np.exp(A), HEAD_DIM) * (z + dt))      # [L, D]
+        else:
+            g = np.maximum(-np.repeat(np.exp(A), HEAD_DIM) * np.logaddexp(0.0, z + dt), lb)
         beta = _sigmoid(P[:, 4 * D + HEAD_DIM:4 * D + HEAD_DIM + H])          # [L, H]
         gate = P[:, 3 * D:4 * D]
 

@@ -35,7 +35,7 @@ def bf16_value(bits) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def prepare(weights: I.LayerWeights, device, dim_first=True) -> kda.PreparedKda:
+def prepare(weights: I.LayerWeights, device, dim_first=True, gate_mode=0) -> kda.PreparedKda:
     return kda.PreparedKda(
         bf16_np_to_torch(weights.conv_w, device),
         None if weights.bias is None else bf16_np_to_torch(weights.bias, device),
@@ -43,17 +43,17 @@ def prepare(weights: I.LayerWeights, device, dim_first=True) -> kda.PreparedKda:
         torch.from_numpy(weights.A_log).to(device),
         torch.from_numpy(weights.dt_bias).to(device),
         torch.from_numpy(weights.o_norm).to(device),
-        gate_lower_bound=weights.gate_lower_bound, eps=weights.eps, conv_dim_first=dim_first)
+        gate_lower_bound=weights.gate_lower_bound, eps=weights.eps, conv_dim_first=dim_first, gate_mode=gate_mode)
 
 
 class DeviceStep:
     """Device copies of one step's inputs (full pools, sentinel-filled)."""
 
-    def __init__(self, si: I.StepInputs, device="cuda:0", dim_first=True, weights=None):
+    def __init__(self, si: I.StepInputs, device="cuda:0", dim_first=True, weights=None, gate_mode=0):
         w = si.workload
         self.si, self.w, self.dim_first = si, w, dim_first
         self.device = torch.device(device)
-        self.prep = prepare(weights or si.weights, self.device, dim_first)
+        self.prep = prepare(weights or si.weights, self.device, dim_first, gate_mode)
         self.projected = bf16_np_to_torch(si.projected, self.device)
         H, sl = w.heads, w.width - 1
         self.state = torch.empty((w.pool, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=self.device)
@@ -83,7 +83,7 @@ class DeviceStep:
         self.prep.close()
 
 
-def oracle_requests(si: I.StepInputs, reqs, dim_first=True):
+def oracle_requests(si: I.StepInputs, reqs, dim_first=True, gate_mode=0):
     """The C oracle on requests `reqs` only, with a pool compacted to the slots
     they touch.  Returns (out rows, used slots, pool [n_used], conv [n_used], err)."""
     w = si.workload
@@ -107,7 +107,8 @@ def oracle_requests(si: I.StepInputs, reqs, dim_first=True):
     W = oracle.Weights(**si.weights.as_dict())
     if not dim_first:
         cconv = np.ascontiguousarray(cconv.transpose(0, 2, 1))
-    out, nconv, npool, err = oracle.step(W, si.projected[rows], cconv, cpool, cslots, L, acc, dim_first=dim_first)
+    out, nconv, npool, err = oracle.step(W, si.projected[rows], cconv, cpool, cslots, L, acc, dim_first=dim_first,
+                                         gate_mode=gate_mode)
     return out, rows, used, npool[: len(used)], nconv[: len(used)], err
 
 

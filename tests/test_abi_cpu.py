@@ -30,7 +30,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["kda_prepare", "kda_step", "kda_check", "kda_destroy", "kda_strerror",
-                            "kda_launch_info"])
+                            "kda_launch_info", "kda_set_gate_mode"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -53,6 +53,7 @@ def test_host_validation_without_gpu(lib):
     lib.kda_destroy(None)
     assert lib.kda_launch_info(0, None, None, None) == -1
     assert lib.kda_launch_info(9, None, None, None) == -1
+    assert lib.kda_set_gate_mode(None, 0) == -1
     assert kda.kda_strerror(0) == "ok"
     assert kda.kda_strerror(-1) == "invalid argument"
     assert kda.kda_strerror(-2) == "CUDA error"

@@ -34,6 +34,8 @@ MUTATIONS = [
     ("q_scale_dropped", "qh[i] = qr[i] * qn * q_scale;", "qh[i] = qr[i] * qn;"),
     ("gate_dt_sign", "(z + (double)dt_bias[c])", "(z - (double)dt_bias[c])"),
     ("gate_bound_ignored", "(double)lb * sigmoid(", "-1.0 * sigmoid("),
+    ("softplus_gate_unclamped", "softplus(z + dt_bias[c]), (double)lb)", "softplus(z + dt_bias[c]), -1e300)"),
+    ("softplus_gate_no_scale", "fmax(-exp((double)A_log[h]) * softplus(", "fmax(-1.0 * softplus("),
     ("gate_one_token", "const double *gr = g + t * D + h * HEAD_DIM;", "const double *gr = g + h * HEAD_DIM;"),
     ("rms_sum_not_mean", "ms /= HEAD_DIM;", "ms /= 1;"),
     ("rms_eps_dropped", "const double rstd = 1.0 / sqrt(ms + (double)eps);", "const double rstd = 1.0 / sqrt(ms);"),

@@ -187,6 +187,25 @@ def test_gate_limits(run):
     assert np.all((g > lb) & (g < 0))
 
 
+def test_gate_limits_softplus_form(run):
+    """gate_mode 1, g = max(-e^A softplus(z + dt), lb): z + dt = 0 gives
+    -e^A ln 2 (per head); z + dt -> +inf is clamped to lb; -> -inf gives 0;
+    otherwise g lies in [lb, 0)."""
+    si, pool, conv = _decode_case(seed=17)
+    lb = -5.0
+    zero_fb = np.zeros_like(si.weights.f_b)
+    A = si.weights.A_log.astype(np.float64)
+    for dt, expect in [(0.0, -np.exp(A) * np.log(2.0)), (1e4, np.full(A.shape, lb)), (-1e4, np.zeros(A.shape))]:
+        W = oracle_weights(si, f_b=zero_fb, dt_bias=np.full_like(si.weights.dt_bias, dt), gate_lower_bound=lb)
+        *_, err, dg = run(W, si.projected, conv, pool, si.slots, 1, None, gate_mode=1, diag=True)
+        g = dg[:, :, 3 * HEAD_DIM:4 * HEAD_DIM]                       # [rows, H, 128]
+        assert err == 0 and np.all(np.abs(g - expect[None, :, None]) <= 1e-12)
+    *_, dg = run(oracle_weights(si, gate_lower_bound=lb), si.projected, conv, pool, si.slots, 1, None,
+                 gate_mode=1, diag=True)
+    g = dg[:, :, 3 * HEAD_DIM:4 * HEAD_DIM]
+    assert np.all((g >= lb) & (g < 0))
+
+
 def test_l2norm_and_q_scale(run):
     si, pool, conv = _decode_case(seed=16)
     *_, dg = run(oracle_weights(si), si.projected, conv, pool, si.slots, 1, None, diag=True)
@@ -367,8 +386,9 @@ def test_c_matches_numpy_on_random_shapes():
         W = oracle_weights(si)
         dim_first = bool(trial % 2 == 0)
         args = (W, si.projected, si.full_conv_state(dim_first), si.full_state_pool(), si.slots, L, si.accepted)
-        a = oracle.step(*args, dim_first=dim_first, diag=True)
-        b = oracle_np.step(*args, dim_first=dim_first, diag=True)
+        gm = trial % 2  # both gate forms
+        a = oracle.step(*args, dim_first=dim_first, gate_mode=gm, diag=True)
+        b = oracle_np.step(*args, dim_first=dim_first, gate_mode=gm, diag=True)
         assert a[3] == b[3] == 0
         da, db = bf16_value(a[0]), bf16_value(b[0])
         assert np.mean(a[0] != b[0]) < 0.01

@@ -29,15 +29,16 @@ def _lib():
     kda.load_library()
 
 
-def _check_full(si: I.StepInputs, dim_first=True, reqs=None):
+def _check_full(si: I.StepInputs, dim_first=True, reqs=None, gate_mode=0):
     """Run the whole step on the GPU; compare requests `reqs` (default all)
     with the oracle and check the untouched part of every pool."""
     w = si.workload
-    ds = G.DeviceStep(si, dim_first=dim_first)
+    ds = G.DeviceStep(si, dim_first=dim_first, gate_mode=gate_mode)
     flags = ds.run()
     if reqs is None:
         reqs = np.arange(w.requests)
-    out_ref, rows, used, pool_ref, conv_ref, err = G.oracle_requests(si, reqs, dim_first=dim_first)
+    out_ref, rows, used, pool_ref, conv_ref, err = G.oracle_requests(si, reqs, dim_first=dim_first,
+                                                                      gate_mode=gate_mode)
     assert flags == err == 0
     out = G.torch_bf16_to_np(ds.out[torch.from_numpy(rows).to(ds.device)])
     G.assert_out_close(out, out_ref)
@@ -96,6 +97,13 @@ def test_conv_widths(width):
 def test_transposed_conv_state_and_bias():
     _check_full(case(heads=3, requests=4, L=4, pool=20, seed=60, with_bias=True), dim_first=False)
     _check_full(case(heads=1, requests=7, L=1, pool=9, seed=61, with_bias=True), dim_first=True)
+
+
+@pytest.mark.parametrize("L", [1, 4])
+def test_softplus_gate_mode(L):
+    """The clamped-softplus gate (kda_set_gate_mode), decode and verify, against
+    the oracle run with the same gate form."""
+    _check_full(case(heads=3, requests=5, L=L, pool=5 * L + 4, seed=70 + L, verify=L > 1), gate_mode=1)
 
 
 def test_verify_with_one_token_accepted_array():
