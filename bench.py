@@ -162,7 +162,7 @@ class DeviceWorkload:
     """One workload's inputs resident on the device (pools sentinel-filled,
     read slots filled from the seeded generator)."""
 
-    def __init__(self, si: I.StepInputs, device, gate_mode: int = 0):
+    def __init__(self, si: I.StepInputs, device, gate_mode: int = 0, plan: bool = False):
         import torch
         import linear_attention_decode_03_gb300 as kda
 
@@ -191,8 +191,15 @@ class DeviceWorkload:
             self.slots = self.slots.view(w.requests, w.L)
         self.accepted = None if si.accepted is None else torch.from_numpy(si.accepted.copy()).to(device)
         self.out = torch.empty((w.rows, w.dim), dtype=torch.bfloat16, device=device)
+        self.plan = None
+        if plan:  # the step recorded once as a CUDA graph (PreparedKda.plan)
+            self.plan = self.prep.plan(self.projected, self.out, caches=(self.conv, self.state), slots=self.slots,
+                                       accepted=self.accepted)
 
     def step(self):
+        if self.plan is not None:
+            self.plan.launch()
+            return
         self.prep.run(self.projected, self.out, caches=(self.conv, self.state), slots=self.slots,
                       accepted=self.accepted)
 
@@ -290,7 +297,8 @@ def workload_config(w: I.Workload, args):
             "l2": ("inputs larger than L2 (%.0f MB of state per step)" % (state / 1e6)) if big
             else "L2 flushed between timed steps (256 MiB write, then 256 MiB read; outside the per-step events)",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU",
-            "gate": getattr(args, "gate_mode", "sigmoid")}
+            "gate": getattr(args, "gate_mode", "sigmoid"),
+            "launch": "plan (CUDA graph)" if getattr(args, "plan", False) else "kda_step"}
 
 
 # -------------------------------------------------------------------- main
@@ -303,6 +311,8 @@ def main():
     ap.add_argument("--workload", default="large_decode", choices=sorted(I.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--plan", action="store_true",
+                    help="launch every step through a launch plan (the step recorded once as a CUDA graph)")
     ap.add_argument("--gate-mode", choices=["sigmoid", "softplus"], default="sigmoid",
                     help="decay gate form (kda_set_gate_mode); the default is the reading the step follows")
     args = ap.parse_args()
@@ -332,7 +342,7 @@ def main():
     kda.load_library()
 
     si = I.make_step_inputs(w)
-    dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1)
+    dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=args.plan)
     state_b, all_b = algorithmic_bytes(w)
     flush = state_b <= L2_BYTES
     # L2 flush between timed steps: write a buffer larger than L2, then read a
@@ -395,12 +405,18 @@ def main():
     h2d = h_proj.numel() * 2 + h_slots.numel() * 4 + (0 if h_acc is None else h_acc.numel() * 4)
     d2h = h_out.numel() * 2
 
+    e2e_plan = (dw.prep.plan(d_proj, dw.out, caches=(dw.conv, dw.state), slots=d_slots, accepted=d_acc)
+                if args.plan else None)
+
     def e2e_step():
         d_proj.copy_(h_proj, non_blocking=True)
         d_slots.view(-1).copy_(h_slots, non_blocking=True)
         if d_acc is not None:
             d_acc.copy_(h_acc, non_blocking=True)
-        dw.prep.run(d_proj, dw.out, caches=(dw.conv, dw.state), slots=d_slots, accepted=d_acc)
+        if e2e_plan is not None:
+            e2e_plan.launch()
+        else:
+            dw.prep.run(d_proj, dw.out, caches=(dw.conv, dw.state), slots=d_slots, accepted=d_acc)
         h_out.copy_(dw.out, non_blocking=True)
 
     for _ in range(3):

@@ -141,6 +141,31 @@ int kda_check(kda_handle* handle, void* cuda_stream, unsigned* device_flags);
 #define KDA_GATE_SOFTPLUS 1
 int kda_set_gate_mode(kda_handle* handle, int mode);
 
+/*
+ * Launch plans.  A plan records one kda_step, with exactly these arguments,
+ * as a CUDA graph (captured once on a private stream and instantiated), so
+ * that each later step is a single graph launch: the analogue of the
+ * per-shape prepared executables of PreparedKda (prepare_caches / run on the
+ * "...cutedsl.kda.prepared" page), for small batches where the launch costs
+ * as much as the kernel.  The pointers, sizes and the handle's gate mode are
+ * fixed when the plan is made; the buffers' contents may change between
+ * launches (write the next step's inputs into the same buffers).  The
+ * buffers and the handle must outlive the plan.
+ *
+ * kda_plan_create -- arguments as kda_step (no stream).  Returns KDA_OK and
+ *   *plan, KDA_EINVAL (the arguments kda_step rejects, or plan == NULL) or
+ *   KDA_ECUDA.
+ * kda_plan_launch -- enqueue the recorded step on cuda_stream (NULL = the
+ *   legacy default stream).  Returns KDA_OK, KDA_EINVAL (NULL plan) or KDA_ECUDA.
+ * kda_plan_destroy -- free the plan (NULL is a no-op).
+ */
+typedef struct kda_plan kda_plan;
+int kda_plan_create(kda_handle* handle, const void* projected, long long rows, long long pitch,
+                    void* conv_state, int conv_dim_first, float* state_pool, long long pool_slots,
+                    const int* slots, int L, const int* accepted, void* out, kda_plan** plan);
+int kda_plan_launch(kda_plan* plan, void* cuda_stream);
+void kda_plan_destroy(kda_plan* plan);
+
 /* kda_destroy -- free the handle's device buffers (synchronises the device). NULL is a no-op. */
 void kda_destroy(kda_handle* handle);
 

@@ -8,12 +8,14 @@ missing or fails to load, every call raises.
 
 Low-level functions carry the C names (:func:`kda_prepare`, :func:`kda_step`,
 :func:`kda_check`, :func:`kda_destroy`, :func:`kda_strerror`,
-:func:`kda_launch_info`, :func:`kda_set_gate_mode`) and take raw device pointers.  :class:`PreparedKda`
+:func:`kda_launch_info`, :func:`kda_set_gate_mode`, :func:`kda_plan_create`,
+:func:`kda_plan_launch`, :func:`kda_plan_destroy`) and take raw device pointers.  :class:`PreparedKda`
 mirrors the PreparedKda wrapper on the
 "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.prepared" page:
 weights prepared once, then ``run(projected, out, caches=..., slots=...,
 accepted=None)`` per step, with ``accepted[:R]`` and contiguous ``slots[:R]``
-for verify steps.
+for verify steps; ``plan(...)`` records a step with fixed buffers as a CUDA
+graph (:class:`KdaPlan`) that each later step launches in one call.
 """
 from __future__ import annotations
 
@@ -25,7 +27,8 @@ from ._build import LIB_PATH, build
 
 __all__ = [
     "KdaError", "build", "load_library", "kda_prepare", "kda_step", "kda_check", "kda_destroy",
-    "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "PreparedKda", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
+    "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "kda_plan_create", "kda_plan_launch",
+    "kda_plan_destroy", "PreparedKda", "KdaPlan", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
     "KDA_ERR_TIMEOUT", "KDA_MAX_TOKENS", "KDA_GATE_SIGMOID", "KDA_GATE_SOFTPLUS", "HEAD_DIM",
 ]
 
@@ -67,6 +70,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_launch_info.restype = i32
     lib.kda_set_gate_mode.argtypes = [vp, i32]
     lib.kda_set_gate_mode.restype = i32
+    lib.kda_plan_create.argtypes = [vp, vp, ll, ll, vp, i32, vp, ll, vp, i32, vp, vp, ctypes.POINTER(vp)]
+    lib.kda_plan_create.restype = i32
+    lib.kda_plan_launch.argtypes = [vp, vp]
+    lib.kda_plan_launch.restype = i32
+    lib.kda_plan_destroy.argtypes = [vp]
+    lib.kda_plan_destroy.restype = None
     _lib = lib
     return lib
 
@@ -93,6 +102,27 @@ def kda_step(handle: int, projected: int, rows: int, pitch: int, conv_state: int
                                  state_pool, pool_slots, slots, L, accepted or None, out, stream or None)
     if rc != KDA_OK:
         raise KdaError("kda_step", rc)
+
+
+def kda_plan_create(handle: int, projected: int, rows: int, pitch: int, conv_state: int, conv_dim_first: bool,
+                    state_pool: int, pool_slots: int, slots: int, L: int, accepted: Optional[int], out: int) -> int:
+    """Record one step (arguments as kda_step, no stream) as a CUDA graph; an opaque plan (int) out."""
+    p = ctypes.c_void_p()
+    rc = load_library().kda_plan_create(handle, projected, rows, pitch, conv_state, 1 if conv_dim_first else 0,
+                                        state_pool, pool_slots, slots, L, accepted or None, out, ctypes.byref(p))
+    if rc != KDA_OK:
+        raise KdaError("kda_plan_create", rc)
+    return p.value
+
+
+def kda_plan_launch(plan: int, stream: int = 0) -> None:
+    rc = load_library().kda_plan_launch(plan, stream or None)
+    if rc != KDA_OK:
+        raise KdaError("kda_plan_launch", rc)
+
+
+def kda_plan_destroy(plan: int) -> None:
+    load_library().kda_plan_destroy(plan)
 
 
 def kda_set_gate_mode(handle: int, mode: int) -> None:
@@ -174,10 +204,9 @@ class PreparedKda:
             if gate_mode != KDA_GATE_SIGMOID:
                 kda_set_gate_mode(self.handle, gate_mode)
 
-    def run(self, projected, out, *, caches, slots, accepted=None, stream=None):
-        """One step.  ``caches`` = (conv_state, state_pool); decode when
-        ``accepted`` is None (``slots`` [>= B]), verify otherwise (``slots``
-        [>= R, L], ``accepted`` [>= R])."""
+    def _args(self, projected, out, caches, slots, accepted):
+        """kda_step's arguments (pointers and sizes) for these tensors, and the
+        tensors they point into (kept alive by a plan)."""
         import torch
 
         conv, state = caches[:2]
@@ -198,15 +227,36 @@ class PreparedKda:
         _dev(out, torch.bfloat16, "out")
         _dev(conv, torch.bfloat16, "conv_state")
         _dev(state, torch.float32, "state_pool")
+        args = (projected.data_ptr(), batch, projected.stride(0), conv.data_ptr(), self.conv_dim_first,
+                state.data_ptr(), state.shape[0], slots.data_ptr(), L,
+                None if accepted is None else accepted.data_ptr(), out.data_ptr())
+        return args, (projected, out, conv, state, slots, accepted)
+
+    def run(self, projected, out, *, caches, slots, accepted=None, stream=None):
+        """One step.  ``caches`` = (conv_state, state_pool); decode when
+        ``accepted`` is None (``slots`` [>= B]), verify otherwise (``slots``
+        [>= R, L], ``accepted`` [>= R])."""
+        import torch
+
+        args, _ = self._args(projected, out, caches, slots, accepted)
         if stream is None:
             stream = torch.cuda.current_stream(self.device).cuda_stream
-        kda_step(self.handle, projected.data_ptr(), batch, projected.stride(0), conv.data_ptr(),
-                 self.conv_dim_first, state.data_ptr(), state.shape[0], slots.data_ptr(), L,
-                 None if accepted is None else accepted.data_ptr(), out.data_ptr(), stream)
+        kda_step(self.handle, *args, stream)
         return out
 
+    def plan(self, projected, out, *, caches, slots, accepted=None) -> "KdaPlan":
+        """Record a step on these buffers (arguments as ``run``) as a CUDA graph.
+        Each ``launch()`` of the plan is one step on whatever the buffers then
+        hold; the gate mode is the one set when the plan is made."""
+        import torch
+
+        args, keep = self._args(projected, out, caches, slots, accepted)
+        with torch.cuda.device(self.device):
+            p = kda_plan_create(self.handle, *args)
+        return KdaPlan(p, keep + (self,), self.device)
+
     def check(self, stream=None) -> int:
-        """Synchronise the stream; return and clear the device error bits."""
+        """Synchronise the stream; return and clear the device error bits (plan launches included)."""
         import torch
 
         if stream is None:
@@ -217,6 +267,32 @@ class PreparedKda:
         if getattr(self, "handle", None):
             kda_destroy(self.handle)
             self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class KdaPlan:
+    """One step of a PreparedKda recorded as a CUDA graph on fixed buffers
+    (``PreparedKda.plan``).  Keeps the buffers and the prepared handle alive."""
+
+    def __init__(self, plan: int, keep, device):
+        self.plan, self._keep, self.device = plan, keep, device
+
+    def launch(self, stream=None) -> None:
+        import torch
+
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device).cuda_stream
+        kda_plan_launch(self.plan, stream)
+
+    def close(self) -> None:
+        if getattr(self, "plan", None):
+            kda_plan_destroy(self.plan)
+            self.plan = None
 
     def __del__(self):
         try:

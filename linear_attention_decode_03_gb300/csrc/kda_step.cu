@@ -1130,6 +1130,53 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
   return e == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
+struct kda_plan {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+int kda_plan_create(kda_handle* h, const void* projected, long long rows, long long pitch, void* conv_state,
+                    int conv_dim_first, float* state_pool, long long pool_slots, const int* slots, int L,
+                    const int* accepted, void* out, kda_plan** plan) {
+  if (plan == nullptr) return KDA_EINVAL;
+  *plan = nullptr;
+  if (h == nullptr) return KDA_EINVAL;
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return KDA_ECUDA;
+  cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+  int rc = KDA_ECUDA;
+  cudaGraph_t g = nullptr;
+  if (e == cudaSuccess) {
+    rc = kda_step(h, projected, rows, pitch, conv_state, conv_dim_first, state_pool, pool_slots, slots, L, accepted,
+                  out, s);
+    e = cudaStreamEndCapture(s, &g);  // always ends the capture, whatever kda_step returned
+  }
+  cudaStreamDestroy(s);
+  if (rc != KDA_OK || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return rc != KDA_OK ? rc : KDA_ECUDA;
+  }
+  cudaGraphExec_t x = nullptr;
+  if (cudaGraphInstantiate(&x, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return KDA_ECUDA;
+  }
+  *plan = new kda_plan{g, x};
+  return KDA_OK;
+}
+
+int kda_plan_launch(kda_plan* p, void* cuda_stream) {
+  if (p == nullptr) return KDA_EINVAL;
+  return cudaGraphLaunch(p->exec, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+void kda_plan_destroy(kda_plan* p) {
+  if (p == nullptr) return;
+  cudaGraphExecDestroy(p->exec);
+  cudaGraphDestroy(p->graph);
+  delete p;
+}
+
 int kda_set_gate_mode(kda_handle* h, int mode) {
   if (h == nullptr || (mode != KDA_GATE_SIGMOID && mode != KDA_GATE_SOFTPLUS)) return KDA_EINVAL;
   h->gate_mode = mode;

@@ -106,6 +106,31 @@ def test_softplus_gate_mode(L):
     _check_full(case(heads=3, requests=5, L=L, pool=5 * L + 4, seed=70 + L, verify=L > 1), gate_mode=1)
 
 
+@pytest.mark.parametrize("L", [1, 4])
+def test_plan_replays_equal_steps(L):
+    """A launch plan (one step recorded as a CUDA graph on fixed buffers) gives
+    the bits kda_step gives, and each launch is a step on what the buffers
+    then hold (new projected rows written between launches)."""
+    si = case(heads=2, requests=4, L=L, pool=4 * L + 3, seed=80 + L, verify=L > 1)
+    a, b = G.DeviceStep(si), G.DeviceStep(si)
+    plan = b.prep.plan(b.projected, b.out, caches=(b.conv, b.state), slots=b.slots, accepted=b.accepted)
+    gen = torch.Generator(device="cpu").manual_seed(L)
+    for step in range(3):
+        if step == 2:  # the same new inputs into both sets of buffers
+            fresh = torch.randn(a.projected.shape, generator=gen).to(torch.bfloat16).to(a.device)
+            a.projected.copy_(fresh)
+            b.projected.copy_(fresh)
+        assert a.run() == 0
+        plan.launch()
+        assert b.prep.check() == 0
+        assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+        assert torch.equal(a.state.view(torch.int32), b.state.view(torch.int32))
+        assert torch.equal(a.conv.view(torch.int16), b.conv.view(torch.int16))
+    plan.close()
+    a.close()
+    b.close()
+
+
 def test_verify_with_one_token_accepted_array():
     _check_full(case(heads=2, requests=6, L=1, pool=8, seed=62, verify=True))
 
