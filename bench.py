@@ -162,7 +162,7 @@ class DeviceWorkload:
     """One workload's inputs resident on the device (pools sentinel-filled,
     read slots filled from the seeded generator)."""
 
-    def __init__(self, si: I.StepInputs, device, gate_mode: int = 0, plan: bool = False):
+    def __init__(self, si: I.StepInputs, device, gate_mode: int = 0, plan: bool = False, state_dtype: str = "f32"):
         import torch
         import linear_attention_decode_03_gb300 as kda
 
@@ -177,12 +177,17 @@ class DeviceWorkload:
         self.prep = kda.PreparedKda(bf16(wt.conv_w), None if wt.bias is None else bf16(wt.bias), bf16(wt.f_b),
                                     torch.from_numpy(wt.A_log).to(device), torch.from_numpy(wt.dt_bias).to(device),
                                     torch.from_numpy(wt.o_norm).to(device), gate_lower_bound=wt.gate_lower_bound,
-                                    eps=wt.eps, conv_dim_first=True, gate_mode=gate_mode)
+                                    eps=wt.eps, conv_dim_first=True, gate_mode=gate_mode, state_dtype=state_dtype)
         self.projected = bf16(si.projected)
-        self.state = torch.empty((w.pool, w.heads, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=device)
-        self.state.view(torch.int32).fill_(int(I.STATE_SENTINEL.view(np.int32)))
         idx = torch.from_numpy(si.read_slots).to(device)
-        self.state[idx] = torch.from_numpy(si.states).to(device)
+        if state_dtype == "bf16":
+            self.state = torch.empty((w.pool, w.heads, HEAD_DIM, HEAD_DIM), dtype=torch.bfloat16, device=device)
+            self.state.view(torch.int16).fill_(int(np.array(I.STATE_SENTINEL_BF16).view(np.int16)))
+            self.state[idx] = bf16(si.states_bf16())
+        else:
+            self.state = torch.empty((w.pool, w.heads, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=device)
+            self.state.view(torch.int32).fill_(int(I.STATE_SENTINEL.view(np.int32)))
+            self.state[idx] = torch.from_numpy(si.states).to(device)
         self.conv = torch.empty((w.pool, 3 * w.dim, w.width - 1), dtype=torch.bfloat16, device=device)
         self.conv.view(torch.int16).fill_(int(np.array(I.CONV_SENTINEL).view(np.int16)))
         self.conv[idx] = bf16(si.windows)
@@ -204,12 +209,14 @@ class DeviceWorkload:
                       accepted=self.accepted)
 
 
-def algorithmic_bytes(w: I.Workload):
-    return w.state_bytes, w.state_bytes + w.other_bytes
+def algorithmic_bytes(w: I.Workload, state_dtype: str = "f32"):
+    """(state bytes, all bytes) per step; a bf16 state pool moves half the state bytes."""
+    state = w.state_bytes // 2 if state_dtype == "bf16" else w.state_bytes
+    return state, state + w.other_bytes
 
 
 # ----------------------------------------------------------- CPU oracle arm
-def oracle_sample_inputs(si: I.StepInputs, reqs):
+def oracle_sample_inputs(si: I.StepInputs, reqs, state_dtype: str = "f32"):
     """Inputs of requests `reqs` with the pools compacted to the slots they touch."""
     w = si.workload
     L = w.L
@@ -217,12 +224,17 @@ def oracle_sample_inputs(si: I.StepInputs, reqs):
     used = np.unique(slots2)
     pos = {int(s): i for i, s in enumerate(used)}
     read_pos = {int(s): i for i, s in enumerate(si.read_slots)}
-    cpool = np.empty((len(used), w.heads, HEAD_DIM, HEAD_DIM), dtype=np.float32)
-    cpool.view(np.uint32)[...] = I.STATE_SENTINEL
+    if state_dtype == "bf16":
+        cpool = np.full((len(used), w.heads, HEAD_DIM, HEAD_DIM), I.STATE_SENTINEL_BF16, dtype=np.uint16)
+        states = si.states_bf16()
+    else:
+        cpool = np.empty((len(used), w.heads, HEAD_DIM, HEAD_DIM), dtype=np.float32)
+        cpool.view(np.uint32)[...] = I.STATE_SENTINEL
+        states = si.states
     cconv = np.full((len(used), 3 * w.dim, w.width - 1), I.CONV_SENTINEL, dtype=np.uint16)
     for s, i in pos.items():
         if s in read_pos:
-            cpool[i] = si.states[read_pos[s]]
+            cpool[i] = states[read_pos[s]]
             cconv[i] = si.windows[read_pos[s]]
     cslots = np.array([pos[int(s)] for s in slots2.reshape(-1)], dtype=np.int32)
     rows = (np.asarray(reqs)[:, None] * L + np.arange(L)[None, :]).reshape(-1)
@@ -230,28 +242,28 @@ def oracle_sample_inputs(si: I.StepInputs, reqs):
     return si.projected[rows], cconv, cpool, cslots, acc
 
 
-def time_oracle(si: I.StepInputs, n_requests: int, repeats: int = 1):
+def time_oracle(si: I.StepInputs, n_requests: int, repeats: int = 1, state_dtype: str = "f32"):
     """Seconds per token of the C oracle over `n_requests` requests (1 thread)."""
     import oracle
 
     W = oracle.Weights(**si.weights.as_dict())
     reqs = np.arange(min(n_requests, si.workload.requests))
-    proj, cconv, cpool, cslots, acc = oracle_sample_inputs(si, reqs)
+    proj, cconv, cpool, cslots, acc = oracle_sample_inputs(si, reqs, state_dtype)
     t0 = time.perf_counter()
     for _ in range(repeats):
-        oracle.step(W, proj, cconv, cpool, cslots, si.workload.L, acc)
+        oracle.step(W, proj, cconv, cpool, cslots, si.workload.L, acc, state_dtype=state_dtype)
     dt = time.perf_counter() - t0
     return dt, len(reqs) * si.workload.L * repeats
 
 
-def cpu_baseline(si: I.StepInputs, budget_s: float = 12.0):
+def cpu_baseline(si: I.StepInputs, budget_s: float = 12.0, state_dtype: str = "f32"):
     """The oracle on a bounded sample of about `budget_s` seconds: as many
     whole requests (in order) as fit, repeated over the whole batch when the
     batch alone takes less; estimated from one request."""
-    dt1, tok1 = time_oracle(si, 1)
+    dt1, tok1 = time_oracle(si, 1, state_dtype=state_dtype)
     n = int(max(1, min(si.workload.requests, budget_s / max(dt1, 1e-6))))
     repeats = int(max(1, budget_s / max(dt1 * n, 1e-6)))
-    dt, tok = time_oracle(si, n, repeats)
+    dt, tok = time_oracle(si, n, repeats, state_dtype)
     return {"value": tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"first {n} of {si.workload.requests} requests of the {si.workload.name} workload "
                       f"x {repeats} passes ({tok} tokens x {si.workload.heads} heads), fp64 C oracle, "
@@ -263,14 +275,15 @@ def run_reference(args, w: I.Workload):
     if rank != 0:
         return
     si = I.make_step_inputs(w)
-    dt1, _ = time_oracle(si, 1)
+    sd = args.state_dtype
+    dt1, _ = time_oracle(si, 1, state_dtype=sd)
     per_step_budget = 150.0 / max(args.steps + args.warmup, 1)
     n = int(max(1, min(w.requests, per_step_budget / max(dt1, 1e-6))))
     for _ in range(args.warmup):
-        time_oracle(si, n)
+        time_oracle(si, n, state_dtype=sd)
     total_t, total_tok = 0.0, 0
     for _ in range(args.steps):
-        dt, tok = time_oracle(si, n)
+        dt, tok = time_oracle(si, n, state_dtype=sd)
         total_t += dt
         total_tok += tok
     value = total_tok / total_t
@@ -289,7 +302,7 @@ def run_reference(args, w: I.Workload):
 
 
 def workload_config(w: I.Workload, args):
-    state, allb = algorithmic_bytes(w)
+    state, allb = algorithmic_bytes(w, getattr(args, "state_dtype", "f32"))
     big = state > L2_BYTES
     return {"workload": w.name, "heads": w.heads, "head_dim": HEAD_DIM, "requests": w.requests, "tokens_per_request": w.L,
             "rows": w.rows, "pool_slots": w.pool, "conv_width": w.width, "state_bytes_per_step": state,
@@ -298,7 +311,8 @@ def workload_config(w: I.Workload, args):
             else "L2 flushed between timed steps (256 MiB write, then 256 MiB read; outside the per-step events)",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU",
             "gate": getattr(args, "gate_mode", "sigmoid"),
-            "launch": "plan (CUDA graph)" if getattr(args, "plan", False) else "kda_step"}
+            "launch": "plan (CUDA graph)" if getattr(args, "plan", False) else "kda_step",
+            "state_storage": getattr(args, "state_dtype", "f32")}
 
 
 # -------------------------------------------------------------------- main
@@ -313,6 +327,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--plan", action="store_true",
                     help="launch every step through a launch plan (the step recorded once as a CUDA graph)")
+    ap.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32",
+                    help="state pool storage type (kda_set_state_dtype); the step computes in fp32 either way")
     ap.add_argument("--gate-mode", choices=["sigmoid", "softplus"], default="sigmoid",
                     help="decay gate form (kda_set_gate_mode); the default is the reading the step follows")
     args = ap.parse_args()
@@ -342,8 +358,9 @@ def main():
     kda.load_library()
 
     si = I.make_step_inputs(w)
-    dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=args.plan)
-    state_b, all_b = algorithmic_bytes(w)
+    dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=args.plan,
+                        state_dtype=args.state_dtype)
+    state_b, all_b = algorithmic_bytes(w, args.state_dtype)
     flush = state_b <= L2_BYTES
     # L2 flush between timed steps: write a buffer larger than L2, then read a
     # second one so that the written lines are back in HBM (clean) before the
@@ -460,7 +477,7 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(si)
+        line["cpu_baseline"] = cpu_baseline(si, state_dtype=args.state_dtype)
     print(json.dumps(line), flush=True)
 
 

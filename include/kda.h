@@ -27,7 +27,8 @@
  *   conv_state  bf16 [pool, C, SL] (conv_dim_first = 1) or [pool, SL, C];
  *               each window holds the last SL inputs, oldest first.
  *   state_pool  fp32 [pool, H, 128 (v), 128 (k)]: one contiguous 64 KiB block
- *               per (slot, head), k contiguous within a 512-byte v row.
+ *               per (slot, head), k contiguous within a 512-byte v row (bf16
+ *               and 32 KiB / 256-byte rows after kda_set_state_dtype(BF16)).
  *   out         bf16 [rows, D].
  * Decode: L = 1, accepted = NULL, row b reads and writes slot slots[b].
  * Verify: rows = R L request-major (row = r L + t), slots [R, L] contiguous,
@@ -104,7 +105,8 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
  *   rows, pitch     rows >= 0, a multiple of L; pitch >= 4D + 128 + H
  *   conv_state      device bf16 windows, see layouts          (read + written)
  *   conv_dim_first  1: [pool, 3D, W-1]; 0: [pool, W-1, 3D]
- *   state_pool      device fp32 [pool, H, 128, 128], 16-byte aligned (read + written)
+ *   state_pool      device fp32 (or bf16, see kda_set_state_dtype) [pool, H, 128, 128],
+ *                   16-byte aligned (read + written)
  *   pool_slots      pool size (slots)
  *   slots           device int32 [rows]
  *   L               1..KDA_MAX_TOKENS tokens per request
@@ -140,6 +142,23 @@ int kda_check(kda_handle* handle, void* cuda_stream, unsigned* device_flags);
 #define KDA_GATE_SIGMOID 0
 #define KDA_GATE_SOFTPLUS 1
 int kda_set_gate_mode(kda_handle* handle, int mode);
+
+/*
+ * kda_set_state_dtype -- the storage type of the state pool the handle's
+ * steps read and write (the layout stays [pool, H, 128 (v), 128 (k)]):
+ *   KDA_STATE_F32  (default)  fp32, 64 KiB a (slot, head)
+ *   KDA_STATE_BF16            bf16, 32 KiB a (slot, head): the step widens the
+ *                             start state exactly, computes in fp32 and rounds
+ *                             each stored state to bf16 (nearest even); half
+ *                             the state bytes, at bf16 precision of the cache
+ * For KDA_STATE_BF16 pass the bf16 pool as kda_step's state_pool (same
+ * 16-byte alignment rule).  Applies to steps enqueued (and plans made) after
+ * the call.  Returns KDA_OK, or KDA_EINVAL for a NULL handle or an unknown
+ * type.  No CUDA call.
+ */
+#define KDA_STATE_F32 0
+#define KDA_STATE_BF16 1
+int kda_set_state_dtype(kda_handle* handle, int dtype);
 
 /*
  * Launch plans.  A plan records one kda_step, with exactly these arguments,

@@ -28,7 +28,7 @@ from ._build import LIB_PATH, build
 __all__ = [
     "KdaError", "build", "load_library", "kda_prepare", "kda_step", "kda_check", "kda_destroy",
     "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "kda_plan_create", "kda_plan_launch",
-    "kda_plan_destroy", "PreparedKda", "KdaPlan", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
+    "kda_plan_destroy", "kda_set_state_dtype", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
     "KDA_ERR_TIMEOUT", "KDA_MAX_TOKENS", "KDA_GATE_SIGMOID", "KDA_GATE_SOFTPLUS", "HEAD_DIM",
 ]
 
@@ -37,6 +37,7 @@ KDA_OK, KDA_EINVAL, KDA_ECUDA = 0, -1, -2
 KDA_ERR_SLOT, KDA_ERR_ACCEPTED, KDA_ERR_TIMEOUT = 1, 2, 4
 KDA_MAX_TOKENS = 8
 KDA_GATE_SIGMOID, KDA_GATE_SOFTPLUS = 0, 1
+KDA_STATE_F32, KDA_STATE_BF16 = 0, 1
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -76,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_plan_launch.restype = i32
     lib.kda_plan_destroy.argtypes = [vp]
     lib.kda_plan_destroy.restype = None
+    lib.kda_set_state_dtype.argtypes = [vp, i32]
+    lib.kda_set_state_dtype.restype = i32
     _lib = lib
     return lib
 
@@ -123,6 +126,13 @@ def kda_plan_launch(plan: int, stream: int = 0) -> None:
 
 def kda_plan_destroy(plan: int) -> None:
     load_library().kda_plan_destroy(plan)
+
+
+def kda_set_state_dtype(handle: int, dtype: int) -> None:
+    """KDA_STATE_F32 (default) or KDA_STATE_BF16: the state pool's storage type for later steps."""
+    rc = load_library().kda_set_state_dtype(handle, int(dtype))
+    if rc != KDA_OK:
+        raise KdaError("kda_set_state_dtype", rc)
 
 
 def kda_set_gate_mode(handle: int, mode: int) -> None:
@@ -173,11 +183,13 @@ class PreparedKda:
     bf16, ``A_log`` [H] f32, ``dt_bias`` [D] f32, ``o_norm`` [128] f32 (cast
     to fp32 as the page's __init__ does).  ``gate_mode`` picks the decay gate
     (``KDA_GATE_SIGMOID``, the default, or ``KDA_GATE_SOFTPLUS``; see
-    ``include/kda.h``).
+    ``include/kda.h``); ``state_dtype`` the state pool's storage type ("f32",
+    the default, or "bf16": computed in fp32, each stored state rounded).
     """
 
     def __init__(self, conv_w, conv_bias, f_b, A_log, dt_bias, o_norm, *, gate_lower_bound: float = -5.0,
-                 eps: float = 1e-6, conv_dim_first: bool = True, gate_mode: int = KDA_GATE_SIGMOID):
+                 eps: float = 1e-6, conv_dim_first: bool = True, gate_mode: int = KDA_GATE_SIGMOID,
+                 state_dtype: str = "f32"):
         import torch
 
         self.heads = int(A_log.numel())
@@ -203,6 +215,11 @@ class PreparedKda:
                                       float(eps))
             if gate_mode != KDA_GATE_SIGMOID:
                 kda_set_gate_mode(self.handle, gate_mode)
+            if state_dtype not in ("f32", "bf16"):
+                raise ValueError("state_dtype must be 'f32' or 'bf16'")
+            self.state_dtype = state_dtype
+            if state_dtype == "bf16":
+                kda_set_state_dtype(self.handle, KDA_STATE_BF16)
 
     def _args(self, projected, out, caches, slots, accepted):
         """kda_step's arguments (pointers and sizes) for these tensors, and the
@@ -226,7 +243,7 @@ class PreparedKda:
             raise TypeError("projected must be a CUDA bf16 tensor with unit column stride")
         _dev(out, torch.bfloat16, "out")
         _dev(conv, torch.bfloat16, "conv_state")
-        _dev(state, torch.float32, "state_pool")
+        _dev(state, torch.bfloat16 if self.state_dtype == "bf16" else torch.float32, "state_pool")
         args = (projected.data_ptr(), batch, projected.stride(0), conv.data_ptr(), self.conv_dim_first,
                 state.data_ptr(), state.shape[0], slots.data_ptr(), L,
                 None if accepted is None else accepted.data_ptr(), out.data_ptr())

@@ -49,11 +49,8 @@ constexpr int HD = 128;                        // head dim (k and v)
 constexpr int THREADS = 256;                   // 8 warps
 constexpr int WARPS = THREADS / 32;
 constexpr int Z_CHANNELS = HD / WARPS;         // 16 decay channels a warp
-constexpr int STATE_FLOATS = HD * HD;          // one (slot, head) state
-constexpr int STATE_BYTES = STATE_FLOATS * 4;  // 64 KiB
+constexpr int STATE_FLOATS = HD * HD;          // elements of one (slot, head) state
 constexpr int QUARTERS = 4;
-constexpr int QUARTER_ROWS = HD / QUARTERS;    // 32 v rows
-constexpr int QUARTER_BYTES = STATE_BYTES / QUARTERS;
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000ll;  // ~1 s at 2 GHz
 
 enum { TASK_OK = 0, TASK_PADDING = 1, TASK_SKIP = 2 };
@@ -62,7 +59,7 @@ struct StepArgs {
   const __nv_bfloat16* projected;
   long long pitch;
   __nv_bfloat16* conv_state;
-  float* state_pool;
+  void* state_pool;             // fp32 or bf16 [pool, H, 128 (v), 128 (k)]
   long long pool;
   const int* slots;
   const int* accepted;
@@ -80,11 +77,20 @@ struct StepArgs {
   int gate_mode;  // KDA_GATE_SIGMOID or KDA_GATE_SOFTPLUS
 };
 
+// Sizes of one (slot, head) state in the pool's storage type: fp32, or bf16
+// (BS) when the handle's state pool holds bf16.
+template <bool BS>
+struct StateT {
+  static constexpr int ELEM = BS ? 2 : 4;               // bytes an element
+  static constexpr int BYTES = STATE_FLOATS * ELEM;     // 64 or 32 KiB
+  static constexpr int QBYTES = BYTES / QUARTERS;       // one 32-row quarter
+};
+
 // Shared-memory carve-up for L tokens (byte offsets from the dynamic base).
-template <int L>
+template <int L, bool BS = false>
 struct Smem {
-  static constexpr int state = 0;                     // float [128][128]  start state
-  static constexpr int eg = state + STATE_BYTES;      // float [L][128]    e^g
+  static constexpr int state = 0;                     // [128][128]        start state (storage type)
+  static constexpr int eg = state + StateT<BS>::BYTES;  // float [L][128]  e^g
   static constexpr int kh = eg + L * HD * 4;          // float [L][128]    k, then k^
   static constexpr int qh = kh + L * HD * 4;          // float [L][128]    q, then q^
   static constexpr int fa = qh + L * HD * 4;          // bf16  [L][128]    f_a; later o
@@ -171,6 +177,15 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Wait until every committed bulk store has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void store_streaming_u2(void* p, uint2 v) {
+  asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+// Two floats -> bf16x2 (nearest even), lo in the low half.
+__device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const unsigned*>(&v);
+}
 
 __device__ __forceinline__ void store_streaming(float* p, float4 v) {
   asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
@@ -465,11 +480,14 @@ __device__ __forceinline__ float conv_dot(const ConvLane<N>& q, float& run) {
   return y;
 }
 
-template <int L>
+template <int L, bool BS>
 __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(const StepArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  using S = Smem<L>;
-  float* st = reinterpret_cast<float*>(smem + S::state);
+  using S = Smem<L, BS>;
+  using SB = StateT<BS>;
+  unsigned char* stc = smem + S::state;  // the state in its storage type
+  float* st = reinterpret_cast<float*>(stc);
+  unsigned short* stb = reinterpret_cast<unsigned short*>(stc);
   float* eg = reinterpret_cast<float*>(smem + S::eg);
   float* kh = reinterpret_cast<float*>(smem + S::kh);
   float* qh = reinterpret_cast<float*>(smem + S::qh);
@@ -601,15 +619,16 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   // CTA's state copies, and has its conv and gates to cover the state's latency.
   auto issue_state = [&]() {
     if (tid == 0) {
-      const float* src = a.state_pool + ((long long)start * a.heads + h) * STATE_FLOATS;
+      const unsigned char* src = static_cast<const unsigned char*>(a.state_pool) +
+                                 ((long long)start * a.heads + h) * SB::BYTES;
 #pragma unroll
       for (int q = 0; q < QUARTERS; ++q) mbar_init(smem_u32(&mbar[q]), 1);
       fence_mbar_init();
 #pragma unroll
       for (int q = 0; q < QUARTERS; ++q) {
         const uint32_t bar = smem_u32(&mbar[q]);
-        mbar_expect_tx(bar, QUARTER_BYTES);
-        bulk_load(smem_u32(st + q * QUARTER_ROWS * HD), src + q * QUARTER_ROWS * HD, QUARTER_BYTES, bar);
+        mbar_expect_tx(bar, SB::QBYTES);
+        bulk_load(smem_u32(stc + q * SB::QBYTES), src + q * SB::QBYTES, SB::QBYTES, bar);
       }
       ctl[0] = 0;
     }
@@ -769,7 +788,8 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   const bool b3 = (kl & 8) != 0, b2 = (kl & 4) != 0, b1 = (kl & 2) != 0;
   const int rsel = (b2 ? 2 : 0) + (b1 ? 1 : 0);  // row of the value this lane ends with
   bool timed_out = false;
-  float* dst_k = a.state_pool + (long long)h * STATE_FLOATS + kl * 4;
+  // element (h, row, 64 m + 4 kl) of a slot's state, in bytes from the slot's block
+  unsigned char* dst_k = static_cast<unsigned char*>(a.state_pool) + ((long long)h * STATE_FLOATS + kl * 4) * SB::ELEM;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mbar[2 * pass]), 0) &&
@@ -783,9 +803,15 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const int row = pass * 64 + (r >> 1) * 32 + (r & 1) * 16 + rbase;
-        const float4 x = *reinterpret_cast<const float4*>(st + row * HD + m * 64 + kl * 4);
-        sv[r][2 * m] = make_float2(x.x, x.y);
-        sv[r][2 * m + 1] = make_float2(x.z, x.w);
+        if constexpr (BS) {  // four bf16, widened exactly
+          const uint2 x = *reinterpret_cast<const uint2*>(stb + row * HD + m * 64 + kl * 4);
+          sv[r][2 * m] = make_float2(bf_lo(x.x), bf_hi(x.x));
+          sv[r][2 * m + 1] = make_float2(bf_lo(x.y), bf_hi(x.y));
+        } else {
+          const float4 x = *reinterpret_cast<const float4*>(st + row * HD + m * 64 + kl * 4);
+          sv[r][2 * m] = make_float2(x.x, x.y);
+          sv[r][2 * m + 1] = make_float2(x.z, x.w);
+        }
       }
     const int vq = pass * 64 + (rsel >> 1) * 32 + (rsel & 1) * 16 + rbase;  // row of this lane's value
 #pragma unroll 1
@@ -847,7 +873,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         const float bur = b2 ? (b1 ? bu[3] : bu[2]) : (b1 ? bu[1] : bu[0]);
         ob[t * HD + vq] = __float2bfloat16_rn(fmaf(bur, kq_s[t], rv));
       }
-      float* dst = dst_k + (long long)slot_s[t] * a.heads * STATE_FLOATS;
+      unsigned char* dst = dst_k + (long long)slot_s[t] * a.heads * SB::BYTES;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int row = pass * 64 + (r >> 1) * 32 + (r & 1) * 16 + rbase;
@@ -857,11 +883,17 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
           sv[r][2 * m] = fma2(bu2, kv[2 * m], sv[r][2 * m]);  // S += beta k^ u^T
           sv[r][2 * m + 1] = fma2(bu2, kv[2 * m + 1], sv[r][2 * m + 1]);
           const float4 row4 = make_float4(sv[r][2 * m].x, sv[r][2 * m].y, sv[r][2 * m + 1].x, sv[r][2 * m + 1].y);
-          if constexpr (L == 1) {
+          if constexpr (BS) {  // rounded to bf16 (nearest even) as it is stored
+            const uint2 w = make_uint2(pack_bf16x2(row4.x, row4.y), pack_bf16x2(row4.z, row4.w));
+            if constexpr (L == 1)
+              *reinterpret_cast<uint2*>(stb + row * HD + m * 64 + kl * 4) = w;
+            else
+              store_streaming_u2(dst + (row * HD + m * 64) * 2, w);
+          } else if constexpr (L == 1) {
             // decode: back into the shared-memory state; TMA stores the quarter
             *reinterpret_cast<float4*>(st + row * HD + m * 64 + kl * 4) = row4;
           } else {
-            store_streaming(dst + row * HD + m * 64, row4);
+            store_streaming(reinterpret_cast<float*>(dst + (row * HD + m * 64) * 4), row4);
           }
         }
       }
@@ -874,11 +906,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       if (timed_out && lane == 0) ctl[0] = 1;
       __syncthreads();
       if (tid == 0 && ctl[0] == 0) {
-        float* gdst = a.state_pool + ((long long)slot_s[0] * a.heads + h) * STATE_FLOATS;
+        unsigned char* gdst = static_cast<unsigned char*>(a.state_pool) + ((long long)slot_s[0] * a.heads + h) * SB::BYTES;
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
           const int q = 2 * pass + qq;
-          bulk_store(gdst + q * QUARTER_ROWS * HD, smem_u32(st + q * QUARTER_ROWS * HD), QUARTER_BYTES);
+          bulk_store(gdst + q * SB::QBYTES, smem_u32(stc + q * SB::QBYTES), SB::QBYTES);
         }
         bulk_commit();
       }
@@ -950,7 +982,11 @@ __global__ void row_norms(const __nv_bfloat16* m, float* norms, int rows) {
 
 template <int L>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(kda_step_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<L>::bytes);
+  const cudaError_t e1 = cudaFuncSetAttribute(kda_step_kernel<L, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              Smem<L, false>::bytes);
+  const cudaError_t e2 = cudaFuncSetAttribute(kda_step_kernel<L, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              Smem<L, true>::bytes);
+  return e1 != cudaSuccess ? e1 : e2;
 }
 
 cudaError_t set_all_smem_attrs() {
@@ -963,14 +999,17 @@ cudaError_t set_all_smem_attrs() {
 }
 
 template <int L>
-cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream) {
-  kda_step_kernel<L><<<(unsigned)ctas, THREADS, Smem<L>::bytes, stream>>>(a);
+cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream, bool bf16_state) {
+  if (bf16_state)
+    kda_step_kernel<L, true><<<(unsigned)ctas, THREADS, Smem<L, true>::bytes, stream>>>(a);
+  else
+    kda_step_kernel<L, false><<<(unsigned)ctas, THREADS, Smem<L, false>::bytes, stream>>>(a);
   return cudaGetLastError();
 }
 
 template <int L>
 const void* kernel_fn() {
-  return reinterpret_cast<const void*>(kda_step_kernel<L>);
+  return reinterpret_cast<const void*>(kda_step_kernel<L, false>);
 }
 
 bool aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
@@ -991,6 +1030,7 @@ struct kda_handle {
   unsigned* err;
   float lb, eps;
   int gate_mode;
+  int state_dtype;  // KDA_STATE_F32 or KDA_STATE_BF16
 };
 
 extern "C" {
@@ -1034,6 +1074,7 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
   h->W = conv_width;
   h->lb = gate_lower_bound;
   h->gate_mode = KDA_GATE_SIGMOID;
+  h->state_dtype = KDA_STATE_F32;
   h->eps = eps;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device);
@@ -1116,16 +1157,17 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
   const long long ctas = (rows / L) * h->heads;
   if (ctas > 0x7fffffffLL) return KDA_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  const bool bs = h->state_dtype == KDA_STATE_BF16;
   cudaError_t e;
   switch (L) {
-    case 1: e = launch<1>(a, ctas, s); break;
-    case 2: e = launch<2>(a, ctas, s); break;
-    case 3: e = launch<3>(a, ctas, s); break;
-    case 4: e = launch<4>(a, ctas, s); break;
-    case 5: e = launch<5>(a, ctas, s); break;
-    case 6: e = launch<6>(a, ctas, s); break;
-    case 7: e = launch<7>(a, ctas, s); break;
-    default: e = launch<8>(a, ctas, s); break;
+    case 1: e = launch<1>(a, ctas, s, bs); break;
+    case 2: e = launch<2>(a, ctas, s, bs); break;
+    case 3: e = launch<3>(a, ctas, s, bs); break;
+    case 4: e = launch<4>(a, ctas, s, bs); break;
+    case 5: e = launch<5>(a, ctas, s, bs); break;
+    case 6: e = launch<6>(a, ctas, s, bs); break;
+    case 7: e = launch<7>(a, ctas, s, bs); break;
+    default: e = launch<8>(a, ctas, s, bs); break;
   }
   return e == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
@@ -1175,6 +1217,12 @@ void kda_plan_destroy(kda_plan* p) {
   cudaGraphExecDestroy(p->exec);
   cudaGraphDestroy(p->graph);
   delete p;
+}
+
+int kda_set_state_dtype(kda_handle* h, int dtype) {
+  if (h == nullptr || (dtype != KDA_STATE_F32 && dtype != KDA_STATE_BF16)) return KDA_EINVAL;
+  h->state_dtype = dtype;
+  return KDA_OK;
 }
 
 int kda_set_gate_mode(kda_handle* h, int mode) {

@@ -25,6 +25,7 @@ import numpy as np
 HEAD_DIM = 128
 STATE_SENTINEL = np.uint32(0x7FEDBEEF)  # quiet NaN, fp32
 CONV_SENTINEL = np.uint16(0x7FDB)       # quiet NaN, bf16
+STATE_SENTINEL_BF16 = np.uint16(0x7FED)  # quiet NaN, bf16 (state pool stored as bf16)
 
 
 def to_bf16_bits(x) -> np.ndarray:
@@ -146,6 +147,16 @@ class StepInputs:
         pool = np.empty((w.pool, w.heads, HEAD_DIM, HEAD_DIM), dtype=np.float32)
         pool.view(np.uint32)[...] = STATE_SENTINEL
         pool[self.read_slots] = self.states
+        return pool
+
+    def states_bf16(self) -> np.ndarray:
+        """The read states as bf16 bit patterns (nearest even), for a bf16 state pool."""
+        return to_bf16_bits(self.states)
+
+    def full_state_pool_bf16(self) -> np.ndarray:
+        w = self.workload
+        pool = np.full((w.pool, w.heads, HEAD_DIM, HEAD_DIM), STATE_SENTINEL_BF16, dtype=np.uint16)
+        pool[self.read_slots] = self.states_bf16()
         return pool
 
     def full_conv_state(self, dim_first: bool = True) -> np.ndarray:

@@ -111,10 +111,13 @@ def bf16_round(x: float) -> int:
 
 
 def step(w: Weights, projected, conv_state, state_pool, slots, L: int, accepted=None, *,
-         dim_first: bool = True, act: str = "silu", gate_mode: int = 0, diag: bool = False):
+         dim_first: bool = True, act: str = "silu", gate_mode: int = 0, state_dtype: str = "f32",
+         diag: bool = False):
     """One decode (accepted None, L = 1) or verify step of the C oracle.
 
     gate_mode 0: g = lb * sigmoid(e^A (z + dt)); 1: g = max(-e^A softplus(z + dt), lb).
+    state_dtype "f32" (state_pool fp32) or "bf16" (state_pool uint16 bf16 bits,
+    each stored state rounded to nearest even).
 
     conv_state and state_pool are copied, not modified.  Returns
     ``(out, conv_state, state_pool, err[, diag])`` where ``diag`` is
@@ -126,7 +129,8 @@ def step(w: Weights, projected, conv_state, state_pool, slots, L: int, accepted=
     heads = w.heads
     D = HEAD_DIM * heads
     conv_state = np.array(conv_state, dtype=np.uint16, copy=True, order="C")
-    state_pool = np.array(state_pool, dtype=np.float32, copy=True, order="C")
+    bf16_state = state_dtype == "bf16"
+    state_pool = np.array(state_pool, dtype=np.uint16 if bf16_state else np.float32, copy=True, order="C")
     pool = state_pool.shape[0]
     slots = np.ascontiguousarray(np.asarray(slots, dtype=np.int32).reshape(-1))
     acc = None if accepted is None else np.ascontiguousarray(np.asarray(accepted, dtype=np.int32))
@@ -144,7 +148,8 @@ def step(w: Weights, projected, conv_state, state_pool, slots, L: int, accepted=
         _ptr(A_log), _ptr(dt_bias), _ptr(o_norm), ctypes.c_float(w.gate_lower_bound),
         ctypes.c_float(w.eps), ctypes.c_int(1 if act == "silu" else 0), ctypes.c_int(int(gate_mode)), _ptr(projected),
         ctypes.c_int64(rows), ctypes.c_int64(pitch), _ptr(conv_state), ctypes.c_int(1 if dim_first else 0),
-        _ptr(state_pool), ctypes.c_int64(pool), _ptr(slots), ctypes.c_int(L), _ptr(acc), _ptr(out),
+        _ptr(state_pool), ctypes.c_int64(pool), ctypes.c_int(1 if bf16_state else 0), _ptr(slots), ctypes.c_int(L),
+        _ptr(acc), _ptr(out),
         ctypes.byref(err), _ptr(dg),
     )
     if rc != 0:

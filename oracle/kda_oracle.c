@@ -38,7 +38,9 @@
  *    slots[r, accepted[r] - 1]; after token t both are written to slots[r, t].
  *  - slot -1 at slots[r, 0] marks a padding row / request: nothing is read or
  *    written in the caches and its output rows are zero.
- *  - state layout [pool, H, v = 128, k = 128], k contiguous.
+ *  - state layout [pool, H, v = 128, k = 128], k contiguous; stored as fp32,
+ *    or (state_bf16 = 1, the bf16 cache variant) as bf16 rounded to nearest
+ *    even when a state is written -- a step always carries it in fp64.
  *  - conv_state layout [pool, 3D, W-1] (dim_first = 1) or [pool, W-1, 3D].
  *  - o_norm weight [128] shared by the heads; A_log [H]; dt_bias [D].
  */
@@ -106,7 +108,7 @@ uint16_t kda_oracle_bf16_round(double x) { return bf16_round(x); }
  *   projected         [rows, pitch] bf16: cols [0,3D) q|k|v, [3D,4D) out-gate,
  *                     [4D, 4D+128) f_a, [4D+128, 4D+128+H) beta
  *   conv_state        bf16 [pool, 3D, W-1] (dim_first) or [pool, W-1, 3D]; updated
- *   state_pool        fp32 [pool, H, 128 (v), 128 (k)]; updated
+ *   state_pool        fp32 [pool, H, 128 (v), 128 (k)]; updated (bf16 bits when state_bf16)
  *   slots             [rows] int32 (request-major [R, L] for verify)
  *   L                 tokens per request (rows = R L)
  *   accepted          [R] int32 in 1..L, or NULL for decode (then L must be 1)
@@ -120,7 +122,7 @@ int kda_oracle_step(int heads, int W, const uint16_t *conv_w, const uint16_t *bi
                     const uint16_t *f_b, const float *A_log, const float *dt_bias,
                     const float *o_norm, float lb, float eps, int act, int gate_mode,
                     const uint16_t *projected, int64_t rows, int64_t pitch,
-                    uint16_t *conv_state, int dim_first, float *state_pool, int64_t pool,
+                    uint16_t *conv_state, int dim_first, float *state_pool, int64_t pool, int state_bf16,
                     const int32_t *slots, int L, const int32_t *accepted, uint16_t *out,
                     uint32_t *err, double *diag) {
     if (heads < 1 || W < 2 || L < 1 || rows < 0 || pool < 0) return -1;
@@ -208,10 +210,14 @@ int kda_oracle_step(int heads, int W, const uint16_t *conv_w, const uint16_t *bi
         }
 
         for (int64_t h = 0; h < heads; ++h) {
-            /* Start state of (request, head), fp32 storage [v][k] -> S[k][v]. */
+            /* Start state of (request, head), storage [v][k] -> S[k][v]. */
             const float *src = state_pool + (start * heads + h) * HEAD_DIM * HEAD_DIM;
+            const uint16_t *src16 = (const uint16_t *)state_pool + (start * heads + h) * HEAD_DIM * HEAD_DIM;
             for (int v = 0; v < HEAD_DIM; ++v)
-                for (int k = 0; k < HEAD_DIM; ++k) S[k * HEAD_DIM + v] = (double)src[v * HEAD_DIM + k];
+                for (int k = 0; k < HEAD_DIM; ++k) {
+                    if (state_bf16) S[k * HEAD_DIM + v] = bf16_value(src16[v * HEAD_DIM + k]);
+                    else S[k * HEAD_DIM + v] = (double)src[v * HEAD_DIM + k];
+                }
 
             for (int64_t t = 0; t < L; ++t) {
                 const double *qr = qkv + t * C + h * HEAD_DIM;
@@ -247,8 +253,12 @@ int kda_oracle_step(int heads, int W, const uint16_t *conv_w, const uint16_t *bi
                 }
                 /* one state written per token, into slots[r, t] */
                 float *dst = state_pool + ((int64_t)slots[row0 + t] * heads + h) * HEAD_DIM * HEAD_DIM;
+                uint16_t *dst16 = (uint16_t *)state_pool + ((int64_t)slots[row0 + t] * heads + h) * HEAD_DIM * HEAD_DIM;
                 for (int v = 0; v < HEAD_DIM; ++v)
-                    for (int k = 0; k < HEAD_DIM; ++k) dst[v * HEAD_DIM + k] = (float)S[k * HEAD_DIM + v];
+                    for (int k = 0; k < HEAD_DIM; ++k) {
+                        if (state_bf16) dst16[v * HEAD_DIM + k] = bf16_round(S[k * HEAD_DIM + v]);
+                        else dst[v * HEAD_DIM + k] = (float)S[k * HEAD_DIM + v];
+                    }
 
                 /* Step 6: gated RMSNorm over the head's 128 -> bf16 core_out. */
                 double ms = 0.0;

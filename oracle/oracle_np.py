@@ -54,7 +54,7 @@ def _sigmoid(x):
 
 
 def step(w, projected, conv_state, state_pool, slots, L, accepted=None, *, dim_first=True,
-         act="silu", gate_mode=0, diag=False):
+         act="silu", gate_mode=0, state_dtype="f32", diag=False):
     """Same contract as ``oracle.step`` (the C oracle); inputs are not modified."""
     projected = np.asarray(projected, dtype=np.uint16)
     rows, pitch = projected.shape
@@ -68,7 +68,8 @@ def step(w, projected, conv_state, state_pool, slots, L, accepted=None, *, dim_f
     conv = np.array(conv_state, dtype=np.uint16, copy=True)
     # work on a [pool, C, SL] view whatever the storage order
     conv_v = conv if dim_first else conv.transpose(0, 2, 1)
-    pool_arr = np.array(state_pool, dtype=np.float32, copy=True)
+    bf16_state = state_dtype == "bf16"
+    pool_arr = np.array(state_pool, dtype=np.uint16 if bf16_state else np.float32, copy=True)
     npool = pool_arr.shape[0]
     slots = np.asarray(slots, dtype=np.int64).reshape(-1)
     out = np.zeros((rows, D), dtype=np.uint16)
@@ -118,7 +119,7 @@ def step(w, projected, conv_state, state_pool, slots, L, accepted=None, *, dim_f
 
         for h in range(H):
             cs = slice(h * HEAD_DIM, (h + 1) * HEAD_DIM)
-            S = pool_arr[start, h].astype(np.float64).T                        # S[k, v]
+            S = (bf16_to_f64(pool_arr[start, h]) if bf16_state else pool_arr[start, h].astype(np.float64)).T  # S[k, v]
             for t in range(L):
                 q = qkv[t, 0 * D:1 * D][cs]
                 k = qkv[t, 1 * D:2 * D][cs]
@@ -129,7 +130,7 @@ def step(w, projected, conv_state, state_pool, slots, L, accepted=None, *, dim_f
                 u = v - S.T @ kh
                 S = S + beta[t, h] * np.outer(kh, u)
                 o = _bf16_round_value(S.T @ qh)
-                pool_arr[req_slots[t], h] = S.T.astype(np.float32)
+                pool_arr[req_slots[t], h] = f64_to_bf16(S.T) if bf16_state else S.T.astype(np.float32)
                 rstd = 1.0 / np.sqrt(np.mean(o * o) + eps)
                 out[rws[t], cs] = f64_to_bf16(o * rstd * onorm * _sigmoid(gate[t, cs]))
                 if diag:

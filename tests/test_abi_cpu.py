@@ -30,8 +30,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["kda_prepare", "kda_step", "kda_check", "kda_destroy", "kda_strerror",
-                            "kda_launch_info", "kda_set_gate_mode", "kda_plan_create", "kda_plan_launch",
-                            "kda_plan_destroy"])
+                            "kda_launch_info", "kda_set_gate_mode", "kda_set_state_dtype", "kda_plan_create",
+                            "kda_plan_launch", "kda_plan_destroy"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -55,6 +55,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.kda_launch_info(0, None, None, None) == -1
     assert lib.kda_launch_info(9, None, None, None) == -1
     assert lib.kda_set_gate_mode(None, 0) == -1
+    assert lib.kda_set_state_dtype(None, 1) == -1
     p = ctypes.c_void_p()
     assert lib.kda_plan_create(None, None, 16, 1154, None, 1, None, 16, None, 1, None, None, ctypes.byref(p)) == -1
     assert lib.kda_plan_create(None, None, 16, 1154, None, 1, None, 16, None, 1, None, None, None) == -1

@@ -36,6 +36,9 @@ MUTATIONS = [
     ("gate_bound_ignored", "(double)lb * sigmoid(", "-1.0 * sigmoid("),
     ("softplus_gate_unclamped", "softplus(z + dt_bias[c]), (double)lb)", "softplus(z + dt_bias[c]), -1e300)"),
     ("softplus_gate_no_scale", "fmax(-exp((double)A_log[h]) * softplus(", "fmax(-1.0 * softplus("),
+    ("bf16_state_truncated", "dst16[v * HEAD_DIM + k] = bf16_round(S[k * HEAD_DIM + v]);",
+     "dst16[v * HEAD_DIM + k] = (uint16_t)(bf16_round(S[k * HEAD_DIM + v]) & 0xFFFEu);"),
+    ("bf16_state_transposed", "bf16_value(src16[v * HEAD_DIM + k])", "bf16_value(src16[k * HEAD_DIM + v])"),
     ("gate_one_token", "const double *gr = g + t * D + h * HEAD_DIM;", "const double *gr = g + h * HEAD_DIM;"),
     ("rms_sum_not_mean", "ms /= HEAD_DIM;", "ms /= 1;"),
     ("rms_eps_dropped", "const double rstd = 1.0 / sqrt(ms + (double)eps);", "const double rstd = 1.0 / sqrt(ms);"),

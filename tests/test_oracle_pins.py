@@ -125,6 +125,26 @@ def test_beta_zero_is_decay_only(run):
             assert np.all(np.abs(o - o_exact) <= 2.0 ** -8 * np.abs(o_exact) + 1e-12)
 
 
+def test_bf16_state_storage(run):
+    """bf16 state pool: the start state is the bf16 values widened exactly, the
+    step carries it in fp64 and each stored state is rounded once to bf16
+    (nearest even).  With beta = 0 the stored state is bf16(e^g S) exactly."""
+    si, _, conv = _decode_case(seed=13)
+    H, D = si.workload.heads, si.workload.dim
+    si.projected[:, 4 * D + HEAD_DIM:4 * D + HEAD_DIM + H] = BF16_NEG_INF
+    pool16 = si.full_state_pool_bf16()
+    out, _, newpool, err, dg = run(oracle_weights(si), si.projected, conv, pool16, si.slots, 1, None,
+                                   state_dtype="bf16", diag=True)
+    assert err == 0 and newpool.dtype == np.uint16
+    for b, slot in enumerate(si.slots):
+        for h in range(H):
+            g = dg[b, h, 3 * HEAD_DIM:4 * HEAD_DIM]
+            S = bf16_value(pool16[slot, h])                          # [v, k], exact
+            assert np.array_equal(newpool[slot, h], oracle_np.f64_to_bf16(S * np.exp(g)[None, :]))
+    untouched = np.setdiff1d(np.arange(si.workload.pool), si.slots)
+    assert np.array_equal(newpool[untouched], pool16[untouched])
+
+
 def test_delta_property(run):
     """g = 0 (lower bound 0), beta = 1 (+inf logit): S'^T k^ = v up to the
     l2norm eps, i.e. the delta rule stores v exactly under key k^."""
@@ -396,3 +416,13 @@ def test_c_matches_numpy_on_random_shapes():
         assert np.array_equal(a[1], b[1])
         np.testing.assert_allclose(np.nan_to_num(a[2]), np.nan_to_num(b[2]), rtol=0, atol=1e-7)
         np.testing.assert_allclose(a[4], b[4], rtol=1e-9, atol=1e-9)
+        # the bf16 state pool: the two oracles' fp64 states round to the same bf16
+        # but where one sits within fp64 noise of a rounding boundary
+        pool16 = si.full_state_pool_bf16()
+        args16 = (W, si.projected, si.full_conv_state(dim_first), pool16, si.slots, L, si.accepted)
+        a16 = oracle.step(*args16, dim_first=dim_first, gate_mode=gm, state_dtype="bf16")
+        b16 = oracle_np.step(*args16, dim_first=dim_first, gate_mode=gm, state_dtype="bf16")
+        assert a16[3] == b16[3] == 0
+        fin = ~np.isnan(bf16_value(b16[2]))
+        assert np.array_equal(np.isnan(bf16_value(a16[2])), ~fin)
+        assert np.mean(a16[2][fin] != b16[2][fin]) < 1e-4

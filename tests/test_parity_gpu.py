@@ -131,6 +131,45 @@ def test_plan_replays_equal_steps(L):
     b.close()
 
 
+def _check_bf16_state(si: I.StepInputs, reqs=None):
+    """The bf16 state pool (kda_set_state_dtype): outputs and windows as in
+    fp32, each stored state within one bf16 step of the oracle's, untouched
+    slots keep their bf16 sentinel."""
+    w = si.workload
+    ds = G.DeviceStep(si, state_dtype="bf16")
+    flags = ds.run()
+    if reqs is None:
+        reqs = np.arange(w.requests)
+    out_ref, rows, used, pool_ref, conv_ref, err = G.oracle_requests(si, reqs, state_dtype="bf16")
+    assert flags == err == 0
+    G.assert_out_close(G.torch_bf16_to_np(ds.out[torch.from_numpy(rows).to(ds.device)]), out_ref)
+    uidx = torch.from_numpy(used).to(ds.device)
+    G.assert_state_close_bf16(G.torch_bf16_to_np(ds.state[uidx]), pool_ref)
+    assert np.array_equal(G.torch_bf16_to_np(ds.conv[uidx]), conv_ref)
+    written = np.zeros(w.pool, dtype=bool)
+    written[si.slots[si.slots >= 0]] = True
+    untouched = torch.from_numpy(np.nonzero(~written)[0]).to(ds.device)
+    if untouched.numel():
+        sentinel = int(np.array(I.STATE_SENTINEL_BF16).view(np.int16))
+        assert bool((ds.state[untouched].view(torch.int16) == sentinel).all())
+    ds.close()
+
+
+@pytest.mark.parametrize("name", ["batched_decode", "spec_verify"])
+def test_bf16_state_workloads(name):
+    _check_bf16_state(I.make_step_inputs(I.WORKLOADS[name]))
+
+
+def test_bf16_state_large_decode_sampled():
+    si = I.make_step_inputs(I.WORKLOADS["large_decode"])
+    _check_bf16_state(si, reqs=np.array([0, 1, 77, 300, 511]))
+
+
+@pytest.mark.parametrize("L", [1, 3, 8])
+def test_bf16_state_token_counts(L):
+    _check_bf16_state(case(heads=2, requests=4, L=L, pool=4 * L + 3, seed=90 + L, verify=L > 1))
+
+
 def test_verify_with_one_token_accepted_array():
     _check_full(case(heads=2, requests=6, L=1, pool=8, seed=62, verify=True))
 
