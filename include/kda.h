@@ -65,6 +65,7 @@ typedef struct kda_handle kda_handle;
 #define KDA_ERR_SLOT 1u     /* a slot outside [0, pool) other than a padding -1: request skipped */
 #define KDA_ERR_ACCEPTED 2u /* accepted[r] outside 1..L: request skipped                         */
 #define KDA_ERR_TIMEOUT 4u  /* a bounded wait for a state tile gave up: that tile is not written  */
+#define KDA_ERR_DUPLICATE 8u /* KDA_DEBUG builds only: two rows of the step write the same slot    */
 
 /* Maximum verify tokens per request. */
 #define KDA_MAX_TOKENS 8

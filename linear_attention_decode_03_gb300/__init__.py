@@ -23,18 +23,18 @@ import ctypes
 import os
 from typing import Optional, Tuple
 
-from ._build import LIB_PATH, build
+from ._build import DEBUG_LIB_PATH, LIB_PATH, build
 
 __all__ = [
     "KdaError", "build", "load_library", "kda_prepare", "kda_step", "kda_check", "kda_destroy",
     "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "kda_plan_create", "kda_plan_launch",
     "kda_plan_destroy", "kda_set_state_dtype", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
-    "KDA_ERR_TIMEOUT", "KDA_MAX_TOKENS", "KDA_GATE_SIGMOID", "KDA_GATE_SOFTPLUS", "HEAD_DIM",
+    "KDA_ERR_TIMEOUT", "KDA_ERR_DUPLICATE", "KDA_MAX_TOKENS", "DEBUG_LIB_PATH", "KDA_GATE_SIGMOID", "KDA_GATE_SOFTPLUS", "HEAD_DIM",
 ]
 
 HEAD_DIM = 128
 KDA_OK, KDA_EINVAL, KDA_ECUDA = 0, -1, -2
-KDA_ERR_SLOT, KDA_ERR_ACCEPTED, KDA_ERR_TIMEOUT = 1, 2, 4
+KDA_ERR_SLOT, KDA_ERR_ACCEPTED, KDA_ERR_TIMEOUT, KDA_ERR_DUPLICATE = 1, 2, 4, 8
 KDA_MAX_TOKENS = 8
 KDA_GATE_SIGMOID, KDA_GATE_SOFTPLUS = 0, 1
 KDA_STATE_F32, KDA_STATE_BF16 = 0, 1

@@ -15,6 +15,8 @@ ROOT = os.path.dirname(PKG_DIR)
 SOURCES = [os.path.join(PKG_DIR, "csrc", "kda_step.cu")]
 HEADERS = [os.path.join(ROOT, "include", "kda.h")]
 LIB_PATH = os.path.join(PKG_DIR, "libkda.so")
+# KDA_DEBUG build: adds the device check for duplicate slots in a step (KDA_ERR_DUPLICATE)
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libkda_debug.so")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -25,29 +27,32 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libkda.so")
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(p) <= t for p in SOURCES + HEADERS)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile libkda.so in place (skipped when it is newer than its sources)."""
-    if not force and up_to_date():
-        return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile libkda.so (or, with debug, libkda_debug.so: -DKDA_DEBUG) in place,
+    skipped when it is newer than its sources."""
+    out = DEBUG_LIB_PATH if debug else LIB_PATH
+    if not force and up_to_date(out):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc_path(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-cudart", "static", "-I", os.path.join(ROOT, "include"), "-o", tmp, *SOURCES]
+           "-cudart", "static", "-I", os.path.join(ROOT, "include"), *(["-DKDA_DEBUG"] if debug else []),
+           "-o", tmp, *SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, out)
     if verbose:
         print(res.stderr)
-    return LIB_PATH
+    return out
 
 
 if __name__ == "__main__":

@@ -968,6 +968,24 @@ __global__ void pack_conv_w(const unsigned short* in, uint2* out, long long chan
   out[ch] = make_uint2(t[0] | ((unsigned)t[1] << 16), t[2] | ((unsigned)t[3] << 16));
 }
 
+#ifdef KDA_DEBUG
+// Debug builds only: a step whose rows write the same slot twice is undefined;
+// flag it (KDA_ERR_DUPLICATE).  Row i (of a request that is not padding)
+// writes slots[i]; each is compared with every later one -- quadratic, which
+// a debug build can afford, and it needs no memory beyond the error word.
+__global__ void debug_duplicate_slots(const int* slots, long long rows, int L, long long pool, unsigned* err) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < rows; i += (long long)gridDim.x * blockDim.x) {
+    const int si = slots[i];
+    if (si < 0 || si >= pool || slots[(i / L) * L] == -1) continue;
+    for (long long j = i + 1; j < rows; ++j)
+      if (slots[j] == si && slots[(j / L) * L] != -1) {
+        atomicOr(err, KDA_ERR_DUPLICATE);
+        break;
+      }
+  }
+}
+#endif
+
 // Euclidean norm of each 128-wide bf16 row, in fp64, rounded up to fp32.
 __global__ void row_norms(const __nv_bfloat16* m, float* norms, int rows) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -1158,6 +1176,10 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
   if (ctas > 0x7fffffffLL) return KDA_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   const bool bs = h->state_dtype == KDA_STATE_BF16;
+#ifdef KDA_DEBUG
+  debug_duplicate_slots<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(slots, rows, L, pool_slots, h->err);
+  if (cudaGetLastError() != cudaSuccess) return KDA_ECUDA;
+#endif
   cudaError_t e;
   switch (L) {
     case 1: e = launch<1>(a, ctas, s, bs); break;
