@@ -316,6 +316,120 @@ def workload_config(w: I.Workload, args):
             "state_storage": getattr(args, "state_dtype", "f32")}
 
 
+# ------------------------------------------------------ the layer's projections
+PROJ_METRIC = "projection tokens/s (kda_linear: in_proj or o_proj of the KDA layer) vs GB300 peak, 1 GPU"
+HIDDEN = 7168  # the model width the projections map from / to
+
+
+def bf16_tflops_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def run_linear(args, w: I.Workload):
+    """--op in_proj / o_proj: kda_linear on the layer's shape for the workload's
+    rows (in_proj: x [rows, 7168] . W [pitch, 7168]^T; o_proj: core [rows, D] .
+    W [7168, D]^T), one launch a step, L2 flushed between steps (the weight fits
+    L2 but would not stay there across a model's layers)."""
+    import torch
+    import linear_attention_decode_03_gb300 as kda
+    from oracle import linear as OL
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    kda.build()
+    kda.load_library()
+    rows = w.rows
+    K, N = (HIDDEN, w.pitch) if args.op == "in_proj" else (w.dim, HIDDEN)
+    rng = np.random.Generator(np.random.PCG64(w.seed + 17))
+    xb = I.to_bf16_bits(rng.normal(0.0, 1.0, size=(rows, K)).astype(np.float32))
+    wb = I.to_bf16_bits(rng.normal(0.0, 0.02, size=(N, K)).astype(np.float32))
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    x, W = dev(xb), dev(wb)
+    y = torch.empty((rows, N), dtype=torch.bfloat16, device=device)
+    nbytes = N * K * 2 + rows * K * 2 + rows * N * 2
+    flops = 2 * rows * N * K
+    hbm, hbm_src = load_peaks()
+    tf, tf_src = bf16_tflops_peak()
+    tensor_bound = flops / nbytes > tf * 1e12 / (hbm * 1e9)
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    scratch_rd = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        kda.linear(x, W, y)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    t_host0 = time.time()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        scratch.fill_(float(i))
+        scratch_rd.sum()
+        starts[i].record(stream)
+        kda.linear(x, W, y)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    # e2e: x up from pinned host memory, y back, every step (the weight is resident)
+    hx = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hy = torch.empty((rows, N), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(hx, non_blocking=True)
+        kda.linear(x, W, y)
+        hy.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": flops / (ms / 1e3) / 1e12, "peak": tf, "unit": "TFLOP/s",
+                "peak_source": f"{tf_src} bf16_tflops (MEASURED_PEAKS.json)"}
+    else:
+        roof = {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                "peak_source": f"{hbm_src} hbm_gbs (MEASURED_PEAKS.json)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = "kda_linear_kernel"
+    line = {
+        "metric": PROJ_METRIC, "value": rows / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 x bf16 -> f32 accumulate", "data": "synthetic",
+        "config": {"workload": f"{args.op} for {w.name}", "op": args.op, "rows": rows, "in_features": K,
+                   "out_features": N, "weight_bytes": N * K * 2, "algorithmic_bytes_per_step": nbytes,
+                   "flops_per_step": flops,
+                   "l2": "L2 flushed between timed steps (256 MiB write, then 256 MiB read; outside the events)"},
+        "roofline": roof,
+        "e2e": {"value": rows / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": rows * K * 2,
+                "d2h_bytes_per_step": rows * N * 2, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(t_host0, t_host1),
+    }
+    if not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 5.0 or reps == 0:
+            OL.linear(xb, wb)
+            reps += 1
+        dt = (time.perf_counter() - t0) / reps
+        line["cpu_baseline"] = {"value": rows / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"the whole step ({rows} rows), fp64 NumPy product (BLAS threads), "
+                                          f"{reps} runs in {time.perf_counter() - t0:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 # -------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -330,6 +444,9 @@ def main():
                     help="launch every step through a launch plan (the step recorded once as a CUDA graph)")
     ap.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32",
                     help="state pool storage type (kda_set_state_dtype); the step computes in fp32 either way")
+    ap.add_argument("--op", choices=["step", "in_proj", "o_proj"], default="step",
+                    help="step: the KDA core (default); in_proj / o_proj: the layer's projections (kda_linear) "
+                         "for the workload's rows")
     ap.add_argument("--gate-mode", choices=["sigmoid", "softplus"], default="sigmoid",
                     help="decay gate form (kda_set_gate_mode); the default is the reading the step follows")
     args = ap.parse_args()
@@ -338,6 +455,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    if args.op != "step":
+        run_linear(args, w)
         return
 
     import torch

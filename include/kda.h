@@ -186,6 +186,21 @@ int kda_plan_create(kda_handle* handle, const void* projected, long long rows, l
 int kda_plan_launch(kda_plan* plan, void* cuda_stream);
 void kda_plan_destroy(kda_plan* plan);
 
+/*
+ * kda_linear -- the layer's projections around the core: y = x . W^T with
+ * x [rows, K] (row stride ldx), W [N, K] row-major (a torch Linear weight:
+ * out_features x in_features), y [rows, N] (row stride ldy); bf16 in and out
+ * (nearest even), fp32 accumulation.  in_proj (x [rows, 7168] -> the packed
+ * projection row, the K1 page's gemv in front of kda_pre) and o_proj
+ * (core_out [rows, D] -> [rows, 7168], the K2a page's GEMV after the core)
+ * are both this product.  Device pointers; x and W 16-byte aligned with
+ * ldx % 8 == 0, y 2-byte aligned; K a multiple of 64.
+ * Enqueued on cuda_stream with no host sync.  Returns KDA_OK (rows = 0
+ * launches nothing), KDA_EINVAL or KDA_ECUDA.
+ */
+int kda_linear(const void* x, long long rows, long long ldx, const void* w, long long N, long long K, void* y,
+               long long ldy, void* cuda_stream);
+
 /* kda_destroy -- free the handle's device buffers (synchronises the device). NULL is a no-op. */
 void kda_destroy(kda_handle* handle);
 

@@ -28,7 +28,7 @@ from ._build import DEBUG_LIB_PATH, LIB_PATH, build
 __all__ = [
     "KdaError", "build", "load_library", "kda_prepare", "kda_step", "kda_check", "kda_destroy",
     "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "kda_plan_create", "kda_plan_launch",
-    "kda_plan_destroy", "kda_set_state_dtype", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
+    "kda_plan_destroy", "kda_set_state_dtype", "kda_linear", "linear", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
     "KDA_ERR_TIMEOUT", "KDA_ERR_DUPLICATE", "KDA_MAX_TOKENS", "DEBUG_LIB_PATH", "KDA_GATE_SIGMOID", "KDA_GATE_SOFTPLUS", "HEAD_DIM",
 ]
 
@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_plan_destroy.restype = None
     lib.kda_set_state_dtype.argtypes = [vp, i32]
     lib.kda_set_state_dtype.restype = i32
+    lib.kda_linear.argtypes = [vp, ll, ll, vp, ll, ll, vp, ll, vp]
+    lib.kda_linear.restype = i32
     _lib = lib
     return lib
 
@@ -126,6 +128,34 @@ def kda_plan_launch(plan: int, stream: int = 0) -> None:
 
 def kda_plan_destroy(plan: int) -> None:
     load_library().kda_plan_destroy(plan)
+
+
+def kda_linear(x: int, rows: int, ldx: int, w: int, N: int, K: int, y: int, ldy: int, stream: int = 0) -> None:
+    """y[rows, N] = x[rows, K] . W[N, K]^T on device pointers (see include/kda.h)."""
+    rc = load_library().kda_linear(x, rows, ldx, w, N, K, y, ldy, stream or None)
+    if rc != KDA_OK:
+        raise KdaError("kda_linear", rc)
+
+
+def linear(x, w, out=None, stream=None):
+    """y = x @ w.T for CUDA bf16 tensors x [rows, K] (unit column stride) and
+    w [N, K] (contiguous), through kda_linear; `out` [rows, N] bf16 or None."""
+    import torch
+
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or not (x.is_cuda and w.is_cuda):
+        raise TypeError("linear takes CUDA bf16 tensors")
+    if x.dim() != 2 or w.dim() != 2 or x.stride(1) != 1 or not w.is_contiguous() or x.shape[1] != w.shape[1]:
+        raise ValueError("x [rows, K] with unit column stride and contiguous w [N, K] expected")
+    rows, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((rows, N), dtype=torch.bfloat16, device=x.device)
+    if out.dtype != torch.bfloat16 or out.dim() != 2 or out.stride(1) != 1 or tuple(out.shape) != (rows, N):
+        raise ValueError("out must be bf16 [rows, N] with unit column stride")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    kda_linear(x.data_ptr(), rows, x.stride(0), w.data_ptr(), N, K, out.data_ptr(), out.stride(0), stream)
+    return out
 
 
 def kda_set_state_dtype(handle: int, dtype: int) -> None:

@@ -12,7 +12,7 @@ import subprocess
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
-SOURCES = [os.path.join(PKG_DIR, "csrc", "kda_step.cu")]
+SOURCES = [os.path.join(PKG_DIR, "csrc", "kda_step.cu"), os.path.join(PKG_DIR, "csrc", "kda_linear.cu")]
 HEADERS = [os.path.join(ROOT, "include", "kda.h")]
 LIB_PATH = os.path.join(PKG_DIR, "libkda.so")
 # KDA_DEBUG build: adds the device check for duplicate slots in a step (KDA_ERR_DUPLICATE)

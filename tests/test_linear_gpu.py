@@ -1,0 +1,75 @@
+"""kda_linear (the in_proj / o_proj projections) against the projection
+oracle: bf16 outputs within one bf16 step of the correctly rounded product,
+plus the fp32 accumulation's share (2^-14 of sum |x_k w_k|); the in_proj and
+o_proj shapes of the 12-head layer, rows past 64 (several passes), ragged
+column tails (odd N), a strided x."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_decode_03_gb300 as kda
+from linear_attention_decode_03_gb300.inputs import to_bf16_bits
+from oracle import linear as OL
+from tests import gpu_harness as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kda.build()
+    kda.load_library()
+
+
+def _check(rows, K, N, seed, wscale=0.02, xcols=None):
+    rng = np.random.default_rng(seed)
+    x = to_bf16_bits(rng.normal(0.0, 1.0, size=(rows, xcols or K)).astype(np.float32))
+    w = to_bf16_bits(rng.normal(0.0, wscale, size=(N, K)).astype(np.float32))
+    xd = G.bf16_np_to_torch(x, "cuda")[:, :K]
+    wd = G.bf16_np_to_torch(w, "cuda")
+    y = G.torch_bf16_to_np(kda.linear(xd, wd))
+    torch.cuda.synchronize()
+    ref = OL.linear(np.ascontiguousarray(x[:, :K]), w)
+    scale = OL.abs_products(np.ascontiguousarray(x[:, :K]), w)
+    g, r = G.bf16_value(y), G.bf16_value(ref)
+    ulp = np.maximum(np.abs(r), 1e-30) * 2.0 ** -7
+    bound = ulp + 2.0 ** -14 * scale
+    diff = np.abs(g - r)
+    assert np.all(np.isfinite(g))
+    assert np.all(diff <= bound), f"worst {diff.max()} (bound there {bound.flat[np.argmax(diff - bound)]})"
+    return np.mean(y != ref)
+
+
+@pytest.mark.parametrize("rows", [1, 8, 64])
+def test_in_proj_shape(rows):
+    # x [rows, 7168] . W_in [6284, 7168]^T -> the packed projection row (pitch 6284 at 12 heads)
+    _check(rows, 7168, 6284, seed=rows)
+
+
+@pytest.mark.parametrize("rows", [1, 64])
+def test_o_proj_shape(rows):
+    # core_out [rows, 1536] . W_o [7168, 1536]^T
+    _check(rows, 1536, 7168, seed=100 + rows, wscale=0.05)
+
+
+def test_several_passes_ragged_tail_and_strided_x():
+    _check(130, 256, 99, seed=7, xcols=320)   # 3 row passes, 4 column blocks, last one with 3 columns
+
+
+@pytest.mark.parametrize("rows,K,N", [(16, 384, 77), (17, 384, 77), (5, 192, 45), (3, 7168, 1154), (2, 128, 5000)])
+def test_row_tile_boundaries_and_k_splits(rows, K, N):
+    # 16 rows: the one-tile shape; 17: 64-row passes; K = 192 is not a multiple of
+    # the one-tile shape's 128-k stage; 1154 columns (the 2-head in_proj) split K
+    # eight ways; K = 128 is a single stage, so no split
+    _check(rows, K, N, seed=rows * 1000 + N, xcols=K + 8)
+
+
+def test_rejects_bad_shapes():
+    x = torch.zeros((4, 96), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((8, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kda.KdaError):
+        kda.linear(x, w)  # K = 96 is not a multiple of 64
