@@ -46,8 +46,7 @@ HEAD_DIM = 128
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "kda_step_kernel_dram_traffic.txt")
-KERNEL_SOURCES = [os.path.join(ROOT, "linear_attention_decode_03_gb300", "csrc", "kda_step.cu"),
-                  os.path.join(ROOT, "include", "kda.h")]
+KERNEL_SOURCES = [os.path.join(ROOT, "linear_attention_decode_03_gb300", "csrc", "kda_step.cu")]
 
 
 def kernel_source_hash() -> str:

@@ -194,12 +194,22 @@ void kda_plan_destroy(kda_plan* plan);
  * projection row, the K1 page's gemv in front of kda_pre) and o_proj
  * (core_out [rows, D] -> [rows, 7168], the K2a page's GEMV after the core)
  * are both this product.  Device pointers; x and W 16-byte aligned with
- * ldx % 8 == 0, y 2-byte aligned; K a multiple of 64.
+ * ldx % 8 == 0, y 2-byte aligned; K a multiple of 8 (16-byte rows).  x, W and y are the
+ * caller's and are not retained; y must not overlap x or W.
  * Enqueued on cuda_stream with no host sync.  Returns KDA_OK (rows = 0
  * launches nothing), KDA_EINVAL or KDA_ECUDA.
  */
 int kda_linear(const void* x, long long rows, long long ldx, const void* w, long long N, long long K, void* y,
                long long ldy, void* cuda_stream);
+
+/*
+ * kda_linear_check -- synchronise `cuda_stream`, then read and clear the
+ * projections' device error bits into *device_flags: KDA_ERR_TIMEOUT if a
+ * kda_linear launch since the last check gave up waiting (about a second) for
+ * its own bulk copies, in which case that launch's y is not meaningful.
+ * Returns KDA_OK, KDA_EINVAL (device_flags NULL) or KDA_ECUDA.
+ */
+int kda_linear_check(void* cuda_stream, unsigned* device_flags);
 
 /* kda_destroy -- free the handle's device buffers (synchronises the device). NULL is a no-op. */
 void kda_destroy(kda_handle* handle);

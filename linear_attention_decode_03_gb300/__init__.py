@@ -28,7 +28,7 @@ from ._build import DEBUG_LIB_PATH, LIB_PATH, build
 __all__ = [
     "KdaError", "build", "load_library", "kda_prepare", "kda_step", "kda_check", "kda_destroy",
     "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "kda_plan_create", "kda_plan_launch",
-    "kda_plan_destroy", "kda_set_state_dtype", "kda_linear", "linear", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
+    "kda_plan_destroy", "kda_set_state_dtype", "kda_linear", "kda_linear_check", "linear", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
     "KDA_ERR_TIMEOUT", "KDA_ERR_DUPLICATE", "KDA_MAX_TOKENS", "DEBUG_LIB_PATH", "KDA_GATE_SIGMOID", "KDA_GATE_SOFTPLUS", "HEAD_DIM",
 ]
 
@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_set_state_dtype.restype = i32
     lib.kda_linear.argtypes = [vp, ll, ll, vp, ll, ll, vp, ll, vp]
     lib.kda_linear.restype = i32
+    lib.kda_linear_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.kda_linear_check.restype = i32
     _lib = lib
     return lib
 
@@ -135,6 +137,15 @@ def kda_linear(x: int, rows: int, ldx: int, w: int, N: int, K: int, y: int, ldy:
     rc = load_library().kda_linear(x, rows, ldx, w, N, K, y, ldy, stream or None)
     if rc != KDA_OK:
         raise KdaError("kda_linear", rc)
+
+
+def kda_linear_check(stream: int = 0) -> int:
+    """Synchronise `stream`, return and clear the projections' device error bits."""
+    flags = ctypes.c_uint(0)
+    rc = load_library().kda_linear_check(stream or None, ctypes.byref(flags))
+    if rc != KDA_OK:
+        raise KdaError("kda_linear_check", rc)
+    return flags.value
 
 
 def linear(x, w, out=None, stream=None):

@@ -12,12 +12,16 @@
 // At decode batch sizes (rows <= 64) the product is bound by streaming the
 // weight from HBM once (90 MB for in_proj at 12 heads), not by the tensor
 // pipe: 2 rows x 2 flops per weight byte.  So a CTA owns 32 output columns
-// and streams their weight rows through a six-deep ring of 16-byte cp.async
-// copies (with the matching x tile), while its four warps multiply from
-// shared memory with m16n8k16 bf16 tensor instructions.  Two shapes: up to
-// 16 rows, one 16-row tile, a warp per 8 columns and K in stages of 128 (the
-// ring's bytes are nearly all weight); beyond, 64-row passes (a warp per 16
-// rows, all 32 columns) with K in stages of 64.
+// and streams their weight rows through a six-deep shared-memory ring fed by
+// TMA tensor copies (cp.async.bulk.tensor, 64 x rows boxes, 128-byte
+// swizzle, completing on an mbarrier per slot), while its four warps load
+// fragments with ldmatrix and multiply with m16n8k16 bf16 tensor
+// instructions.  Two shapes, both 12 KB a stage: up to 16 rows, one 16-row
+// tile, a warp per 8 columns, K in stages of 128 (the bytes are mostly
+// weight); beyond, 64-row passes, a warp per 16 rows and all 32 columns, K in
+// stages of 64.  (Stages of twice the k, four deep, measured slower: fewer
+// bytes in flight per SM.)  Rows past `rows`, weight rows past N and k past K
+// are outside the tensor maps: the copy engine fills them with zeros.
 //
 // 32-column tiles alone give too few CTAs to keep HBM busy (37 for the
 // 2-head in_proj, 197 at 12 heads on 152 SMs), so K is split over a thread-
@@ -27,6 +31,7 @@
 // sums 1/C of the tile's elements over the C partials through distributed
 // shared memory and writes them out -- no global scratch, no atomics, and the
 // sum is taken in the same order (rank 0 first) for every element.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -36,36 +41,84 @@
 namespace {
 
 constexpr int LIN_NB = 32;        // output columns a CTA
-constexpr int LIN_STAGES = 5;     // ring depth (three CTAs fit an SM)
+constexpr int LIN_STAGES = 6;     // ring depth (three CTAs fit an SM)
 constexpr int LIN_MAX_SPLIT = 8;  // portable cluster size
 constexpr int LIN_THREADS = 128;  // 4 warps
-constexpr int LIN_KMULT = 64;     // K must be a multiple of this
+constexpr int LIN_KMULT = 8;      // K must be a multiple of this (16-byte weight rows)
+constexpr int LIN_BOXK = 64;      // k a TMA box (128 bytes: the swizzle span)
+constexpr int LIN_STAGE_BYTES = 12288;
+constexpr long long LIN_WAIT_LIMIT = 2000000000ll;  // SM cycles (~1 s) before a copy wait gives up
 
-// Tile shape: MB rows a pass, KS k a stage; rows padded by 8 bf16 in shared
-// memory so that the fragment loads hit 32 distinct banks.
+// Tile shape: MB rows a pass, KS k a stage in KS / 64 boxes; a stage holds the
+// x boxes (MB rows x 128 bytes each) and then the weight boxes (32 rows).
 template <int MB>
 struct LinShape {
   static constexpr int KS = MB == 16 ? 128 : 64;
-  static constexpr int LD = KS + 8;
-  static constexpr int STAGE_ELEMS = (MB + LIN_NB) * LD;
-  static constexpr int SMEM = LIN_STAGES * STAGE_ELEMS * 2;  // bytes
-  static constexpr int NT = MB == 16 ? 1 : 4;                 // n-tiles (of 8 columns) a warp
-  static constexpr int RED = LIN_THREADS * NT * 4;            // fp32 partials a CTA
-  static_assert(RED * 4 <= SMEM, "partials overlay the ring");
+  static constexpr int NBOX = KS / LIN_BOXK;
+  static constexpr int XBOX = MB * 128;      // bytes
+  static constexpr int WBOX = LIN_NB * 128;  // bytes
+  static constexpr int NT = MB == 16 ? 1 : 4;       // n-tiles (of 8 columns) a warp
+  static constexpr int RED = LIN_THREADS * NT * 4;  // fp32 partials a CTA
+  static constexpr int RING = LIN_STAGES * LIN_STAGE_BYTES;
+  static constexpr int SMEM = 1024 + RING + 8 * LIN_STAGES;  // + 1024-byte alignment slack + an mbarrier a slot
+  static_assert(NBOX * (XBOX + WBOX) == LIN_STAGE_BYTES, "12 KB stages");
+  static_assert(XBOX % 1024 == 0 && WBOX % 1024 == 0, "boxes start on the swizzle pattern's 1 KB period");
+  static_assert(RED * 4 <= RING, "partials overlay the ring");
 };
+
+// Sticky device-side error bits of the projections (KDA_ERR_TIMEOUT), read and
+// cleared by kda_linear_check.
+__device__ unsigned g_lin_err;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// 16-byte async copy; src_bytes = 0 fills the destination with zeros (no read).
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, unsigned src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
-               : "memory");
+// Byte address of 16-byte chunk `chunk` (0..7) of row `row` of a box written
+// with the 128-byte swizzle: the chunk index is XORed with the row mod 8.
+__device__ __forceinline__ uint32_t swz(uint32_t box, int row, int chunk) {
+  return box + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Phase `parity` of an mbarrier, or false after LIN_WAIT_LIMIT cycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long c0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - c0 > LIN_WAIT_LIMIT) return false;
+  return true;
+}
+// One 2-D TMA box (coordinates: k, row) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, int k, int row, uint32_t bar,
+                                        unsigned long long policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
 
 __device__ __forceinline__ unsigned cluster_ctarank() {
   unsigned r;
@@ -96,121 +149,149 @@ __device__ __forceinline__ float ld_peer_f32(const float* local, unsigned rank) 
   return v;
 }
 
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 struct LinArgs {
-  const __nv_bfloat16* x;
-  long long ldx;
-  const __nv_bfloat16* w;  // [N, K]
   __nv_bfloat16* y;
   long long ldy;
   long long M, N, K;
+  unsigned x_box_bytes;  // bytes of one x box: its rows (min(rows, MB)) x 128
 };
 
-// Stage s of the ring: x rows [m0, m0 + MB) and weight rows [n0, n0 + 32) over
-// k [k0, k0 + KS), zeros where the rows run past M or N (no read there).
+// Issued by one thread: the x and weight boxes of stage k0 .. k0 + KS into
+// ring slot `st`, all completing on `bar`.
 template <int MB>
-__device__ __forceinline__ void load_stage(const LinArgs& a, __nv_bfloat16* st, long long m0, long long n0,
-                                           long long k0) {
+__device__ __forceinline__ void issue_stage(const LinArgs& a, const CUtensorMap* tmx, const CUtensorMap* tmw,
+                                            uint32_t st, uint32_t bar, long long m0, long long n0, long long k0) {
   using T = LinShape<MB>;
-  constexpr int CPR = T::KS / 8;  // 16-byte chunks a row
-  __nv_bfloat16* xs = st;
-  __nv_bfloat16* ws = st + MB * T::LD;
-  const int tid = threadIdx.x;
+  unsigned long long w_policy, x_policy;  // the weight is read once, x by every CTA
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w_policy));
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(x_policy));
+  mbar_expect_tx(bar, T::NBOX * (a.x_box_bytes + T::WBOX));
 #pragma unroll
-  for (int i = 0; i < (MB * CPR) / LIN_THREADS; ++i) {
-    const int c = tid + i * LIN_THREADS;
-    const int r = c / CPR, kc = (c % CPR) * 8;
-    const bool in = m0 + r < a.M;
-    const __nv_bfloat16* src = in ? a.x + (m0 + r) * a.ldx + k0 + kc : a.x;
-    cp_async16(xs + r * T::LD + kc, src, in ? 16u : 0u);
-  }
-#pragma unroll
-  for (int i = 0; i < (LIN_NB * CPR) / LIN_THREADS; ++i) {
-    const int c = tid + i * LIN_THREADS;
-    const int r = c / CPR, kc = (c % CPR) * 8;
-    const bool in = n0 + r < a.N;
-    const __nv_bfloat16* src = in ? a.w + (n0 + r) * a.K + k0 + kc : a.w;
-    cp_async16(ws + r * T::LD + kc, src, in ? 16u : 0u);
+  for (int b = 0; b < T::NBOX; ++b) {
+    tma_box(st + b * T::XBOX, tmx, (int)(k0 + b * LIN_BOXK), (int)m0, bar, x_policy);
+    tma_box(st + T::NBOX * T::XBOX + b * T::WBOX, tmw, (int)(k0 + b * LIN_BOXK), (int)n0, bar, w_policy);
   }
 }
 
 template <int MB>
-__global__ void __launch_bounds__(LIN_THREADS) kda_linear_kernel(const LinArgs a) {
+__global__ void __launch_bounds__(LIN_THREADS) kda_linear_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                                 const __grid_constant__ CUtensorMap tmw,
+                                                                 const LinArgs a) {
   using T = LinShape<MB>;
   constexpr int NT = T::NT;
   extern __shared__ __align__(128) unsigned char lsmem[];
-  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(lsmem);
-  float* red = reinterpret_cast<float*>(lsmem);  // the partial tile, over the drained ring
+  // the ring starts on a 1 KB boundary (the swizzle pattern's period)
+  const uint32_t raw = smem_addr(lsmem);
+  const uint32_t ring_s = (raw + 1023u) & ~1023u, bar0 = ring_s + T::RING;
+  float* red = reinterpret_cast<float*>(lsmem + (ring_s - raw));  // the partial tile, over the drained ring
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
   // without a cluster launch each CTA is a cluster of one: rank 0 of 1
   const unsigned split = cluster_nctarank(), rank = cluster_ctarank();
   const long long n0 = (long long)cluster_id_x() * LIN_NB;
-  const long long total = a.K / T::KS;  // k stages over the whole K
+  const long long total = (a.K + T::KS - 1) / T::KS;  // k stages over the whole K (the last one zero-padded)
   const long long s_begin = total * rank / split;
   const long long stages = total * (rank + 1) / split - s_begin;
-  // the warp's 16 rows (within the pass) and first n-tile
-  const int wrow = MB == 16 ? 0 : warp * 16;
-  const int wnt = MB == 16 ? warp : 0;
+  // ldmatrix row addresses: lane l feeds row l & 7 of 8x8 matrix l >> 3
+  const int lr = lane & 7, lm = lane >> 3;
 
-  for (long long m0 = 0; m0 < a.M; m0 += MB) {
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
+    for (int i = 0; i < LIN_STAGES; ++i) mbar_init(bar0 + 8 * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  bool dead = false;  // a copy wait gave up: no more copies, outputs not meaningful
+  long long g0 = 0;   // ring stages used by earlier passes (slot and phase bookkeeping)
+  for (long long m0 = 0; m0 < a.M; m0 += MB, g0 += stages) {
     float acc[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-    // ring prologue: stages 0 .. STAGES-2 in flight
-#pragma unroll
-    for (int s = 0; s < LIN_STAGES - 1; ++s) {
-      if (s < stages) load_stage<MB>(a, ring + s * T::STAGE_ELEMS, m0, n0, (s_begin + s) * T::KS);
-      cp_async_commit();
+    const long long run = dead ? 0 : stages;
+    if (threadIdx.x == 0) {  // ring prologue: stages 0 .. STAGES-2 in flight
+      for (int s = 0; s < LIN_STAGES - 1 && s < run; ++s) {
+        const uint32_t slot = (uint32_t)((g0 + s) % LIN_STAGES);
+        issue_stage<MB>(a, &tmx, &tmw, ring_s + slot * LIN_STAGE_BYTES, bar0 + 8 * slot, m0, n0,
+                        (s_begin + s) * T::KS);
+      }
     }
-    for (long long s = 0; s < stages; ++s) {
-      cp_async_wait<LIN_STAGES - 2>();  // stage s has landed (this thread's copies) ...
-      __syncthreads();                  // ... and everyone's; stage s-1's slot is free again
+    long long issued = run < LIN_STAGES - 1 ? run : LIN_STAGES - 1;
+    for (long long s = 0; s < run; ++s) {
+      const long long g = g0 + s;
+      const uint32_t slot = (uint32_t)(g % LIN_STAGES);
+      const bool ok = mbar_wait_bounded(bar0 + 8 * slot, (unsigned)((g / LIN_STAGES) & 1));
+      // every warp is past stage s-1 (its slot is free again) and agrees on the outcome
+      if (__syncthreads_or(!ok)) {
+        dead = true;
+        if (threadIdx.x == 0) atomicOr(&g_lin_err, KDA_ERR_TIMEOUT);
+        for (long long q = s; q < issued; ++q)  // the copies still in flight land before the CTA moves on
+          mbar_wait_bounded(bar0 + 8 * (uint32_t)((g0 + q) % LIN_STAGES), (unsigned)(((g0 + q) / LIN_STAGES) & 1));
+        break;
+      }
       const long long next = s + LIN_STAGES - 1;
-      if (next < stages)
-        load_stage<MB>(a, ring + (next % LIN_STAGES) * T::STAGE_ELEMS, m0, n0, (s_begin + next) * T::KS);
-      cp_async_commit();
-      const __nv_bfloat16* xs = ring + (s % LIN_STAGES) * T::STAGE_ELEMS;
-      const __nv_bfloat16* ws = xs + MB * T::LD;
-      const int r0 = wrow + gid;
+      if (next < run) {
+        if (threadIdx.x == 0) {
+          const uint32_t ns = (uint32_t)((g0 + next) % LIN_STAGES);
+          issue_stage<MB>(a, &tmx, &tmw, ring_s + ns * LIN_STAGE_BYTES, bar0 + 8 * ns, m0, n0,
+                          (s_begin + next) * T::KS);
+        }
+        issued = next + 1;
+      }
+      const uint32_t xs = ring_s + slot * LIN_STAGE_BYTES, ws = xs + T::NBOX * T::XBOX;
+      if (MB == 16) {
+        // all warps: the 16 x rows; warp w: weight rows 8w .. 8w + 7 (its n-tile)
 #pragma unroll
-      for (int kk = 0; kk < T::KS / 16; ++kk) {
-        const int kb = kk * 16 + tig * 2;
-        uint32_t af[4];
-        af[0] = *reinterpret_cast<const uint32_t*>(xs + r0 * T::LD + kb);
-        af[1] = *reinterpret_cast<const uint32_t*>(xs + (r0 + 8) * T::LD + kb);
-        af[2] = *reinterpret_cast<const uint32_t*>(xs + r0 * T::LD + kb + 8);
-        af[3] = *reinterpret_cast<const uint32_t*>(xs + (r0 + 8) * T::LD + kb + 8);
+        for (int kk = 0; kk < T::KS / 16; kk += 2) {
+          const int box = kk >> 2, c0 = 2 * (kk & 3);
+          uint32_t a0[4], a1[4], b[4];
+          ldsm_x4(a0, swz(xs + box * T::XBOX, lr + (lm & 1) * 8, c0 + (lm >> 1)));
+          ldsm_x4(a1, swz(xs + box * T::XBOX, lr + (lm & 1) * 8, c0 + 2 + (lm >> 1)));
+          ldsm_x4(b, swz(ws + box * T::WBOX, warp * 8 + lr, c0 + lm));
+          mma_bf16(acc[0], a0[0], a0[1], a0[2], a0[3], b[0], b[1]);
+          mma_bf16(acc[0], a1[0], a1[1], a1[2], a1[3], b[2], b[3]);
+        }
+      } else {
+        // warp w: x rows 16w .. 16w + 15 against all four n-tiles
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int nr = (wnt + j) * 8 + gid;
-          uint32_t bf[2];
-          bf[0] = *reinterpret_cast<const uint32_t*>(ws + nr * T::LD + kb);
-          bf[1] = *reinterpret_cast<const uint32_t*>(ws + nr * T::LD + kb + 8);
-          mma_bf16(acc[j], af, bf);
+        for (int kk = 0; kk < T::KS / 16; ++kk) {
+          const int box = kk >> 2, c0 = 2 * (kk & 3);
+          const uint32_t xb = xs + box * T::XBOX, wb = ws + box * T::WBOX;
+          uint32_t af[4], b01[4], b23[4];
+          ldsm_x4(af, swz(xb, warp * 16 + lr + (lm & 1) * 8, c0 + (lm >> 1)));
+          ldsm_x4(b01, swz(wb, (lm >> 1) * 8 + lr, c0 + (lm & 1)));
+          ldsm_x4(b23, swz(wb, (2 + (lm >> 1)) * 8 + lr, c0 + (lm & 1)));
+          mma_bf16(acc[0], af[0], af[1], af[2], af[3], b01[0], b01[1]);
+          mma_bf16(acc[NT > 1 ? 1 : 0], af[0], af[1], af[2], af[3], b01[2], b01[3]);
+          mma_bf16(acc[NT > 2 ? 2 : 0], af[0], af[1], af[2], af[3], b23[0], b23[1]);
+          mma_bf16(acc[NT > 3 ? 3 : 0], af[0], af[1], af[2], af[3], b23[2], b23[3]);
         }
       }
     }
-    cp_async_wait<0>();
     __syncthreads();  // every warp is done with the ring: the partials overlay it
     // partial element e = ((j * 4 + c) * 128 + thread): fragment c of n-tile j of a thread
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
       for (int c = 0; c < 4; ++c) red[(j * 4 + c) * LIN_THREADS + threadIdx.x] = acc[j][c];
+    // these generic-proxy writes precede the next pass's tensor copies into the same bytes
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (split > 1) cluster_sync(); else __syncthreads();
     // this CTA's share of the tile: elements [rank * RED / split, (rank + 1) * RED / split)
     const int e_end = (int)(T::RED * (rank + 1) / split);
     for (int e = (int)(T::RED * rank / split) + threadIdx.x; e < e_end; e += LIN_THREADS) {
       float v = 0.0f;
       for (unsigned q = 0; q < split; ++q) v += split > 1 ? ld_peer_f32(red + e, q) : red[e];
+      // accumulator layout of m16n8: c0, c1 at row lane/4, columns 2 (lane % 4) + {0, 1}; c2, c3 eight rows down
       const int t = e % LIN_THREADS, jc = e / LIN_THREADS, j = jc >> 2, c = jc & 3;
       const int tw = t >> 5, tl = t & 31;
       const long long m = m0 + (MB == 16 ? 0 : tw * 16) + (tl >> 2) + (c >> 1) * 8;
@@ -224,11 +305,49 @@ __global__ void __launch_bounds__(LIN_THREADS) kda_linear_kernel(const LinArgs a
 
 bool lin_aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
-// K split: the largest C <= 8 (and <= the K stages) with tiles x C within the
-// GPU's resident CTA slots, so that one wave covers the grid.
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no link to libcuda).
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// A bf16 matrix [rows, cols] with row stride ld (elements) as 64 x box_rows boxes, 128-byte swizzle.
+bool encode_map(CUtensorMap* map, const void* base, long long rows, long long cols, long long ld, int box_rows) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)LIN_BOXK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K split C (<= 8, <= the K stages): a CTA's time is about its share of the
+// stages, so the kernel's is about waves x stages / C, waves = the grid over
+// the GPU's resident CTA slots, rounded up; the smallest C that minimises
+// ceil(tiles C / slots) / C.
 template <int MB>
-int lin_launch(const LinArgs& a, long long tiles, cudaStream_t st) {
+int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, long long tiles, cudaStream_t st) {
   using T = LinShape<MB>;
+  const int box_rows = (int)(a.M < MB ? a.M : MB);
+  a.x_box_bytes = (unsigned)box_rows * 128u;
+  CUtensorMap tmx, tmw;
+  if (!encode_map(&tmx, x, a.M, a.K, ldx, box_rows) || !encode_map(&tmw, w, a.N, a.K, a.K, LIN_NB))
+    return KDA_ECUDA;
   // the shared-memory attribute is per device and cheap: set on every call
   if (cudaFuncSetAttribute(kda_linear_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
       cudaSuccess)
@@ -247,10 +366,13 @@ int lin_launch(const LinArgs& a, long long tiles, cudaStream_t st) {
     slots = (long long)sms * (per_sm > 0 ? per_sm : 1);
     if (dev < 64) slot_cache[dev] = slots;
   }
-  long long split = slots / tiles;
-  if (split > LIN_MAX_SPLIT) split = LIN_MAX_SPLIT;
-  if (split > a.K / T::KS) split = a.K / T::KS;
-  if (split < 1) split = 1;
+  const long long stages = (a.K + T::KS - 1) / T::KS;
+  long long split = 1;
+  double best = 1e300;
+  for (long long c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
+    const double cost = (double)((tiles * c + slots - 1) / slots) / (double)c;
+    if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
+  }
   if (tiles * split > 0x7fffffffLL) return KDA_EINVAL;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
@@ -264,7 +386,7 @@ int lin_launch(const LinArgs& a, long long tiles, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kda_linear_kernel<MB>, a) != cudaSuccess) return KDA_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, kda_linear_kernel<MB>, tmx, tmw, a) != cudaSuccess) return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
@@ -275,21 +397,31 @@ extern "C" int kda_linear(const void* x, long long rows, long long ldx, const vo
   if (rows < 0 || N < 1 || K < LIN_KMULT || K % LIN_KMULT != 0) return KDA_EINVAL;
   if (rows == 0) return KDA_OK;
   if (!x || !w || !y || ldx < K || ldy < N) return KDA_EINVAL;
-  // 16-byte copies: x and weight rows start on 16-byte boundaries
+  // tensor maps: 16-byte aligned bases and row strides; coordinates fit 32 bits
   if (!lin_aligned(x, 16) || !lin_aligned(w, 16) || (ldx % 8) != 0 || !lin_aligned(y, 2)) return KDA_EINVAL;
-  const long long ctas = (N + LIN_NB - 1) / LIN_NB;
-  if (ctas > 0x7fffffffLL) return KDA_EINVAL;
-  // rows <= 16 (and K a multiple of its 128-k stage): the one-tile shape
-  const bool small = rows <= 16 && K % LinShape<16>::KS == 0;
+  if (K > 0x7fffffffLL || N > 0x7fffffffLL || rows > 0x7fffffffLL) return KDA_EINVAL;
+  const long long tiles = (N + LIN_NB - 1) / LIN_NB;
+  // rows <= 16: the one-tile shape
+  const bool small = rows <= 16;
   LinArgs a;
-  a.x = static_cast<const __nv_bfloat16*>(x);
-  a.ldx = ldx;
-  a.w = static_cast<const __nv_bfloat16*>(w);
   a.y = static_cast<__nv_bfloat16*>(y);
   a.ldy = ldy;
   a.M = rows;
   a.N = N;
   a.K = K;
+  a.x_box_bytes = 0;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  return small ? lin_launch<16>(a, ctas, st) : lin_launch<64>(a, ctas, st);
+  return small ? lin_launch<16>(x, ldx, w, a, tiles, st) : lin_launch<64>(x, ldx, w, a, tiles, st);
+}
+
+extern "C" int kda_linear_check(void* cuda_stream, unsigned* device_flags) {
+  if (!device_flags) return KDA_EINVAL;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return KDA_ECUDA;
+  unsigned v = 0;
+  const unsigned zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_lin_err, sizeof(v)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_lin_err, &zero, sizeof(zero)) != cudaSuccess)
+    return KDA_ECUDA;
+  *device_flags = v;
+  return KDA_OK;
 }

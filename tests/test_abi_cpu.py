@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["kda_prepare", "kda_step", "kda_check", "kda_destroy", "kda_strerror",
                             "kda_launch_info", "kda_set_gate_mode", "kda_set_state_dtype", "kda_plan_create",
-                            "kda_plan_launch", "kda_plan_destroy", "kda_linear"])
+                            "kda_plan_launch", "kda_plan_destroy", "kda_linear", "kda_linear_check"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -57,10 +57,11 @@ def test_host_validation_without_gpu(lib):
     assert lib.kda_set_gate_mode(None, 0) == -1
     assert lib.kda_set_state_dtype(None, 1) == -1
     # kda_linear: bad shapes rejected before any CUDA call
-    assert lib.kda_linear(None, 4, 64, None, 8, 60, None, 8, None) == -1    # K not a multiple of 64
+    assert lib.kda_linear(None, 4, 64, None, 8, 60, None, 8, None) == -1    # K not a multiple of 8
     assert lib.kda_linear(None, 4, 64, None, 0, 64, None, 8, None) == -1    # N < 1
     assert lib.kda_linear(None, 4, 64, None, 8, 64, None, 8, None) == -1    # null pointers
     assert lib.kda_linear(None, 0, 64, None, 8, 64, None, 8, None) == 0     # rows = 0: nothing
+    assert lib.kda_linear_check(None, None) == -1                            # null flags pointer
     p = ctypes.c_void_p()
     assert lib.kda_plan_create(None, None, 16, 1154, None, 1, None, 16, None, 1, None, None, ctypes.byref(p)) == -1
     assert lib.kda_plan_create(None, None, 16, 1154, None, 1, None, 16, None, 1, None, None, None) == -1

@@ -32,7 +32,7 @@ def _check(rows, K, N, seed, wscale=0.02, xcols=None):
     xd = G.bf16_np_to_torch(x, "cuda")[:, :K]
     wd = G.bf16_np_to_torch(w, "cuda")
     y = G.torch_bf16_to_np(kda.linear(xd, wd))
-    torch.cuda.synchronize()
+    assert kda.kda_linear_check() == 0
     ref = OL.linear(np.ascontiguousarray(x[:, :K]), w)
     scale = OL.abs_products(np.ascontiguousarray(x[:, :K]), w)
     g, r = G.bf16_value(y), G.bf16_value(ref)
@@ -60,16 +60,17 @@ def test_several_passes_ragged_tail_and_strided_x():
     _check(130, 256, 99, seed=7, xcols=320)   # 3 row passes, 4 column blocks, last one with 3 columns
 
 
-@pytest.mark.parametrize("rows,K,N", [(16, 384, 77), (17, 384, 77), (5, 192, 45), (3, 7168, 1154), (2, 128, 5000)])
-def test_row_tile_boundaries_and_k_splits(rows, K, N):
-    # 16 rows: the one-tile shape; 17: 64-row passes; K = 192 is not a multiple of
-    # the one-tile shape's 128-k stage; 1154 columns (the 2-head in_proj) split K
-    # eight ways; K = 128 is a single stage, so no split
+@pytest.mark.parametrize("rows,K,N", [(16, 512, 77), (17, 384, 77), (5, 200, 45), (20, 328, 70), (1, 8, 33),
+                                     (3, 7168, 1154), (2, 128, 5000)])
+def test_row_tile_boundaries_ragged_k_and_k_splits(rows, K, N):
+    # 16 rows: the one-tile shape; 17: 64-row passes; K = 200, 328, 8 end in a
+    # partial k stage (zero-filled past K); 1154 columns (the 2-head in_proj)
+    # split K eight ways; K = 128 is a single stage, so no split
     _check(rows, K, N, seed=rows * 1000 + N, xcols=K + 8)
 
 
 def test_rejects_bad_shapes():
-    x = torch.zeros((4, 96), dtype=torch.bfloat16, device="cuda")
-    w = torch.zeros((8, 96), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((4, 100), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((8, 100), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(kda.KdaError):
-        kda.linear(x, w)  # K = 96 is not a multiple of 64
+        kda.linear(x, w)  # K = 100: weight rows of 200 bytes, not a multiple of 16
