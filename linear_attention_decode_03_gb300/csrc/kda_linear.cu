@@ -9,28 +9,30 @@
 // [rows, 7168]); both weights are [out_features, in_features], the layout of
 // a torch Linear.
 //
-// At decode batch sizes (rows <= 64) the product is bound by streaming the
-// weight from HBM once (90 MB for in_proj at 12 heads), not by the tensor
-// pipe: 2 rows x 2 flops per weight byte.  So a CTA owns 32 output columns
-// and streams their weight rows through a six-deep shared-memory ring fed by
-// TMA tensor copies (cp.async.bulk.tensor, 64 x rows boxes, 128-byte
-// swizzle, completing on an mbarrier per slot), while its four warps load
-// fragments with ldmatrix and multiply with m16n8k16 bf16 tensor
-// instructions.  Two shapes, both 12 KB a stage: up to 16 rows, one 16-row
-// tile, a warp per 8 columns, K in stages of 128 (the bytes are mostly
-// weight); beyond, 64-row passes, a warp per 16 rows and all 32 columns, K in
-// stages of 64.  (Stages of twice the k, four deep, measured slower: fewer
-// bytes in flight per SM.)  Rows past `rows`, weight rows past N and k past K
-// are outside the tensor maps: the copy engine fills them with zeros.
+// At decode batch sizes the product is bound by streaming the weight from
+// HBM once (90 MB for in_proj at 12 heads), not by the tensor pipe: 2 x rows
+// flops per weight element.  A CTA owns NB output columns and streams their
+// weight rows (and the matching x rows) through a shared-memory ring fed by
+// TMA tensor copies (cp.async.bulk.tensor, 64 x rows boxes, 128-byte swizzle,
+// completing on an mbarrier per slot), while its warps load fragments with
+// ldmatrix and multiply with m16n8k16 bf16 tensor instructions.  Two shapes:
+//   rows <= 16: one 16-row tile, 32 columns, 4 warps (one 8-column n-tile
+//     each), K in stages of 128, six stages of 12 KB: the bytes are weight;
+//   rows > 16: 64-row passes, 128 columns, 8 warps (16 rows x 64 columns
+//     each), K in stages of 64, four stages of 24 KB: x is re-read from L2 by
+//     every column tile, so wide tiles keep the copy engine's bytes mostly
+//     weight (x : W = 1 : 2; with 32-column tiles it was 2 : 1 and the kernel
+//     ran at a third of the HBM rate).
+// Rows past `rows`, weight rows past N and k past K are outside the tensor
+// maps: the copy engine fills them with zeros.
 //
-// 32-column tiles alone give too few CTAs to keep HBM busy (37 for the
-// 2-head in_proj, 197 at 12 heads on 152 SMs), so K is split over a thread-
-// block cluster of C CTAs (C <= 8, chosen so that the grid fills the SMs'
-// resident slots once): each CTA streams 1/C of the K stages, leaves its fp32
-// partial tile in its own shared memory, and after a cluster barrier each CTA
-// sums 1/C of the tile's elements over the C partials through distributed
-// shared memory and writes them out -- no global scratch, no atomics, and the
-// sum is taken in the same order (rank 0 first) for every element.
+// Column tiles alone give too few CTAs to keep HBM busy (37 for the 2-head
+// in_proj on 152 SMs), so K is split over a thread-block cluster of C CTAs
+// (C <= 8): each CTA streams 1/C of the K stages, leaves its fp32 partial
+// tile in its own shared memory, and after a cluster barrier each CTA sums
+// 1/C of the tile's elements over the C partials through distributed shared
+// memory and writes them out -- no global scratch, no atomics, and the sum is
+// taken in the same order (rank 0 first) for every element.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,30 +42,34 @@
 
 namespace {
 
-constexpr int LIN_NB = 32;        // output columns a CTA
-constexpr int LIN_STAGES = 6;     // ring depth (three CTAs fit an SM)
 constexpr int LIN_MAX_SPLIT = 8;  // portable cluster size
-constexpr int LIN_THREADS = 128;  // 4 warps
 constexpr int LIN_KMULT = 8;      // K must be a multiple of this (16-byte weight rows)
 constexpr int LIN_BOXK = 64;      // k a TMA box (128 bytes: the swizzle span)
-constexpr int LIN_STAGE_BYTES = 12288;
 constexpr long long LIN_WAIT_LIMIT = 2000000000ll;  // SM cycles (~1 s) before a copy wait gives up
 
-// Tile shape: MB rows a pass, KS k a stage in KS / 64 boxes; a stage holds the
-// x boxes (MB rows x 128 bytes each) and then the weight boxes (32 rows).
-template <int MB>
+// Tile shape: MB rows a pass and NB columns a CTA; KS k a stage in KS / 64
+// boxes; a stage holds the x boxes (MB rows x 128 bytes each), then the weight
+// boxes (NB rows).  Warp w takes rows 16 (w % WM) .. + 15 against n-tiles
+// NT (w / WM) .. + NT - 1.
+template <int MB, int NB>
 struct LinShape {
+  static constexpr int WARPS = MB == 16 ? 4 : 8;
+  static constexpr int THREADS = 32 * WARPS;
   static constexpr int KS = MB == 16 ? 128 : 64;
+  static constexpr int STAGES = MB == 16 ? 6 : 4;
   static constexpr int NBOX = KS / LIN_BOXK;
-  static constexpr int XBOX = MB * 128;      // bytes
-  static constexpr int WBOX = LIN_NB * 128;  // bytes
-  static constexpr int NT = MB == 16 ? 1 : 4;       // n-tiles (of 8 columns) a warp
-  static constexpr int RED = LIN_THREADS * NT * 4;  // fp32 partials a CTA
-  static constexpr int RING = LIN_STAGES * LIN_STAGE_BYTES;
-  static constexpr int SMEM = 1024 + RING + 8 * LIN_STAGES;  // + 1024-byte alignment slack + an mbarrier a slot
-  static_assert(NBOX * (XBOX + WBOX) == LIN_STAGE_BYTES, "12 KB stages");
+  static constexpr int XBOX = MB * 128;  // bytes
+  static constexpr int WBOX = NB * 128;  // bytes
+  static constexpr int STAGE = NBOX * (XBOX + WBOX);
+  static constexpr int WM = MB / 16;                  // warps along the rows
+  static constexpr int NT = NB / 8 / (WARPS / WM);    // n-tiles a warp
+  static constexpr int RED = THREADS * NT * 4;        // fp32 partials a CTA
+  static constexpr int RING = STAGES * STAGE;
+  static constexpr int SMEM = 1024 + RING + 8 * STAGES;  // + 1024-byte alignment slack + an mbarrier a slot
+  static_assert(WARPS % WM == 0 && NT >= 1 && (NT == 1 || NT % 2 == 0), "warp tiling");
   static_assert(XBOX % 1024 == 0 && WBOX % 1024 == 0, "boxes start on the swizzle pattern's 1 KB period");
   static_assert(RED * 4 <= RING, "partials overlay the ring");
+  static_assert(NB <= 256 && MB <= 256, "a TMA box is at most 256 rows");
 };
 
 // Sticky device-side error bits of the projections (KDA_ERR_TIMEOUT), read and
@@ -167,10 +173,10 @@ struct LinArgs {
 
 // Issued by one thread: the x and weight boxes of stage k0 .. k0 + KS into
 // ring slot `st`, all completing on `bar`.
-template <int MB>
+template <int MB, int NB>
 __device__ __forceinline__ void issue_stage(const LinArgs& a, const CUtensorMap* tmx, const CUtensorMap* tmw,
                                             uint32_t st, uint32_t bar, long long m0, long long n0, long long k0) {
-  using T = LinShape<MB>;
+  using T = LinShape<MB, NB>;
   unsigned long long w_policy, x_policy;  // the weight is read once, x by every CTA
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w_policy));
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(x_policy));
@@ -182,21 +188,21 @@ __device__ __forceinline__ void issue_stage(const LinArgs& a, const CUtensorMap*
   }
 }
 
-template <int MB>
-__global__ void __launch_bounds__(LIN_THREADS) kda_linear_kernel(const __grid_constant__ CUtensorMap tmx,
-                                                                 const __grid_constant__ CUtensorMap tmw,
-                                                                 const LinArgs a) {
-  using T = LinShape<MB>;
-  constexpr int NT = T::NT;
+template <int MB, int NB>
+__global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
+    const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, const LinArgs a) {
+  using T = LinShape<MB, NB>;
+  constexpr int NT = T::NT, STAGES = T::STAGES;
   extern __shared__ __align__(128) unsigned char lsmem[];
   // the ring starts on a 1 KB boundary (the swizzle pattern's period)
   const uint32_t raw = smem_addr(lsmem);
   const uint32_t ring_s = (raw + 1023u) & ~1023u, bar0 = ring_s + T::RING;
   float* red = reinterpret_cast<float*>(lsmem + (ring_s - raw));  // the partial tile, over the drained ring
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wrow = (warp % T::WM) * 16, wnt = (warp / T::WM) * NT;  // the warp's rows and first n-tile
   // without a cluster launch each CTA is a cluster of one: rank 0 of 1
   const unsigned split = cluster_nctarank(), rank = cluster_ctarank();
-  const long long n0 = (long long)cluster_id_x() * LIN_NB;
+  const long long n0 = (long long)cluster_id_x() * NB;
   const long long total = (a.K + T::KS - 1) / T::KS;  // k stages over the whole K (the last one zero-padded)
   const long long s_begin = total * rank / split;
   const long long stages = total * (rank + 1) / split - s_begin;
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(LIN_THREADS) kda_linear_kernel(const __grid_co
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
-    for (int i = 0; i < LIN_STAGES; ++i) mbar_init(bar0 + 8 * i, 1);
+    for (int i = 0; i < STAGES; ++i) mbar_init(bar0 + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -219,83 +225,84 @@ __global__ void __launch_bounds__(LIN_THREADS) kda_linear_kernel(const __grid_co
     for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
     const long long run = dead ? 0 : stages;
     if (threadIdx.x == 0) {  // ring prologue: stages 0 .. STAGES-2 in flight
-      for (int s = 0; s < LIN_STAGES - 1 && s < run; ++s) {
-        const uint32_t slot = (uint32_t)((g0 + s) % LIN_STAGES);
-        issue_stage<MB>(a, &tmx, &tmw, ring_s + slot * LIN_STAGE_BYTES, bar0 + 8 * slot, m0, n0,
-                        (s_begin + s) * T::KS);
+      for (int s = 0; s < STAGES - 1 && s < run; ++s) {
+        const uint32_t slot = (uint32_t)((g0 + s) % STAGES);
+        issue_stage<MB, NB>(a, &tmx, &tmw, ring_s + slot * T::STAGE, bar0 + 8 * slot, m0, n0,
+                            (s_begin + s) * T::KS);
       }
     }
-    long long issued = run < LIN_STAGES - 1 ? run : LIN_STAGES - 1;
+    long long issued = run < STAGES - 1 ? run : STAGES - 1;
     for (long long s = 0; s < run; ++s) {
       const long long g = g0 + s;
-      const uint32_t slot = (uint32_t)(g % LIN_STAGES);
-      const bool ok = mbar_wait_bounded(bar0 + 8 * slot, (unsigned)((g / LIN_STAGES) & 1));
+      const uint32_t slot = (uint32_t)(g % STAGES);
+      const bool ok = mbar_wait_bounded(bar0 + 8 * slot, (unsigned)((g / STAGES) & 1));
       // every warp is past stage s-1 (its slot is free again) and agrees on the outcome
       if (__syncthreads_or(!ok)) {
         dead = true;
         if (threadIdx.x == 0) atomicOr(&g_lin_err, KDA_ERR_TIMEOUT);
         for (long long q = s; q < issued; ++q)  // the copies still in flight land before the CTA moves on
-          mbar_wait_bounded(bar0 + 8 * (uint32_t)((g0 + q) % LIN_STAGES), (unsigned)(((g0 + q) / LIN_STAGES) & 1));
+          mbar_wait_bounded(bar0 + 8 * (uint32_t)((g0 + q) % STAGES), (unsigned)(((g0 + q) / STAGES) & 1));
         break;
       }
-      const long long next = s + LIN_STAGES - 1;
+      const long long next = s + STAGES - 1;
       if (next < run) {
         if (threadIdx.x == 0) {
-          const uint32_t ns = (uint32_t)((g0 + next) % LIN_STAGES);
-          issue_stage<MB>(a, &tmx, &tmw, ring_s + ns * LIN_STAGE_BYTES, bar0 + 8 * ns, m0, n0,
-                          (s_begin + next) * T::KS);
+          const uint32_t ns = (uint32_t)((g0 + next) % STAGES);
+          issue_stage<MB, NB>(a, &tmx, &tmw, ring_s + ns * T::STAGE, bar0 + 8 * ns, m0, n0,
+                              (s_begin + next) * T::KS);
         }
         issued = next + 1;
       }
-      const uint32_t xs = ring_s + slot * LIN_STAGE_BYTES, ws = xs + T::NBOX * T::XBOX;
-      if (MB == 16) {
-        // all warps: the 16 x rows; warp w: weight rows 8w .. 8w + 7 (its n-tile)
+      const uint32_t xs = ring_s + slot * T::STAGE, ws = xs + T::NBOX * T::XBOX;
+      if (NT == 1) {
+        // one n-tile: B fragments of two k16 steps in one ldmatrix.x4
 #pragma unroll
         for (int kk = 0; kk < T::KS / 16; kk += 2) {
           const int box = kk >> 2, c0 = 2 * (kk & 3);
           uint32_t a0[4], a1[4], b[4];
-          ldsm_x4(a0, swz(xs + box * T::XBOX, lr + (lm & 1) * 8, c0 + (lm >> 1)));
-          ldsm_x4(a1, swz(xs + box * T::XBOX, lr + (lm & 1) * 8, c0 + 2 + (lm >> 1)));
-          ldsm_x4(b, swz(ws + box * T::WBOX, warp * 8 + lr, c0 + lm));
+          ldsm_x4(a0, swz(xs + box * T::XBOX, wrow + lr + (lm & 1) * 8, c0 + (lm >> 1)));
+          ldsm_x4(a1, swz(xs + box * T::XBOX, wrow + lr + (lm & 1) * 8, c0 + 2 + (lm >> 1)));
+          ldsm_x4(b, swz(ws + box * T::WBOX, wnt * 8 + lr, c0 + lm));
           mma_bf16(acc[0], a0[0], a0[1], a0[2], a0[3], b[0], b[1]);
           mma_bf16(acc[0], a1[0], a1[1], a1[2], a1[3], b[2], b[3]);
         }
       } else {
-        // warp w: x rows 16w .. 16w + 15 against all four n-tiles
+        // the warp's 16 rows against its NT n-tiles, two n-tiles an ldmatrix.x4
 #pragma unroll
         for (int kk = 0; kk < T::KS / 16; ++kk) {
           const int box = kk >> 2, c0 = 2 * (kk & 3);
           const uint32_t xb = xs + box * T::XBOX, wb = ws + box * T::WBOX;
-          uint32_t af[4], b01[4], b23[4];
-          ldsm_x4(af, swz(xb, warp * 16 + lr + (lm & 1) * 8, c0 + (lm >> 1)));
-          ldsm_x4(b01, swz(wb, (lm >> 1) * 8 + lr, c0 + (lm & 1)));
-          ldsm_x4(b23, swz(wb, (2 + (lm >> 1)) * 8 + lr, c0 + (lm & 1)));
-          mma_bf16(acc[0], af[0], af[1], af[2], af[3], b01[0], b01[1]);
-          mma_bf16(acc[NT > 1 ? 1 : 0], af[0], af[1], af[2], af[3], b01[2], b01[3]);
-          mma_bf16(acc[NT > 2 ? 2 : 0], af[0], af[1], af[2], af[3], b23[0], b23[1]);
-          mma_bf16(acc[NT > 3 ? 3 : 0], af[0], af[1], af[2], af[3], b23[2], b23[3]);
+          uint32_t af[4];
+          ldsm_x4(af, swz(xb, wrow + lr + (lm & 1) * 8, c0 + (lm >> 1)));
+#pragma unroll
+          for (int jp = 0; jp < NT / 2; ++jp) {
+            uint32_t b[4];
+            ldsm_x4(b, swz(wb, (wnt + 2 * jp + (lm >> 1)) * 8 + lr, c0 + (lm & 1)));
+            mma_bf16(acc[2 * jp], af[0], af[1], af[2], af[3], b[0], b[1]);
+            mma_bf16(acc[2 * jp + 1], af[0], af[1], af[2], af[3], b[2], b[3]);
+          }
         }
       }
     }
     __syncthreads();  // every warp is done with the ring: the partials overlay it
-    // partial element e = ((j * 4 + c) * 128 + thread): fragment c of n-tile j of a thread
+    // partial element e = ((j * 4 + c) * THREADS + thread): fragment c of the thread's n-tile j
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) red[(j * 4 + c) * LIN_THREADS + threadIdx.x] = acc[j][c];
+      for (int c = 0; c < 4; ++c) red[(j * 4 + c) * T::THREADS + threadIdx.x] = acc[j][c];
     // these generic-proxy writes precede the next pass's tensor copies into the same bytes
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (split > 1) cluster_sync(); else __syncthreads();
     // this CTA's share of the tile: elements [rank * RED / split, (rank + 1) * RED / split)
     const int e_end = (int)(T::RED * (rank + 1) / split);
-    for (int e = (int)(T::RED * rank / split) + threadIdx.x; e < e_end; e += LIN_THREADS) {
+    for (int e = (int)(T::RED * rank / split) + threadIdx.x; e < e_end; e += T::THREADS) {
       float v = 0.0f;
       for (unsigned q = 0; q < split; ++q) v += split > 1 ? ld_peer_f32(red + e, q) : red[e];
       // accumulator layout of m16n8: c0, c1 at row lane/4, columns 2 (lane % 4) + {0, 1}; c2, c3 eight rows down
-      const int t = e % LIN_THREADS, jc = e / LIN_THREADS, j = jc >> 2, c = jc & 3;
+      const int t = e % T::THREADS, jc = e / T::THREADS, j = jc >> 2, c = jc & 3;
       const int tw = t >> 5, tl = t & 31;
-      const long long m = m0 + (MB == 16 ? 0 : tw * 16) + (tl >> 2) + (c >> 1) * 8;
-      const long long n = n0 + ((MB == 16 ? tw : 0) + j) * 8 + (tl & 3) * 2 + (c & 1);
+      const long long m = m0 + (tw % T::WM) * 16 + (tl >> 2) + (c >> 1) * 8;
+      const long long n = n0 + ((tw / T::WM) * NT + j) * 8 + (tl & 3) * 2 + (c & 1);
       if (m < a.M && n < a.N) a.y[m * a.ldy + n] = __float2bfloat16_rn(v);
     }
     // the peers have read this CTA's partials before it refills the ring or exits
@@ -337,56 +344,55 @@ bool encode_map(CUtensorMap* map, const void* base, long long rows, long long co
 }
 
 // K split C (<= 8, <= the K stages): a CTA's time is about its share of the
-// stages, so the kernel's is about waves x stages / C, waves = the grid over
-// the GPU's resident CTA slots, rounded up; the smallest C that minimises
-// ceil(tiles C / slots) / C.
-template <int MB>
-int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, long long tiles, cudaStream_t st) {
-  using T = LinShape<MB>;
+// stages, so the kernel's is about waves x stages / C, waves = the tiles over
+// the clusters of C that the GPU holds at once (cudaOccupancyMaxActiveClusters:
+// a cluster must fit one GPC, so large clusters fit fewer times than the SM
+// count suggests), rounded up; the smallest C that minimises that.
+template <int MB, int NB>
+int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st) {
+  using T = LinShape<MB, NB>;
+  const long long tiles = (a.N + NB - 1) / NB;
   const int box_rows = (int)(a.M < MB ? a.M : MB);
   a.x_box_bytes = (unsigned)box_rows * 128u;
   CUtensorMap tmx, tmw;
-  if (!encode_map(&tmx, x, a.M, a.K, ldx, box_rows) || !encode_map(&tmw, w, a.N, a.K, a.K, LIN_NB))
-    return KDA_ECUDA;
+  if (!encode_map(&tmx, x, a.M, a.K, ldx, box_rows) || !encode_map(&tmw, w, a.N, a.K, a.K, NB)) return KDA_ECUDA;
   // the shared-memory attribute is per device and cheap: set on every call
-  if (cudaFuncSetAttribute(kda_linear_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
+  if (cudaFuncSetAttribute(kda_linear_kernel<MB, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
       cudaSuccess)
     return KDA_ECUDA;
-  // resident CTA slots of the device, looked up once per device and shape
-  static long long slot_cache[64];
+  // clusters of each size the device holds at once, looked up once per device and shape
+  static int cluster_cache[64][LIN_MAX_SPLIT + 1];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ECUDA;
-  long long slots = dev < 64 ? slot_cache[dev] : 0;
-  if (slots <= 0) {
-    int sms = 0, per_sm = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_kernel<MB>, LIN_THREADS, T::SMEM) !=
-            cudaSuccess)
-      return KDA_ECUDA;
-    slots = (long long)sms * (per_sm > 0 ? per_sm : 1);
-    if (dev < 64) slot_cache[dev] = slots;
-  }
-  const long long stages = (a.K + T::KS - 1) / T::KS;
-  long long split = 1;
-  double best = 1e300;
-  for (long long c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
-    const double cost = (double)((tiles * c + slots - 1) / slots) / (double)c;
-    if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
-  }
-  if (tiles * split > 0x7fffffffLL) return KDA_EINVAL;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
-  cfg.blockDim = dim3(LIN_THREADS, 1, 1);
+  cfg.blockDim = dim3(T::THREADS, 1, 1);
   cfg.dynamicSmemBytes = T::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)split;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kda_linear_kernel<MB>, tmx, tmw, a) != cudaSuccess) return KDA_ECUDA;
+  const long long stages = (a.K + T::KS - 1) / T::KS;
+  long long split = 1;
+  double best = 1e300;
+  for (int c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
+    int held = dev < 64 ? cluster_cache[dev][c] : 0;
+    if (held <= 0) {
+      attr[0].val.clusterDim.x = (unsigned)c;
+      cfg.gridDim = dim3((unsigned)c, 1, 1);
+      if (cudaOccupancyMaxActiveClusters(&held, kda_linear_kernel<MB, NB>, &cfg) != cudaSuccess) return KDA_ECUDA;
+      if (held <= 0) continue;
+      if (dev < 64) cluster_cache[dev][c] = held;
+    }
+    const double cost = (double)((tiles + held - 1) / held) / (double)c;
+    if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
+  }
+  if (tiles * split > 0x7fffffffLL) return KDA_EINVAL;
+  cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
+  attr[0].val.clusterDim.x = (unsigned)split;
+  if (cudaLaunchKernelEx(&cfg, kda_linear_kernel<MB, NB>, tmx, tmw, a) != cudaSuccess) return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
@@ -400,8 +406,7 @@ extern "C" int kda_linear(const void* x, long long rows, long long ldx, const vo
   // tensor maps: 16-byte aligned bases and row strides; coordinates fit 32 bits
   if (!lin_aligned(x, 16) || !lin_aligned(w, 16) || (ldx % 8) != 0 || !lin_aligned(y, 2)) return KDA_EINVAL;
   if (K > 0x7fffffffLL || N > 0x7fffffffLL || rows > 0x7fffffffLL) return KDA_EINVAL;
-  const long long tiles = (N + LIN_NB - 1) / LIN_NB;
-  // rows <= 16: the one-tile shape
+  // rows <= 16: the one-tile shape; else 64-row passes over 128-column tiles
   const bool small = rows <= 16;
   LinArgs a;
   a.y = static_cast<__nv_bfloat16*>(y);
@@ -411,7 +416,7 @@ extern "C" int kda_linear(const void* x, long long rows, long long ldx, const vo
   a.K = K;
   a.x_box_bytes = 0;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  return small ? lin_launch<16>(x, ldx, w, a, tiles, st) : lin_launch<64>(x, ldx, w, a, tiles, st);
+  return small ? lin_launch<16, 32>(x, ldx, w, a, st) : lin_launch<64, 128>(x, ldx, w, a, st);
 }
 
 extern "C" int kda_linear_check(void* cuda_stream, unsigned* device_flags) {
