@@ -146,12 +146,31 @@ __device__ __forceinline__ unsigned cluster_id_x() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// fp32 at the same shared-memory offset in CTA `rank` of the cluster
-__device__ __forceinline__ float ld_peer_f32(const float* local, unsigned rank) {
+// 16 bytes at the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ float4 ld_peer_f32x4(const float* local, unsigned rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote));
+  return v;
+}
+// Sum of the `split` CTAs' four floats at `local`, in rank order; every load is
+// issued before the first add, so the distributed-shared-memory round trips overlap.
+__device__ __forceinline__ float4 cluster_sum4(const float* local, unsigned split) {
+  float4 t[LIN_MAX_SPLIT];
+#pragma unroll
+  for (int q = 0; q < LIN_MAX_SPLIT; ++q)
+    t[q] = (unsigned)q < split ? ld_peer_f32x4(local, q) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 v = t[0];
+#pragma unroll
+  for (int q = 1; q < LIN_MAX_SPLIT; ++q) {
+    v.x += t[q].x;
+    v.y += t[q].y;
+    v.z += t[q].z;
+    v.w += t[q].w;
+  }
   return v;
 }
 
@@ -169,6 +188,7 @@ struct LinArgs {
   long long ldy;
   long long M, N, K;
   unsigned x_box_bytes;  // bytes of one x box: its rows (min(rows, MB)) x 128
+  int y_vec;             // y and ldy allow 16-byte stores (y 16-byte aligned, ldy % 8 == 0)
 };
 
 // Issued by one thread: the x and weight boxes of stage k0 .. k0 + KS into
@@ -293,21 +313,281 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
     // these generic-proxy writes precede the next pass's tensor copies into the same bytes
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (split > 1) cluster_sync(); else __syncthreads();
-    // this CTA's share of the tile: elements [rank * RED / split, (rank + 1) * RED / split)
-    const int e_end = (int)(T::RED * (rank + 1) / split);
-    for (int e = (int)(T::RED * rank / split) + threadIdx.x; e < e_end; e += T::THREADS) {
-      float v = 0.0f;
-      for (unsigned q = 0; q < split; ++q) v += split > 1 ? ld_peer_f32(red + e, q) : red[e];
-      // accumulator layout of m16n8: c0, c1 at row lane/4, columns 2 (lane % 4) + {0, 1}; c2, c3 eight rows down
-      const int t = e % T::THREADS, jc = e / T::THREADS, j = jc >> 2, c = jc & 3;
-      const int tw = t >> 5, tl = t & 31;
-      const long long m = m0 + (tw % T::WM) * 16 + (tl >> 2) + (c >> 1) * 8;
-      const long long n = n0 + ((tw / T::WM) * NT + j) * 8 + (tl & 3) * 2 + (c & 1);
-      if (m < a.M && n < a.N) a.y[m * a.ldy + n] = __float2bfloat16_rn(v);
+    // this CTA's share of the tile: quads of elements [rank * Q / split, (rank + 1) * Q / split), Q = RED / 4
+    constexpr int Q = T::RED / 4;
+    const int q_end = (int)(Q * (rank + 1) / split);
+    for (int qd = (int)(Q * rank / split) + threadIdx.x; qd < q_end; qd += T::THREADS) {
+      const float4 v4 = split > 1 ? cluster_sum4(red + 4 * qd, split) : *reinterpret_cast<const float4*>(red + 4 * qd);
+      const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // accumulator layout of m16n8: c0, c1 at row lane/4, columns 2 (lane % 4) + {0, 1}; c2, c3 eight rows down
+        const int e = 4 * qd + i;
+        const int t = e % T::THREADS, jc = e / T::THREADS, j = jc >> 2, c = jc & 3;
+        const int tw = t >> 5, tl = t & 31;
+        const long long m = m0 + (tw % T::WM) * 16 + (tl >> 2) + (c >> 1) * 8;
+        const long long n = n0 + ((tw / T::WM) * NT + j) * 8 + (tl & 3) * 2 + (c & 1);
+        if (m < a.M && n < a.N) a.y[m * a.ldy + n] = __float2bfloat16_rn(vv[i]);
+      }
     }
     // the peers have read this CTA's partials before it refills the ring or exits
     if (split > 1) cluster_sync(); else __syncthreads();
   }
+}
+
+// ---------------------------------------------------------------------------
+// rows > 64: tcgen05 (5th-generation tensor core) tiles.  A CTA owns a
+// 128 x 256 output tile (rows past `rows` are the copy engine's zeros), K in
+// stages of 64 through a four-deep ring (x box 16 KB + weight box 32 KB, both
+// 128-byte swizzled: the canonical K-major layout of the MMA's shared-memory
+// descriptors).  Warp 0's lane 0 issues the TMA copies, warp 1's lane 0 the
+// MMAs (M 128, N 256, K 16; four a stage) into a 256-column fp32 accumulator
+// in tensor memory; each MMA group's commit frees its ring slot.  After the
+// last stage the four warps read the accumulator (warp w: lanes = rows 32w ..
+// 32w + 31), stage it in shared memory (column-major, padded) and write bf16.
+// K split over a cluster as in the kernel above, the partial tiles summed
+// through distributed shared memory.  The copy engine's bytes per SM bound
+// these tiles as much as the tensor pipe does, so the tile is as wide as one
+// MMA allows (x : W bytes = 1 : 2).
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4, TC_THREADS = 128;
+constexpr int TC_ABYTES = TC_BM * 128, TC_BBYTES = TC_BN * 128;  // one 64-k box each
+constexpr int TC_STAGE = TC_ABYTES + TC_BBYTES;
+constexpr int TC_RING = TC_STAGES * TC_STAGE;
+constexpr int TC_RED_LD = TC_BM + 4;  // partial tile, column-major: element (r, c) at c * 132 + r (16-byte rows)
+constexpr int TC_SMEM = 1024 + TC_RING + 8 * (2 * TC_STAGES + 1) + 16;
+constexpr double TC_FIXED_STAGES = 16.0;  // F of the split model below for these tiles (a stage ~0.3 us)
+static_assert(TC_BN * TC_RED_LD * 4 <= TC_RING, "partials overlay the ring");
+
+// tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1),
+// bf16 A and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
+// at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t TC_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TC_BN >> 3) << 17) |
+                              ((uint32_t)(TC_BM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
+// whose 8-row x 128-byte swizzle atoms are stacked every 1024 bytes: start
+// address >> 4 (bits 0-13), leading offset (bits 16-29; not used by this
+// layout, set to 1), stride between atoms 1024 >> 4 (bits 32-45), the fixed
+// 0b001 at bits 46-48, base offset 0 (the atoms start on 1024-byte
+// boundaries), swizzle mode 2 (128-byte) at bits 61-63.
+__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                                    const __grid_constant__ CUtensorMap tmw,
+                                                                    const LinArgs a, int tiles_n) {
+  extern __shared__ __align__(128) unsigned char tsmem[];
+  const uint32_t raw = smem_addr(tsmem);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  const uint32_t full0 = ring + TC_RING, empty0 = full0 + 8 * TC_STAGES, accum_bar = empty0 + 8 * TC_STAGES;
+  const uint32_t tmem_slot = accum_bar + 8;  // tcgen05.alloc writes the accumulator's address here
+  unsigned char* ring_p = tsmem + (ring - raw);
+  float* red = reinterpret_cast<float*>(ring_p);
+  volatile uint32_t* tmem_slot_p = reinterpret_cast<volatile uint32_t*>(ring_p + (tmem_slot - ring));
+  volatile int* consumed_p = reinterpret_cast<volatile int*>(ring_p + (tmem_slot - ring) + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned split = cluster_nctarank(), rank = cluster_ctarank();
+  const long long tile = cluster_id_x();
+  const long long m0 = (tile / tiles_n) * TC_BM, n0 = (tile % tiles_n) * TC_BN;
+  const long long total = (a.K + TC_BK - 1) / TC_BK;
+  const long long s_begin = total * rank / split;
+  const long long stages = total * (rank + 1) / split - s_begin;
+
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
+    for (int i = 0; i < TC_STAGES; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    mbar_init(accum_bar, 1);
+    *consumed_p = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {  // the accumulator: 128 lanes x 128 fp32 columns of tensor memory
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(TC_BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot_p;
+
+  // Warps 0 and 1 run their loops whole (converged, spinning on the barrier
+  // without the sleep hint: a suspended thread wakes late), lane 0 issuing.
+  bool ok_all = true;
+  long long issued = 0;
+  if (warp == 0) {  // producer
+    // the weight tile is read once when there is one row tile (evict first), else kept for the others
+    unsigned long long w_policy, x_policy;
+    if (a.M <= TC_BM)
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w_policy));
+    else
+      asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(w_policy));
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(x_policy));
+    for (long long s = 0; s < stages; ++s) {
+      const uint32_t slot = (uint32_t)(s % TC_STAGES);
+      const bool ok = mbar_wait_bounded(empty0 + 8 * slot, (unsigned)(((s / TC_STAGES) & 1) ^ 1));
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        ok_all = false;
+        break;
+      }
+      if (lane == 0) {
+        const uint32_t st = ring + slot * TC_STAGE, bar = full0 + 8 * slot;
+        const int k = (int)((s_begin + s) * TC_BK);
+        mbar_expect_tx(bar, TC_STAGE);
+        tma_box(st, &tmx, k, (int)m0, bar, x_policy);
+        tma_box(st + TC_ABYTES, &tmw, k, (int)n0, bar, w_policy);
+      }
+      __syncwarp();
+      issued = s + 1;
+    }
+  } else if (warp == 1) {  // MMA issuer
+    long long s = 0;
+    for (; s < stages; ++s) {
+      const uint32_t slot = (uint32_t)(s % TC_STAGES);
+      const bool ok = mbar_wait_bounded(full0 + 8 * slot, (unsigned)((s / TC_STAGES) & 1));
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        ok_all = false;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (lane == 0) {
+        const uint32_t st = ring + slot * TC_STAGE;
+#pragma unroll
+        for (int k = 0; k < TC_BK / 16; ++k) {  // 16 k = 32 bytes along the swizzled row
+          const uint64_t da = tc_desc(st + 32 * k), db = tc_desc(st + TC_ABYTES + 32 * k);
+          const uint32_t acc = (s > 0 || k > 0) ? 1u : 0u;
+          asm volatile(
+              "{\n\t.reg .pred p;\n\t"
+              "setp.ne.u32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+              "l"(da), "l"(db), "r"(TC_IDESC), "r"(acc)
+              : "memory");
+        }
+        // the slot is free once these MMAs have read it
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 +
+                                                                                                       8 * slot)
+                     : "memory");
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      *consumed_p = (int)s;
+      // the accumulator is final once every MMA issued above has completed
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(accum_bar)
+                   : "memory");
+    }
+    __syncwarp();
+  }
+  // everyone: wait for the accumulator (no MMA at all when this CTA has no stages)
+  bool have = stages > 0;
+  if (have && !mbar_wait_bounded(accum_bar, 0)) ok_all = false;
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const bool dead = __syncthreads_or(!ok_all);
+  if (threadIdx.x == 0 && dead) atomicOr(&g_lin_err, KDA_ERR_TIMEOUT);
+  if (warp == 0 && lane == 0 && dead) {
+    // copies issued but never consumed land before the ring is reused or the CTA exits
+    for (long long q = *consumed_p; q < issued; ++q)
+      mbar_wait_bounded(full0 + 8 * (uint32_t)(q % TC_STAGES), (unsigned)((q / TC_STAGES) & 1));
+  }
+  __syncthreads();
+  const int r = warp * 32 + lane;
+  const int rows_here = (int)(a.M - m0 < TC_BM ? a.M - m0 : TC_BM);
+  if (split == 1) {
+    // accumulator -> bf16 -> global: thread (warp w, lane l) owns row 32w + l, 32 columns a load
+    __nv_bfloat16* yr = a.y + (m0 + r) * a.ldy;
+#pragma unroll 1
+    for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+      uint32_t v[32];
+      if (have && !dead) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+            "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+              "=r"(v[30]), "=r"(v[31])
+            : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0u;
+      }
+      if (r >= rows_here) continue;
+      const long long n = n0 + c0;
+      if (a.y_vec && n + 32 <= a.N) {
+        uint32_t p[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          p[j] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(yr + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n + j < a.N) yr[n + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+      }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {  // the accumulator is read: give the tensor memory back
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
+    }
+    return;
+  }
+  // K split: accumulator -> shared memory (column-major, padded), 32 columns a load
+#pragma unroll 1
+  for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+    uint32_t v[32];
+    if (have && !dead) {
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+          "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+            "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+            "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+          : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) red[(c0 + j) * TC_RED_LD + r] = __uint_as_float(v[j]);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  cluster_sync();
+  if (warp == 0) {  // the accumulator is read: give the tensor memory back
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
+  }
+  // this CTA's share of the tile: (4-row group, column) pairs in row-group-major order, each
+  // summed over the cluster's partials with 16-byte loads
+  const int E = ((rows_here + 3) / 4) * TC_BN;
+  const int e_end = (int)((long long)E * (rank + 1) / split);
+  for (int e = (int)((long long)E * rank / split) + threadIdx.x; e < e_end; e += TC_THREADS) {
+    const int rq = e / TC_BN, cc = e % TC_BN;
+    const float4 v4 = cluster_sum4(red + cc * TC_RED_LD + 4 * rq, split);
+    const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+    const long long n = n0 + cc;
+    if (n < a.N) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (4 * rq + i < rows_here) a.y[(m0 + 4 * rq + i) * a.ldy + n] = __float2bfloat16_rn(vv[i]);
+    }
+  }
+  // the peers have read this CTA's partials before it exits
+  cluster_sync();
 }
 
 bool lin_aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
@@ -344,10 +624,13 @@ bool encode_map(CUtensorMap* map, const void* base, long long rows, long long co
 }
 
 // K split C (<= 8, <= the K stages): a CTA's time is about its share of the
-// stages, so the kernel's is about waves x stages / C, waves = the tiles over
-// the clusters of C that the GPU holds at once (cudaOccupancyMaxActiveClusters:
-// a cluster must fit one GPC, so large clusters fit fewer times than the SM
-// count suggests), rounded up; the smallest C that minimises that.
+// stages plus a fixed part (the first copies' latency, the reduction and the
+// stores), so the kernel's is about waves x (stages / C + F), waves = the
+// tiles over the clusters of C that the GPU holds at once
+// (cudaOccupancyMaxActiveClusters -- a cluster must fit one GPC, so large
+// clusters fit fewer times than the SM count suggests -- capped by the
+// resident CTA slots), rounded up; the smallest C that minimises that.
+constexpr double LIN_FIXED_STAGES = 4.0;  // F for the mma.sync tiles, in stages (measured per-stage ~0.5 us)
 template <int MB, int NB>
 int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st) {
   using T = LinShape<MB, NB>;
@@ -382,17 +665,75 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
     if (held <= 0) {
       attr[0].val.clusterDim.x = (unsigned)c;
       cfg.gridDim = dim3((unsigned)c, 1, 1);
-      if (cudaOccupancyMaxActiveClusters(&held, kda_linear_kernel<MB, NB>, &cfg) != cudaSuccess) return KDA_ECUDA;
+      int sms = 0, per_sm = 0;
+      if (cudaOccupancyMaxActiveClusters(&held, kda_linear_kernel<MB, NB>, &cfg) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_kernel<MB, NB>, T::THREADS, T::SMEM) !=
+              cudaSuccess)
+        return KDA_ECUDA;
+      // never more clusters than the resident CTA slots hold
+      const int cap = sms * (per_sm > 0 ? per_sm : 1) / c;
+      if (held > cap) held = cap;
       if (held <= 0) continue;
       if (dev < 64) cluster_cache[dev][c] = held;
     }
-    const double cost = (double)((tiles + held - 1) / held) / (double)c;
+    const double cost = (double)((tiles + held - 1) / held) * ((double)stages / c + LIN_FIXED_STAGES);
     if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
   }
   if (tiles * split > 0x7fffffffLL) return KDA_EINVAL;
   cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
   attr[0].val.clusterDim.x = (unsigned)split;
   if (cudaLaunchKernelEx(&cfg, kda_linear_kernel<MB, NB>, tmx, tmw, a) != cudaSuccess) return KDA_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st) {
+  const long long tiles_n = (a.N + TC_BN - 1) / TC_BN, tiles = ((a.M + TC_BM - 1) / TC_BM) * tiles_n;
+  CUtensorMap tmx, tmw;
+  if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, TC_BN)) return KDA_ECUDA;
+  if (cudaFuncSetAttribute(kda_linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM) !=
+      cudaSuccess)
+    return KDA_ECUDA;
+  static int cluster_cache[64][LIN_MAX_SPLIT + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(TC_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = TC_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const long long stages = (a.K + TC_BK - 1) / TC_BK;
+  long long split = 1;
+  double best = 1e300;
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_tc_kernel, TC_THREADS, TC_SMEM) !=
+          cudaSuccess)
+    return KDA_ECUDA;
+  for (int c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
+    int held = dev < 64 ? cluster_cache[dev][c] : 0;
+    if (held <= 0) {
+      attr[0].val.clusterDim.x = (unsigned)c;
+      cfg.gridDim = dim3((unsigned)c, 1, 1);
+      if (cudaOccupancyMaxActiveClusters(&held, kda_linear_tc_kernel, &cfg) != cudaSuccess) return KDA_ECUDA;
+      // never more clusters than the resident CTA slots hold
+      const int cap = sms * (per_sm > 0 ? per_sm : 1) / c;
+      if (held > cap) held = cap;
+      if (held <= 0) continue;
+      if (dev < 64) cluster_cache[dev][c] = held;
+    }
+    const double cost = (double)((tiles + held - 1) / held) * ((double)stages / c + TC_FIXED_STAGES);
+    if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
+  }
+  if (tiles * split > 0x7fffffffLL) return KDA_EINVAL;
+  cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
+  attr[0].val.clusterDim.x = (unsigned)split;
+  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel, tmx, tmw, a, (int)tiles_n) != cudaSuccess) return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
@@ -406,8 +747,9 @@ extern "C" int kda_linear(const void* x, long long rows, long long ldx, const vo
   // tensor maps: 16-byte aligned bases and row strides; coordinates fit 32 bits
   if (!lin_aligned(x, 16) || !lin_aligned(w, 16) || (ldx % 8) != 0 || !lin_aligned(y, 2)) return KDA_EINVAL;
   if (K > 0x7fffffffLL || N > 0x7fffffffLL || rows > 0x7fffffffLL) return KDA_EINVAL;
-  // rows <= 16: the one-tile shape; else 64-row passes over 128-column tiles
-  const bool small = rows <= 16;
+  // rows <= 16: the one-tile shape; <= 64: one 64-row pass over 128-column
+  // tiles (HBM-bound: mma.sync keeps up, and its x tile is not padded to the
+  // tcgen05 tile's 128 rows); beyond: tcgen05 tiles
   LinArgs a;
   a.y = static_cast<__nv_bfloat16*>(y);
   a.ldy = ldy;
@@ -415,8 +757,11 @@ extern "C" int kda_linear(const void* x, long long rows, long long ldx, const vo
   a.N = N;
   a.K = K;
   a.x_box_bytes = 0;
+  a.y_vec = lin_aligned(y, 16) && (ldy % 8) == 0;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  return small ? lin_launch<16, 32>(x, ldx, w, a, st) : lin_launch<64, 128>(x, ldx, w, a, st);
+  if (rows <= 16) return lin_launch<16, 32>(x, ldx, w, a, st);
+  if (rows <= 64) return lin_launch<64, 128>(x, ldx, w, a, st);
+  return lin_launch_tc(x, ldx, w, a, st);
 }
 
 extern "C" int kda_linear_check(void* cuda_stream, unsigned* device_flags) {
