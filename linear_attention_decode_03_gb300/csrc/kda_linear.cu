@@ -5,7 +5,8 @@
 // Sources: the K1 page ("vllm.models.kimi_k3.amd.specialized_decode.mono.
 // attention.kda", module docstring) gives the layer's in_proj GEMV in front
 // of the KDA core -- x [rows, 7168] to the packed projection row -- and the
-// K2a page ("...attn_post") the o_proj GEMV after it (core_out [rows, D] to
+// K2a page ("vllm.models.kimi_k3.amd.specialized_decode.mono.attention.back",
+// module docstring: K2a attn_post) the o_proj GEMV after it (core_out [rows, D] to
 // [rows, 7168]); both weights are [out_features, in_features], the layout of
 // a torch Linear.
 //

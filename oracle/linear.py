@@ -6,8 +6,9 @@ with the CUDA library.
 
 Sources: the K1 page ("vllm.models.kimi_k3.amd.specialized_decode.mono.
 attention.kda") puts an in_proj GEMV in front of the KDA core (x [rows, 7168]
-to the packed projection row) and the K2a page ("...attn_post") an o_proj GEMV
-after it (core_out [rows, D] to [rows, 7168]).  A GEMV has a plain
+to the packed projection row) and the K2a page ("vllm.models.kimi_k3.amd.
+specialized_decode.mono.attention.back", module docstring: K2a attn_post) an
+o_proj GEMV after it (core_out [rows, D] to [rows, 7168]).  A GEMV has a plain
 definition, so the oracle is that definition: the exact product of the bf16
 inputs in fp64, rounded once to bf16 (nearest even).  W is [out, in] (a torch
 Linear weight).

@@ -1,8 +1,9 @@
 """kda_linear (the in_proj / o_proj projections) against the projection
 oracle: bf16 outputs within one bf16 step of the correctly rounded product,
 plus the fp32 accumulation's share (2^-14 of sum |x_k w_k|); the in_proj and
-o_proj shapes of the 12-head layer, rows past 64 (several passes), ragged
-column tails (odd N), a strided x."""
+o_proj shapes of the 12-head layer through all three kernels (rows <= 16,
+17..64, > 64 on tcgen05), ragged column tails (odd N), ragged K, K splits, a
+strided x."""
 from __future__ import annotations
 
 import numpy as np
@@ -50,10 +51,15 @@ def test_in_proj_shape(rows):
     _check(rows, 7168, 6284, seed=rows)
 
 
-@pytest.mark.parametrize("rows", [1, 64])
+@pytest.mark.parametrize("rows", [1, 64, 256])
 def test_o_proj_shape(rows):
-    # core_out [rows, 1536] . W_o [7168, 1536]^T
+    # core_out [rows, 1536] . W_o [7168, 1536]^T; 256 rows: two tcgen05 row tiles
     _check(rows, 1536, 7168, seed=100 + rows, wscale=0.05)
+
+
+def test_in_proj_tensor_core_tiles():
+    # 160 rows: tcgen05 tiles, a full 128-row tile and a 32-row one (rows past 160 zero-filled)
+    _check(160, 7168, 6284, seed=160)
 
 
 def test_several_passes_ragged_tail_and_strided_x():
