@@ -429,6 +429,141 @@ def run_linear(args, w: I.Workload):
     print(json.dumps(line), flush=True)
 
 
+LAYER_METRIC = "KDA layer tokens/s (in_proj -> KDA core -> o_proj as one CUDA graph) vs GB300 peak, 1 GPU"
+
+
+def _timed_launches(fn, steps, stream, flush_w, flush_r):
+    """Per-call device times (ms) of `fn`, L2 flushed (outside the events) before each."""
+    import torch
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush_w.fill_(float(i))
+        flush_r.sum()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def run_layer(args, w: I.Workload):
+    """--op layer: one step of the whole layer -- in_proj (x [rows, 7168] -> the packed
+    projection row), the KDA core, o_proj (core_out -> [rows, 7168]) -- recorded once as
+    a CUDA graph (PreparedKda.layer_plan, programmatic dependent launches between the
+    kernels) and replayed every step, L2 flushed between steps. Also timed: the same graph
+    without dependent launches, and the three calls made one by one."""
+    import torch
+    import linear_attention_decode_03_gb300 as kda
+    from oracle import linear as OL
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    kda.build()
+    kda.load_library()
+    si = I.make_step_inputs(w)
+    dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1,
+                        state_dtype=args.state_dtype)
+    rng = np.random.Generator(np.random.PCG64(w.seed + 29))
+    xb = I.to_bf16_bits(rng.normal(0.0, 1.0, size=(w.rows, HIDDEN)).astype(np.float32))
+    wib = I.to_bf16_bits(rng.normal(0.0, 0.02, size=(w.pitch, HIDDEN)).astype(np.float32))
+    wob = I.to_bf16_bits(rng.normal(0.0, 0.05, size=(HIDDEN, w.dim)).astype(np.float32))
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    x, w_in, w_o = dev(xb), dev(wib), dev(wob)
+    y = torch.empty((w.rows, HIDDEN), dtype=torch.bfloat16, device=device)
+    caches = (dw.conv, dw.state)
+    masks = {"both": 3, "none": 0, "step_edge": 1, "o_proj_edge": 2}
+    plans = {k: dw.prep.layer_plan(x, w_in, dw.projected, dw.out, w_o, y, caches=caches, slots=dw.slots,
+                                   accepted=dw.accepted, pdl=m) for k, m in masks.items()}
+    head = args.layer_pdl
+    stream = torch.cuda.current_stream(device)
+    flush_w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    flush_r = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def separate():
+        kda.linear(x, w_in, dw.projected)
+        dw.prep.run(dw.projected, dw.out, caches=caches, slots=dw.slots, accepted=dw.accepted)
+        kda.linear(dw.out, w_o, y)
+
+    for _ in range(args.warmup):
+        for p in plans.values():
+            p.launch()
+        separate()
+    torch.cuda.synchronize()
+    if dw.prep.check() != 0 or kda.kda_linear_check() != 0:
+        raise RuntimeError("device error bits set during warm-up")
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    t_host0 = time.time()
+    t_head = _timed_launches(plans[head].launch, args.steps, stream, flush_w, flush_r)
+    t_host1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    others = {k: sum(_timed_launches(p.launch, args.steps, stream, flush_w, flush_r)) / args.steps
+              for k, p in plans.items() if k != head}
+    t_sep = _timed_launches(separate, args.steps, stream, flush_w, flush_r)
+    if dw.prep.check() != 0 or kda.kda_linear_check() != 0:
+        raise RuntimeError("device error bits set during the timed steps")
+    ms = sum(t_head) / args.steps
+
+    # e2e: x up from pinned host memory and y back every step, around the plan's launch
+    hx = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hy = torch.empty((w.rows, HIDDEN), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(hx, non_blocking=True)
+        plans[head].launch()
+        hy.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    state_b, step_b = algorithmic_bytes(w, args.state_dtype)
+    proj_b = (w.pitch * HIDDEN + HIDDEN * w.dim) * 2 + w.rows * (HIDDEN * 2 + w.pitch + w.dim) * 2
+    layer_b = step_b + proj_b
+    flops = 2 * w.rows * HIDDEN * (w.pitch + w.dim)
+    peak, peak_kind = load_peaks()
+    achieved = layer_b / (ms / 1e3) / 1e9
+    line = {
+        "metric": LAYER_METRIC, "value": w.rows / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 projections (fp32 accumulate), f32 core", "data": "synthetic",
+        "config": dict(workload_config(w, args), workload=f"layer for {w.name}", op="layer", hidden=HIDDEN,
+                       dependent_launch_edges=head,
+                       weight_bytes=(w.pitch * HIDDEN + HIDDEN * w.dim) * 2, algorithmic_bytes_per_step=layer_b,
+                       projection_flops_per_step=flops,
+                       l2="L2 flushed between timed steps (256 MiB write, then 256 MiB read; outside the events)"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "layer graph (kda_linear, kda_step_kernel, kda_linear)",
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"},
+        "layer_ms": dict({f"graph_pdl_{head}": ms}, **{f"graph_pdl_{k}": v for k, v in others.items()},
+                         three_calls=sum(t_sep) / args.steps),
+        "e2e": {"value": w.rows / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": w.rows * HIDDEN * 2,
+                "d2h_bytes_per_step": w.rows * HIDDEN * 2, "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(t_host0, t_host1),
+    }
+    if not args.no_cpu_baseline:
+        cb = cpu_baseline(si, budget_s=8.0, state_dtype=args.state_dtype)
+        t0 = time.perf_counter()
+        OL.linear(xb, wib)
+        OL.linear(xb[:, :w.dim], wob)  # o_proj's shape: rows x D . (hidden x D)^T
+        t_proj = time.perf_counter() - t0
+        per_tok = 1.0 / cb["value"] + t_proj / w.rows
+        line["cpu_baseline"] = {"value": 1.0 / per_tok, "unit": "tokens/s", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": cb["sample"] + f"; plus both projections of all {w.rows} rows in fp64 "
+                                                         f"NumPy ({t_proj:.2f} s, BLAS threads)"}
+    print(json.dumps(line), flush=True)
+
+
 # -------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -443,9 +578,12 @@ def main():
                     help="launch every step through a launch plan (the step recorded once as a CUDA graph)")
     ap.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32",
                     help="state pool storage type (kda_set_state_dtype); the step computes in fp32 either way")
-    ap.add_argument("--op", choices=["step", "in_proj", "o_proj"], default="step",
+    ap.add_argument("--op", choices=["step", "in_proj", "o_proj", "layer"], default="step",
                     help="step: the KDA core (default); in_proj / o_proj: the layer's projections (kda_linear) "
-                         "for the workload's rows")
+                         "for the workload's rows; layer: in_proj -> core -> o_proj as one CUDA graph")
+    ap.add_argument("--layer-pdl", choices=["none", "step_edge", "o_proj_edge", "both"], default="step_edge",
+                    help="--op layer: the edges of the timed graph launched as programmatic dependents "
+                         "(the others are timed too and reported under layer_ms)")
     ap.add_argument("--gate-mode", choices=["sigmoid", "softplus"], default="sigmoid",
                     help="decay gate form (kda_set_gate_mode); the default is the reading the step follows")
     args = ap.parse_args()
@@ -454,6 +592,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    if args.op == "layer":
+        run_layer(args, w)
         return
     if args.op != "step":
         run_linear(args, w)

@@ -184,6 +184,31 @@ int kda_plan_create(kda_handle* handle, const void* projected, long long rows, l
                     void* conv_state, int conv_dim_first, float* state_pool, long long pool_slots,
                     const int* slots, int L, const int* accepted, void* out, kda_plan** plan);
 int kda_plan_launch(kda_plan* plan, void* cuda_stream);
+
+/*
+ * kda_layer_plan_create -- one decode / verify step of the whole layer as a
+ * CUDA graph: in_proj (kda_linear: x [rows, hidden] (row stride ldx) .
+ * w_in [pitch, hidden]^T -> projected [rows, pitch]), kda_step (projected ->
+ * core_out [rows, D], the caches updated as by kda_step), o_proj (kda_linear:
+ * core_out . w_o [hidden, D]^T -> y [rows, hidden], row stride ldy).  The K1
+ * page's gemv stage in front of kda_pre and the K2a page's o_proj after it,
+ * without the all-reduce.  projected and core_out are the caller's
+ * intermediate buffers (contiguous); every pointer is the caller's, must stay
+ * valid while the plan exists, and is read or written at each launch; the
+ * handle's gate mode and state dtype at creation are baked in.  pdl is a
+ * mask of the edges launched as programmatic dependents (the kernel may start
+ * while the previous one finishes; it loads what does not depend on its
+ * predecessor, then waits for it before reading its output):
+ * KDA_PDL_STEP (in_proj -> kda_step), KDA_PDL_O_PROJ (kda_step -> o_proj);
+ * 0 = plain stream order.  Validation and error codes as kda_step and
+ * kda_linear; launch with kda_plan_launch, free with kda_plan_destroy.
+ */
+#define KDA_PDL_STEP 1
+#define KDA_PDL_O_PROJ 2
+int kda_layer_plan_create(kda_handle* handle, const void* x, long long rows, long long ldx, long long hidden,
+                          const void* w_in, void* projected, long long pitch, void* conv_state, int conv_dim_first,
+                          float* state_pool, long long pool_slots, const int* slots, int L, const int* accepted,
+                          void* core_out, const void* w_o, void* y, long long ldy, int pdl, kda_plan** plan);
 void kda_plan_destroy(kda_plan* plan);
 
 /*

@@ -27,8 +27,8 @@ from ._build import DEBUG_LIB_PATH, LIB_PATH, build
 
 __all__ = [
     "KdaError", "build", "load_library", "kda_prepare", "kda_step", "kda_check", "kda_destroy",
-    "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "kda_plan_create", "kda_plan_launch",
-    "kda_plan_destroy", "kda_set_state_dtype", "kda_linear", "kda_linear_check", "linear", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
+    "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "kda_plan_create", "kda_layer_plan_create", "kda_plan_launch",
+    "kda_plan_destroy", "kda_set_state_dtype", "kda_linear", "kda_linear_check", "linear", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_PDL_STEP", "KDA_PDL_O_PROJ", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
     "KDA_ERR_TIMEOUT", "KDA_ERR_DUPLICATE", "KDA_MAX_TOKENS", "DEBUG_LIB_PATH", "KDA_GATE_SIGMOID", "KDA_GATE_SOFTPLUS", "HEAD_DIM",
 ]
 
@@ -38,6 +38,7 @@ KDA_ERR_SLOT, KDA_ERR_ACCEPTED, KDA_ERR_TIMEOUT, KDA_ERR_DUPLICATE = 1, 2, 4, 8
 KDA_MAX_TOKENS = 8
 KDA_GATE_SIGMOID, KDA_GATE_SOFTPLUS = 0, 1
 KDA_STATE_F32, KDA_STATE_BF16 = 0, 1
+KDA_PDL_STEP, KDA_PDL_O_PROJ = 1, 2
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -73,6 +74,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_set_gate_mode.restype = i32
     lib.kda_plan_create.argtypes = [vp, vp, ll, ll, vp, i32, vp, ll, vp, i32, vp, vp, ctypes.POINTER(vp)]
     lib.kda_plan_create.restype = i32
+    lib.kda_layer_plan_create.argtypes = [vp, vp, ll, ll, ll, vp, vp, ll, vp, i32, vp, ll, vp, i32, vp, vp, vp, vp,
+                                          ll, i32, ctypes.POINTER(vp)]
+    lib.kda_layer_plan_create.restype = i32
     lib.kda_plan_launch.argtypes = [vp, vp]
     lib.kda_plan_launch.restype = i32
     lib.kda_plan_destroy.argtypes = [vp]
@@ -119,6 +123,21 @@ def kda_plan_create(handle: int, projected: int, rows: int, pitch: int, conv_sta
                                         state_pool, pool_slots, slots, L, accepted or None, out, ctypes.byref(p))
     if rc != KDA_OK:
         raise KdaError("kda_plan_create", rc)
+    return p.value
+
+
+def kda_layer_plan_create(handle: int, x: int, rows: int, ldx: int, hidden: int, w_in: int, projected: int,
+                          pitch: int, conv_state: int, conv_dim_first: bool, state_pool: int, pool_slots: int,
+                          slots: int, L: int, accepted: Optional[int], core_out: int, w_o: int, y: int, ldy: int,
+                          pdl: int = 0) -> int:
+    """Record in_proj -> kda_step -> o_proj on these buffers as one CUDA graph (see include/kda.h)."""
+    p = ctypes.c_void_p()
+    rc = load_library().kda_layer_plan_create(handle, x, rows, ldx, hidden, w_in, projected, pitch, conv_state,
+                                              1 if conv_dim_first else 0, state_pool, pool_slots, slots, L,
+                                              accepted or None, core_out, w_o, y, ldy, int(pdl),
+                                              ctypes.byref(p))
+    if rc != KDA_OK:
+        raise KdaError("kda_layer_plan_create", rc)
     return p.value
 
 
@@ -312,6 +331,37 @@ class PreparedKda:
         with torch.cuda.device(self.device):
             p = kda_plan_create(self.handle, *args)
         return KdaPlan(p, keep + (self,), self.device)
+
+    def layer_plan(self, x, w_in, projected, core_out, w_o, y, *, caches, slots, accepted=None,
+                   pdl=0) -> "KdaPlan":
+        """Record one step of the layer on these buffers as a CUDA graph:
+        ``projected = x @ w_in.T`` (in_proj), the core step ``projected ->
+        core_out`` (arguments as ``run``), ``y = core_out @ w_o.T`` (o_proj).
+        x [rows, hidden] bf16 (unit column stride), w_in [pitch, hidden] and
+        w_o [hidden, D] contiguous bf16, projected [rows, pitch], core_out
+        [rows, D] and y [rows, hidden] bf16.  ``pdl``: a mask of the edges
+        launched as programmatic dependents (KDA_PDL_STEP | KDA_PDL_O_PROJ;
+        True = both, 0 = plain stream order)."""
+        import torch
+
+        args, keep = self._args(projected, core_out, caches, slots, accepted)
+        for t, name in ((x, "x"), (w_in, "w_in"), (w_o, "w_o"), (y, "y")):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or t.stride(1) != 1:
+                raise TypeError(f"{name} must be a CUDA bf16 tensor with unit column stride")
+        if not (w_in.is_contiguous() and w_o.is_contiguous() and projected.is_contiguous() and core_out.is_contiguous()):
+            raise ValueError("w_in, w_o, projected and core_out must be contiguous")
+        rows, hidden = x.shape
+        pitch = projected.shape[1]
+        if (tuple(w_in.shape) != (pitch, hidden) or tuple(w_o.shape) != (hidden, core_out.shape[1])
+                or projected.shape[0] != rows or tuple(y.shape) != (rows, hidden)):
+            raise ValueError("layer_plan: inconsistent shapes")
+        (_, batch, _, conv, dim_first, state, pool, slot_ptr, L, acc, out) = args
+        with torch.cuda.device(self.device):
+            mask = (KDA_PDL_STEP | KDA_PDL_O_PROJ) if pdl is True else int(pdl)
+            p = kda_layer_plan_create(self.handle, x.data_ptr(), rows, x.stride(0), hidden, w_in.data_ptr(),
+                                      projected.data_ptr(), pitch, conv, dim_first, state, pool, slot_ptr, L, acc,
+                                      out, w_o.data_ptr(), y.data_ptr(), y.stride(0), mask)
+        return KdaPlan(p, keep + (x, w_in, w_o, y, self), self.device)
 
     def check(self, stream=None) -> int:
         """Synchronise the stream; return and clear the device error bits (plan launches included)."""

@@ -40,6 +40,7 @@
 #include <stdint.h>
 
 #include "kda.h"
+#include "internal.h"
 
 namespace {
 
@@ -238,6 +239,9 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
   }
   __syncthreads();
 
+  // As a programmatic dependent (a layer plan's o_proj) the set-up above
+  // overlaps the previous kernel's tail; x is its output. Otherwise a no-op.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   bool dead = false;  // a copy wait gave up: no more copies, outputs not meaningful
   long long g0 = 0;   // ring stages used by earlier passes (slot and phase bookkeeping)
   for (long long m0 = 0; m0 < a.M; m0 += MB, g0 += stages) {
@@ -306,6 +310,7 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
       }
     }
     __syncthreads();  // every warp is done with the ring: the partials overlay it
+    if (m0 + MB >= a.M) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // partial element e = ((j * 4 + c) * THREADS + thread): fragment c of the thread's n-tile j
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -416,6 +421,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot_p;
+  // As a programmatic dependent (a layer plan's o_proj) the set-up above
+  // overlaps the previous kernel's tail; x is its output. Otherwise a no-op.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Warps 0 and 1 run their loops whole (converged, spinning on the barrier
   // without the sleep hint: a suspended thread wakes late), lane 0 issuing.
@@ -484,6 +492,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
     }
     __syncwarp();
   }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // everyone: wait for the accumulator (no MMA at all when this CTA has no stages)
   bool have = stages > 0;
   if (have && !mbar_wait_bounded(accum_bar, 0)) ok_all = false;
@@ -633,7 +642,7 @@ bool encode_map(CUtensorMap* map, const void* base, long long rows, long long co
 // resident CTA slots), rounded up; the smallest C that minimises that.
 constexpr double LIN_FIXED_STAGES = 4.0;  // F for the mma.sync tiles, in stages (measured per-stage ~0.5 us)
 template <int MB, int NB>
-int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st) {
+int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl) {
   using T = LinShape<MB, NB>;
   const long long tiles = (a.N + NB - 1) / NB;
   const int box_rows = (int)(a.M < MB ? a.M : MB);
@@ -652,10 +661,12 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
   cfg.blockDim = dim3(T::THREADS, 1, 1);
   cfg.dynamicSmemBytes = T::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the previous kernel ends
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const long long stages = (a.K + T::KS - 1) / T::KS;
@@ -684,11 +695,12 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
   if (tiles * split > 0x7fffffffLL) return KDA_EINVAL;
   cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
   attr[0].val.clusterDim.x = (unsigned)split;
+  cfg.numAttrs = pdl ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, kda_linear_kernel<MB, NB>, tmx, tmw, a) != cudaSuccess) return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
-int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st) {
+int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl) {
   const long long tiles_n = (a.N + TC_BN - 1) / TC_BN, tiles = ((a.M + TC_BM - 1) / TC_BM) * tiles_n;
   CUtensorMap tmx, tmw;
   if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, TC_BN)) return KDA_ECUDA;
@@ -702,10 +714,12 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
   cfg.blockDim = dim3(TC_THREADS, 1, 1);
   cfg.dynamicSmemBytes = TC_SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the previous kernel ends
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const long long stages = (a.K + TC_BK - 1) / TC_BK;
@@ -734,14 +748,15 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
   if (tiles * split > 0x7fffffffLL) return KDA_EINVAL;
   cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
   attr[0].val.clusterDim.x = (unsigned)split;
+  cfg.numAttrs = pdl ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel, tmx, tmw, a, (int)tiles_n) != cudaSuccess) return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
 }  // namespace
 
-extern "C" int kda_linear(const void* x, long long rows, long long ldx, const void* w, long long N, long long K,
-                          void* y, long long ldy, void* cuda_stream) {
+int kda_linear_enqueue(const void* x, long long rows, long long ldx, const void* w, long long N, long long K,
+                       void* y, long long ldy, void* cuda_stream, bool pdl) {
   if (rows < 0 || N < 1 || K < LIN_KMULT || K % LIN_KMULT != 0) return KDA_EINVAL;
   if (rows == 0) return KDA_OK;
   if (!x || !w || !y || ldx < K || ldy < N) return KDA_EINVAL;
@@ -760,9 +775,14 @@ extern "C" int kda_linear(const void* x, long long rows, long long ldx, const vo
   a.x_box_bytes = 0;
   a.y_vec = lin_aligned(y, 16) && (ldy % 8) == 0;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
-  if (rows <= 16) return lin_launch<16, 32>(x, ldx, w, a, st);
-  if (rows <= 64) return lin_launch<64, 128>(x, ldx, w, a, st);
-  return lin_launch_tc(x, ldx, w, a, st);
+  if (rows <= 16) return lin_launch<16, 32>(x, ldx, w, a, st, pdl);
+  if (rows <= 64) return lin_launch<64, 128>(x, ldx, w, a, st, pdl);
+  return lin_launch_tc(x, ldx, w, a, st, pdl);
+}
+
+extern "C" int kda_linear(const void* x, long long rows, long long ldx, const void* w, long long N, long long K,
+                          void* y, long long ldy, void* cuda_stream) {
+  return kda_linear_enqueue(x, rows, ldx, w, N, K, y, ldy, cuda_stream, false);
 }
 
 extern "C" int kda_linear_check(void* cuda_stream, unsigned* device_flags) {

@@ -42,6 +42,7 @@
 #include <stdint.h>
 
 #include "kda.h"
+#include "internal.h"
 
 namespace {
 
@@ -526,6 +527,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   const float fbn = a.fb_norm[h * HD + zc];  // |f_b row|_2, rounded up
   const float dtc = a.dt_bias[h * HD + zc];
   const float a_log = a.A_log[h];
+  // Launched as a programmatic dependent of the projection that writes
+  // `projected` (a layer plan), the loads above -- weights, slots -- overlap
+  // that kernel's tail; from here on its output is read. Without such a
+  // dependency this returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // f_a and out-gate of the L tokens, raw bf16
   constexpr int PER_THREAD = (L * HD + THREADS - 1) / THREADS;
   unsigned short fa_v[PER_THREAD], gate_v[PER_THREAD];
@@ -916,6 +922,8 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       }
     }
   }
+  // a dependent launch (the o_proj of a layer plan) may start its CTAs now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the RMSNorm weights of this lane, in flight across the barrier
   const float4 onw = (warp < L) ? *reinterpret_cast<const float4*>(a.o_norm + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
   if (timed_out && lane == 0) {
@@ -1017,12 +1025,20 @@ cudaError_t set_all_smem_attrs() {
 }
 
 template <int L>
-cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream, bool bf16_state) {
-  if (bf16_state)
-    kda_step_kernel<L, true><<<(unsigned)ctas, THREADS, Smem<L, true>::bytes, stream>>>(a);
-  else
-    kda_step_kernel<L, false><<<(unsigned)ctas, THREADS, Smem<L, false>::bytes, stream>>>(a);
-  return cudaGetLastError();
+cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream, bool bf16_state, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = bf16_state ? Smem<L, true>::bytes : Smem<L, false>::bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the previous kernel ends
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true>, a)
+                                   : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false>, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int L>
@@ -1131,9 +1147,10 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
   return KDA_OK;
 }
 
-int kda_step(kda_handle* h, const void* projected, long long rows, long long pitch, void* conv_state,
-             int conv_dim_first, float* state_pool, long long pool_slots, const int* slots, int L,
-             const int* accepted, void* out, void* cuda_stream) {
+namespace {
+int step_enqueue(kda_handle* h, const void* projected, long long rows, long long pitch, void* conv_state,
+                 int conv_dim_first, float* state_pool, long long pool_slots, const int* slots, int L,
+                 const int* accepted, void* out, void* cuda_stream, bool pdl) {
   if (h == nullptr) return KDA_EINVAL;
   if (L < 1 || L > KDA_MAX_TOKENS || rows < 0 || rows % L != 0 || pool_slots < 0) return KDA_EINVAL;
   const long long D = (long long)HD * h->heads;
@@ -1182,16 +1199,24 @@ int kda_step(kda_handle* h, const void* projected, long long rows, long long pit
 #endif
   cudaError_t e;
   switch (L) {
-    case 1: e = launch<1>(a, ctas, s, bs); break;
-    case 2: e = launch<2>(a, ctas, s, bs); break;
-    case 3: e = launch<3>(a, ctas, s, bs); break;
-    case 4: e = launch<4>(a, ctas, s, bs); break;
-    case 5: e = launch<5>(a, ctas, s, bs); break;
-    case 6: e = launch<6>(a, ctas, s, bs); break;
-    case 7: e = launch<7>(a, ctas, s, bs); break;
-    default: e = launch<8>(a, ctas, s, bs); break;
+    case 1: e = launch<1>(a, ctas, s, bs, pdl); break;
+    case 2: e = launch<2>(a, ctas, s, bs, pdl); break;
+    case 3: e = launch<3>(a, ctas, s, bs, pdl); break;
+    case 4: e = launch<4>(a, ctas, s, bs, pdl); break;
+    case 5: e = launch<5>(a, ctas, s, bs, pdl); break;
+    case 6: e = launch<6>(a, ctas, s, bs, pdl); break;
+    case 7: e = launch<7>(a, ctas, s, bs, pdl); break;
+    default: e = launch<8>(a, ctas, s, bs, pdl); break;
   }
   return e == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+}  // namespace
+
+int kda_step(kda_handle* h, const void* projected, long long rows, long long pitch, void* conv_state,
+             int conv_dim_first, float* state_pool, long long pool_slots, const int* slots, int L,
+             const int* accepted, void* out, void* cuda_stream) {
+  return step_enqueue(h, projected, rows, pitch, conv_state, conv_dim_first, state_pool, pool_slots, slots, L,
+                      accepted, out, cuda_stream, false);
 }
 
 struct kda_plan {
@@ -1226,6 +1251,42 @@ int kda_plan_create(kda_handle* h, const void* projected, long long rows, long l
     return KDA_ECUDA;
   }
   *plan = new kda_plan{g, x};
+  return KDA_OK;
+}
+
+int kda_layer_plan_create(kda_handle* h, const void* x, long long rows, long long ldx, long long hidden,
+                          const void* w_in, void* projected, long long pitch, void* conv_state, int conv_dim_first,
+                          float* state_pool, long long pool_slots, const int* slots, int L, const int* accepted,
+                          void* core_out, const void* w_o, void* y, long long ldy, int pdl, kda_plan** plan) {
+  if (plan == nullptr) return KDA_EINVAL;
+  *plan = nullptr;
+  if (h == nullptr || rows < 1) return KDA_EINVAL;
+  const long long D = (long long)HD * h->heads;
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return KDA_ECUDA;
+  cudaError_t e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+  int rc = KDA_ECUDA;
+  cudaGraph_t g = nullptr;
+  if (e == cudaSuccess) {
+    // in_proj -> projected [rows, pitch]; the core -> core_out [rows, D]; o_proj -> y [rows, hidden]
+    rc = kda_linear_enqueue(x, rows, ldx, w_in, pitch, hidden, projected, pitch, s, false);
+    if (rc == KDA_OK)
+      rc = step_enqueue(h, projected, rows, pitch, conv_state, conv_dim_first, state_pool, pool_slots, slots, L,
+                        accepted, core_out, s, (pdl & KDA_PDL_STEP) != 0);
+    if (rc == KDA_OK) rc = kda_linear_enqueue(core_out, rows, D, w_o, hidden, D, y, ldy, s, (pdl & KDA_PDL_O_PROJ) != 0);
+    e = cudaStreamEndCapture(s, &g);  // always ends the capture, whatever the enqueues returned
+  }
+  cudaStreamDestroy(s);
+  if (rc != KDA_OK || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return rc != KDA_OK ? rc : KDA_ECUDA;
+  }
+  cudaGraphExec_t xg = nullptr;
+  if (cudaGraphInstantiate(&xg, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return KDA_ECUDA;
+  }
+  *plan = new kda_plan{g, xg};
   return KDA_OK;
 }
 

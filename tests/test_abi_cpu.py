@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["kda_prepare", "kda_step", "kda_check", "kda_destroy", "kda_strerror",
                             "kda_launch_info", "kda_set_gate_mode", "kda_set_state_dtype", "kda_plan_create",
-                            "kda_plan_launch", "kda_plan_destroy", "kda_linear", "kda_linear_check"])
+                            "kda_plan_launch", "kda_plan_destroy", "kda_linear", "kda_linear_check",
+                            "kda_layer_plan_create"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -62,6 +63,9 @@ def test_host_validation_without_gpu(lib):
     assert lib.kda_linear(None, 4, 64, None, 8, 64, None, 8, None) == -1    # null pointers
     assert lib.kda_linear(None, 0, 64, None, 8, 64, None, 8, None) == 0     # rows = 0: nothing
     assert lib.kda_linear_check(None, None) == -1                            # null flags pointer
+    # (argument types as set by the binding)
+    assert lib.kda_layer_plan_create(None, None, 1, 7168, 7168, None, None, 1154, None, 1, None, 4, None, 1,
+                                     None, None, None, None, 7168, 1, None) == -1  # no plan out-pointer / handle
     p = ctypes.c_void_p()
     assert lib.kda_plan_create(None, None, 16, 1154, None, 1, None, 16, None, 1, None, None, ctypes.byref(p)) == -1
     assert lib.kda_plan_create(None, None, 16, 1154, None, 1, None, 16, None, 1, None, None, None) == -1
