@@ -16,14 +16,11 @@
 // weight rows (and the matching x rows) through a shared-memory ring fed by
 // TMA tensor copies (cp.async.bulk.tensor, 64 x rows boxes, 128-byte swizzle,
 // completing on an mbarrier per slot), while its warps load fragments with
-// ldmatrix and multiply with m16n8k16 bf16 tensor instructions.  Two shapes:
-//   rows <= 16: one 16-row tile, 32 columns, 4 warps (one 8-column n-tile
-//     each), K in stages of 128, six stages of 12 KB: the bytes are weight;
-//   rows > 16: 64-row passes, 128 columns, 8 warps (16 rows x 64 columns
-//     each), K in stages of 64, four stages of 24 KB: x is re-read from L2 by
-//     every column tile, so wide tiles keep the copy engine's bytes mostly
-//     weight (x : W = 1 : 2; with 32-column tiles it was 2 : 1 and the kernel
-//     ran at a third of the HBM rate).
+// ldmatrix and multiply with m16n8k16 bf16 tensor instructions, for up to 16
+// rows: one 16-row tile, 32 columns, 4 warps (one 8-column n-tile each), K in
+// stages of 128, six stages of 12 KB: the bytes are weight.  (The template
+// also takes 64-row passes over 128-column tiles with 8 warps; more rows go
+// to the tcgen05 kernel below, which measured faster from 64 rows on.)
 // Rows past `rows`, weight rows past N and k past K are outside the tensor
 // maps: the copy engine fills them with zeros.
 //
@@ -191,6 +188,7 @@ struct LinArgs {
   long long M, N, K;
   unsigned x_box_bytes;  // bytes of one x box: its rows (min(rows, MB)) x 128
   int y_vec;             // y and ldy allow 16-byte stores (y 16-byte aligned, ldy % 8 == 0)
+  int y_vec8;            // y and ldy allow 8-byte stores (y 8-byte aligned, ldy % 4 == 0)
 };
 
 // Issued by one thread: the x and weight boxes of stage k0 .. k0 + KS into
@@ -342,7 +340,7 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// rows > 64: tcgen05 (5th-generation tensor core) tiles.  A CTA owns a
+// rows > 16: tcgen05 (5th-generation tensor core) tiles.  A CTA owns a
 // 128 x 256 output tile (rows past `rows` are the copy engine's zeros), K in
 // stages of 64 through a four-deep ring (x box 16 KB + weight box 32 KB, both
 // 128-byte swizzled: the canonical K-major layout of the MMA's shared-memory
@@ -359,10 +357,15 @@ constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4, TC_THREADS = 
 constexpr int TC_ABYTES = TC_BM * 128, TC_BBYTES = TC_BN * 128;  // one 64-k box each
 constexpr int TC_STAGE = TC_ABYTES + TC_BBYTES;
 constexpr int TC_RING = TC_STAGES * TC_STAGE;
-constexpr int TC_RED_LD = TC_BM + 4;  // partial tile, column-major: element (r, c) at c * 132 + r (16-byte rows)
+constexpr int TC_RED_LD = TC_BN + 4;  // partial tile, row-major: element (r, c) at r * 260 + c (16-byte stores, no bank conflicts)
 constexpr int TC_SMEM = 1024 + TC_RING + 8 * (2 * TC_STAGES + 1) + 16;
-constexpr double TC_FIXED_STAGES = 16.0;  // F of the split model below for these tiles (a stage ~0.3 us)
-static_assert(TC_BN * TC_RED_LD * 4 <= TC_RING, "partials overlay the ring");
+// split model for these tiles, in stages (~0.4 us each under load): a CTA's fixed
+// part (launch ramp, first copies, epilogue) and the extra of a K split (partials
+// through shared memory and the cluster reduction), fitted to splits 1..8 of
+// the 64-, 128- and 512-row in_proj and o_proj shapes
+constexpr double TC_FIXED_STAGES = 16.0;
+constexpr double TC_REDUCE_STAGES = 10.0;
+static_assert(TC_BM * TC_RED_LD * 4 <= TC_RING, "partials overlay the ring");
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1),
 // bf16 A and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
@@ -554,7 +557,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
     }
     return;
   }
-  // K split: accumulator -> shared memory (column-major, padded), 32 columns a load
+  // K split: accumulator -> shared memory (row-major, padded), 32 columns a load; rows past `rows` are not needed
 #pragma unroll 1
   for (int c0 = 0; c0 < TC_BN; c0 += 32) {
     uint32_t v[32];
@@ -572,8 +575,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0u;
     }
+    if (r < rows_here) {
+      float4* dst = reinterpret_cast<float4*>(red + r * TC_RED_LD + c0);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) red[(c0 + j) * TC_RED_LD + r] = __uint_as_float(v[j]);
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                             __uint_as_float(v[4 * q + 3]));
+    }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   cluster_sync();
@@ -581,19 +589,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
   }
-  // this CTA's share of the tile: (4-row group, column) pairs in row-group-major order, each
-  // summed over the cluster's partials with 16-byte loads
-  const int E = ((rows_here + 3) / 4) * TC_BN;
+  // this CTA's share of the tile: (row, 4-column group) pairs in row-major order, each summed
+  // over the cluster's partials with 16-byte loads and stored as 4 bf16
+  constexpr int CQ = TC_BN / 4;
+  const int E = rows_here * CQ;
   const int e_end = (int)((long long)E * (rank + 1) / split);
   for (int e = (int)((long long)E * rank / split) + threadIdx.x; e < e_end; e += TC_THREADS) {
-    const int rq = e / TC_BN, cc = e % TC_BN;
-    const float4 v4 = cluster_sum4(red + cc * TC_RED_LD + 4 * rq, split);
-    const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-    const long long n = n0 + cc;
-    if (n < a.N) {
+    const int rr = e / CQ, cq = e % CQ;
+    const float4 v4 = cluster_sum4(red + rr * TC_RED_LD + 4 * cq, split);
+    const long long n = n0 + 4 * cq;
+    __nv_bfloat16* yr = a.y + (m0 + rr) * a.ldy;
+    if (a.y_vec8 && n + 4 <= a.N) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(v4.x, v4.y), hi = __floats2bfloat162_rn(v4.z, v4.w);
+      *reinterpret_cast<uint2*>(yr + n) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    } else {
+      const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        if (4 * rq + i < rows_here) a.y[(m0 + 4 * rq + i) * a.ldy + n] = __float2bfloat16_rn(vv[i]);
+        if (n + i < a.N) yr[n + i] = __float2bfloat16_rn(vv[i]);
     }
   }
   // the peers have read this CTA's partials before it exits
@@ -742,7 +756,12 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
       if (held <= 0) continue;
       if (dev < 64) cluster_cache[dev][c] = held;
     }
-    const double cost = (double)((tiles + held - 1) / held) * ((double)stages / c + TC_FIXED_STAGES);
+    // waves of clusters: a last wave at least a quarter full counts by its share (its
+    // CTAs run with the copy engines and L2 less loaded), a smaller one as a whole wave
+    const double w = (double)tiles / held;
+    const double whole = (double)((tiles + held - 1) / held), tail = w - (whole - 1.0);
+    const double waves = w <= 1.0 ? 1.0 : (tail >= 0.25 ? w : whole);
+    const double cost = waves * ((double)stages / c) + TC_FIXED_STAGES + (c > 1 ? TC_REDUCE_STAGES : 0.0);
     if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
   }
   if (tiles * split > 0x7fffffffLL) return KDA_EINVAL;
@@ -763,9 +782,10 @@ int kda_linear_enqueue(const void* x, long long rows, long long ldx, const void*
   // tensor maps: 16-byte aligned bases and row strides; coordinates fit 32 bits
   if (!lin_aligned(x, 16) || !lin_aligned(w, 16) || (ldx % 8) != 0 || !lin_aligned(y, 2)) return KDA_EINVAL;
   if (K > 0x7fffffffLL || N > 0x7fffffffLL || rows > 0x7fffffffLL) return KDA_EINVAL;
-  // rows <= 16: the one-tile shape; <= 64: one 64-row pass over 128-column
-  // tiles (HBM-bound: mma.sync keeps up, and its x tile is not padded to the
-  // tcgen05 tile's 128 rows); beyond: tcgen05 tiles
+  // rows <= 16: the one-tile mma.sync shape (the bytes are the weight);
+  // beyond: tcgen05 tiles (at 64 rows they beat 64 x 128 mma.sync tiles,
+  // 30.8 against 35.8 us for the 12-head in_proj, although half their x box
+  // is the copy engine's zeros)
   LinArgs a;
   a.y = static_cast<__nv_bfloat16*>(y);
   a.ldy = ldy;
@@ -774,9 +794,9 @@ int kda_linear_enqueue(const void* x, long long rows, long long ldx, const void*
   a.K = K;
   a.x_box_bytes = 0;
   a.y_vec = lin_aligned(y, 16) && (ldy % 8) == 0;
+  a.y_vec8 = lin_aligned(y, 8) && (ldy % 4) == 0;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   if (rows <= 16) return lin_launch<16, 32>(x, ldx, w, a, st, pdl);
-  if (rows <= 64) return lin_launch<64, 128>(x, ldx, w, a, st, pdl);
   return lin_launch_tc(x, ldx, w, a, st, pdl);
 }
 

@@ -62,14 +62,14 @@ def test_in_proj_tensor_core_tiles():
     _check(160, 7168, 6284, seed=160)
 
 
-def test_several_passes_ragged_tail_and_strided_x():
-    _check(130, 256, 99, seed=7, xcols=320)   # 3 row passes, 4 column blocks, last one with 3 columns
+def test_several_row_tiles_ragged_tail_and_strided_x():
+    _check(130, 256, 99, seed=7, xcols=320)   # 2 row tiles (the second 2 rows), one 99-column tile
 
 
 @pytest.mark.parametrize("rows,K,N", [(16, 512, 77), (17, 384, 77), (5, 200, 45), (20, 328, 70), (1, 8, 33),
                                      (3, 7168, 1154), (2, 128, 5000)])
 def test_row_tile_boundaries_ragged_k_and_k_splits(rows, K, N):
-    # 16 rows: the one-tile shape; 17: 64-row passes; K = 200, 328, 8 end in a
+    # 16 rows: the mma.sync one-tile shape; 17: tcgen05 tiles; K = 200, 328, 8 end in a
     # partial k stage (zero-filled past K); 1154 columns (the 2-head in_proj)
     # split K eight ways; K = 128 is a single stage, so no split
     _check(rows, K, N, seed=rows * 1000 + N, xcols=K + 8)
