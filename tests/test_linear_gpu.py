@@ -67,11 +67,12 @@ def test_several_row_tiles_ragged_tail_and_strided_x():
 
 
 @pytest.mark.parametrize("rows,K,N", [(16, 512, 77), (17, 384, 77), (5, 200, 45), (20, 328, 70), (1, 8, 33),
-                                     (3, 7168, 1154), (2, 128, 5000)])
+                                     (3, 7168, 1154), (2, 128, 5000), (300, 256, 600), (257, 1536, 300)])
 def test_row_tile_boundaries_ragged_k_and_k_splits(rows, K, N):
     # 16 rows: the mma.sync one-tile shape; 17: tcgen05 tiles; K = 200, 328, 8 end in a
     # partial k stage (zero-filled past K); 1154 columns (the 2-head in_proj)
-    # split K eight ways; K = 128 is a single stage, so no split
+    # split K eight ways; K = 128 is a single stage, so no split; 300 and 257 rows: three
+    # tcgen05 row tiles, the last one mostly past the end
     _check(rows, K, N, seed=rows * 1000 + N, xcols=K + 8)
 
 
