@@ -119,6 +119,16 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, in
       "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(bar), "l"(policy)
       : "memory");
 }
+// As tma_box, written to the same offset (and completing on the same mbarrier
+// offset) in every CTA of the cluster whose bit is set in `mask`.
+__device__ __forceinline__ void tma_box_multicast(uint32_t dst, const CUtensorMap* map, int k, int row, uint32_t bar,
+                                                  uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(bar), "h"(mask)
+      : "memory");
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -155,13 +165,15 @@ __device__ __forceinline__ float4 ld_peer_f32x4(const float* local, unsigned ran
                : "r"(remote));
   return v;
 }
-// Sum of the `split` CTAs' four floats at `local`, in rank order; every load is
-// issued before the first add, so the distributed-shared-memory round trips overlap.
-__device__ __forceinline__ float4 cluster_sum4(const float* local, unsigned split) {
+// Sum of the `split` CTAs' four floats at `local` (CTA ranks q * stride + offset,
+// q < split), in rank order; every load is issued before the first add, so the
+// distributed-shared-memory round trips overlap.
+__device__ __forceinline__ float4 cluster_sum4(const float* local, unsigned split, unsigned stride = 1,
+                                               unsigned offset = 0) {
   float4 t[LIN_MAX_SPLIT];
 #pragma unroll
   for (int q = 0; q < LIN_MAX_SPLIT; ++q)
-    t[q] = (unsigned)q < split ? ld_peer_f32x4(local, q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    t[q] = (unsigned)q < split ? ld_peer_f32x4(local, q * stride + offset) : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 v = t[0];
 #pragma unroll
   for (int q = 1; q < LIN_MAX_SPLIT; ++q) {
@@ -350,9 +362,14 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
 // last stage the four warps read the accumulator (warp w: lanes = rows 32w ..
 // 32w + 31), stage it in shared memory (column-major, padded) and write bf16.
 // K split over a cluster as in the kernel above, the partial tiles summed
-// through distributed shared memory.  The copy engine's bytes per SM bound
-// these tiles as much as the tensor pipe does, so the tile is as wide as one
-// MMA allows (x : W bytes = 1 : 2).
+// through distributed shared memory.  The operand bytes out of L2 (about
+// 8 TB/s for TMA reads on this part, the same for 100 or 152 reading SMs)
+// bound these tiles as much as the tensor pipe does, so the tile is as wide as
+// one MMA allows (x : W bytes = 1 : 2) and, with two or more row tiles, CTAs
+// come in pairs (two row tiles, one column tile) inside the cluster: each
+// loads half the 256-row weight box and multicasts it to both, so the pair
+// reads the weight from L2 once.  A slot is refilled only when both CTAs' MMAs
+// are done with it: every MMA group commits to the empty barriers of both.
 constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4, TC_THREADS = 128;
 constexpr int TC_ABYTES = TC_BM * 128, TC_BBYTES = TC_BN * 128;  // one 64-k box each
 constexpr int TC_STAGE = TC_ABYTES + TC_BBYTES;
@@ -386,7 +403,7 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
 
 __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __grid_constant__ CUtensorMap tmx,
                                                                     const __grid_constant__ CUtensorMap tmw,
-                                                                    const LinArgs a, int tiles_n) {
+                                                                    const LinArgs a, int tiles_n, int pair) {
   extern __shared__ __align__(128) unsigned char tsmem[];
   const uint32_t raw = smem_addr(tsmem);
   const uint32_t ring = (raw + 1023u) & ~1023u;
@@ -397,9 +414,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   volatile uint32_t* tmem_slot_p = reinterpret_cast<volatile uint32_t*>(ring_p + (tmem_slot - ring));
   volatile int* consumed_p = reinterpret_cast<volatile int*>(ring_p + (tmem_slot - ring) + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const unsigned split = cluster_nctarank(), rank = cluster_ctarank();
-  const long long tile = cluster_id_x();
-  const long long m0 = (tile / tiles_n) * TC_BM, n0 = (tile % tiles_n) * TC_BN;
+  // cluster = pair x split CTAs: rank = kc * pair + p (p: row tile within the pair, kc: K part)
+  const unsigned csize = cluster_nctarank(), crank = cluster_ctarank();
+  const unsigned split = csize / (unsigned)pair, p = crank % (unsigned)pair, rank = crank / (unsigned)pair;
+  const long long grp = cluster_id_x();
+  const long long m0 = ((grp / tiles_n) * pair + p) * TC_BM, n0 = (grp % tiles_n) * TC_BN;
+  const uint16_t pair_mask = (uint16_t)(((1u << pair) - 1u) << (rank * (unsigned)pair));
+  const int wpart = TC_BN / pair;  // weight rows a CTA copies (and multicasts to its pair)
   const long long total = (a.K + TC_BK - 1) / TC_BK;
   const long long s_begin = total * rank / split;
   const long long stages = total * (rank + 1) / split - s_begin;
@@ -409,7 +430,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
     for (int i = 0; i < TC_STAGES; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, (unsigned)pair);  // both CTAs of a pair release a slot
     }
     mbar_init(accum_bar, 1);
     *consumed_p = 0;
@@ -422,6 +443,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  // a pair's barriers are initialised before either CTA copies into or signals the other
+  if (pair > 1) cluster_sync();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot_p;
   // As a programmatic dependent (a layer plan's o_proj) the set-up above
@@ -450,13 +473,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
       if (lane == 0) {
         const uint32_t st = ring + slot * TC_STAGE, bar = full0 + 8 * slot;
         const int k = (int)((s_begin + s) * TC_BK);
-        mbar_expect_tx(bar, TC_STAGE);
+        mbar_expect_tx(bar, TC_STAGE);  // x, this CTA's weight part and the partner's
         tma_box(st, &tmx, k, (int)m0, bar, x_policy);
-        tma_box(st + TC_ABYTES, &tmw, k, (int)n0, bar, w_policy);
+        if (pair > 1)
+          tma_box_multicast(st + TC_ABYTES + p * wpart * 128, &tmw, k, (int)(n0 + p * wpart), bar, pair_mask);
+        else
+          tma_box(st + TC_ABYTES, &tmw, k, (int)n0, bar, w_policy);
       }
       __syncwarp();
       issued = s + 1;
     }
+    // a pair: the last releases of this CTA's slots (its own MMAs' and the partner's) have
+    // arrived before it goes on, so nothing signals its barriers after it exits
+    if (pair > 1 && ok_all)
+      for (long long q = issued > TC_STAGES ? issued - TC_STAGES : 0; q < issued; ++q)
+        if (!mbar_wait_bounded(empty0 + 8 * (uint32_t)(q % TC_STAGES), (unsigned)((q / TC_STAGES) & 1)))
+          ok_all = false;
   } else if (warp == 1) {  // MMA issuer
     long long s = 0;
     for (; s < stages; ++s) {
@@ -480,10 +512,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
               "l"(da), "l"(db), "r"(TC_IDESC), "r"(acc)
               : "memory");
         }
-        // the slot is free once these MMAs have read it
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 +
-                                                                                                       8 * slot)
-                     : "memory");
+        // the slot is free (in this CTA and, for a pair, in the partner) once these MMAs have read it
+        if (pair > 1)
+          asm volatile(
+              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                  empty0 + 8 * slot),
+              "h"(pair_mask)
+              : "memory");
+        else
+          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 +
+                                                                                                         8 * slot)
+                       : "memory");
       }
       __syncwarp();
     }
@@ -555,6 +594,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
     }
+    if (pair > 1) cluster_sync();  // the partner is done with this CTA's barriers
     return;
   }
   // K split: accumulator -> shared memory (row-major, padded), 32 columns a load; rows past `rows` are not needed
@@ -596,7 +636,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   const int e_end = (int)((long long)E * (rank + 1) / split);
   for (int e = (int)((long long)E * rank / split) + threadIdx.x; e < e_end; e += TC_THREADS) {
     const int rr = e / CQ, cq = e % CQ;
-    const float4 v4 = cluster_sum4(red + rr * TC_RED_LD + 4 * cq, split);
+    const float4 v4 = cluster_sum4(red + rr * TC_RED_LD + 4 * cq, split, (unsigned)pair, p);
     const long long n = n0 + 4 * cq;
     __nv_bfloat16* yr = a.y + (m0 + rr) * a.ldy;
     if (a.y_vec8 && n + 4 <= a.N) {
@@ -715,13 +755,17 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
 }
 
 int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl) {
-  const long long tiles_n = (a.N + TC_BN - 1) / TC_BN, tiles = ((a.M + TC_BM - 1) / TC_BM) * tiles_n;
+  const long long tiles_m = (a.M + TC_BM - 1) / TC_BM, tiles_n = (a.N + TC_BN - 1) / TC_BN;
+  // two or more row tiles: CTAs in pairs that share (multicast) the weight box
+  const int pair = tiles_m >= 2 ? 2 : 1;
+  const long long groups = ((tiles_m + pair - 1) / pair) * tiles_n;  // clusters of one K part
   CUtensorMap tmx, tmw;
-  if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, TC_BN)) return KDA_ECUDA;
+  if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, TC_BN / pair))
+    return KDA_ECUDA;
   if (cudaFuncSetAttribute(kda_linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM) !=
       cudaSuccess)
     return KDA_ECUDA;
-  static int cluster_cache[64][LIN_MAX_SPLIT + 1];
+  static int cluster_cache[64][LIN_MAX_SPLIT + 1];  // by cluster size
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ECUDA;
   cudaLaunchConfig_t cfg = {};
@@ -744,31 +788,33 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_tc_kernel, TC_THREADS, TC_SMEM) !=
           cudaSuccess)
     return KDA_ECUDA;
-  for (int c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
-    int held = dev < 64 ? cluster_cache[dev][c] : 0;
+  for (int c = 1; c * pair <= LIN_MAX_SPLIT && c <= stages; ++c) {
+    const int cs = c * pair;  // cluster size
+    int held = dev < 64 ? cluster_cache[dev][cs] : 0;
     if (held <= 0) {
-      attr[0].val.clusterDim.x = (unsigned)c;
-      cfg.gridDim = dim3((unsigned)c, 1, 1);
+      attr[0].val.clusterDim.x = (unsigned)cs;
+      cfg.gridDim = dim3((unsigned)cs, 1, 1);
       if (cudaOccupancyMaxActiveClusters(&held, kda_linear_tc_kernel, &cfg) != cudaSuccess) return KDA_ECUDA;
       // never more clusters than the resident CTA slots hold
-      const int cap = sms * (per_sm > 0 ? per_sm : 1) / c;
+      const int cap = sms * (per_sm > 0 ? per_sm : 1) / cs;
       if (held > cap) held = cap;
       if (held <= 0) continue;
-      if (dev < 64) cluster_cache[dev][c] = held;
+      if (dev < 64) cluster_cache[dev][cs] = held;
     }
     // waves of clusters: a last wave at least a quarter full counts by its share (its
     // CTAs run with the copy engines and L2 less loaded), a smaller one as a whole wave
-    const double w = (double)tiles / held;
-    const double whole = (double)((tiles + held - 1) / held), tail = w - (whole - 1.0);
+    const double w = (double)groups / held;
+    const double whole = (double)((groups + held - 1) / held), tail = w - (whole - 1.0);
     const double waves = w <= 1.0 ? 1.0 : (tail >= 0.25 ? w : whole);
     const double cost = waves * ((double)stages / c) + TC_FIXED_STAGES + (c > 1 ? TC_REDUCE_STAGES : 0.0);
     if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
   }
-  if (tiles * split > 0x7fffffffLL) return KDA_EINVAL;
-  cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
-  attr[0].val.clusterDim.x = (unsigned)split;
+  if (groups * pair * split > 0x7fffffffLL) return KDA_EINVAL;
+  cfg.gridDim = dim3((unsigned)(groups * pair * split), 1, 1);
+  attr[0].val.clusterDim.x = (unsigned)(pair * split);
   cfg.numAttrs = pdl ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel, tmx, tmw, a, (int)tiles_n) != cudaSuccess) return KDA_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel, tmx, tmw, a, (int)tiles_n, pair) != cudaSuccess)
+    return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
