@@ -36,6 +36,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kda.h"
 #include "internal.h"
 
@@ -662,14 +664,17 @@ using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, 
 
 // cuTensorMapEncodeTiled from the driver, looked up once (no link to libcuda).
 EncodeTiled encode_fn() {
-  static EncodeTiled fn = nullptr;
+  static std::atomic<EncodeTiled> cached{nullptr};
+  EncodeTiled fn = cached.load(std::memory_order_acquire);
   if (!fn) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<EncodeTiled>(p);
+      cached.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }
@@ -708,7 +713,9 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
       cudaSuccess)
     return KDA_ECUDA;
   // clusters of each size the device holds at once, looked up once per device and shape
-  static int cluster_cache[64][LIN_MAX_SPLIT + 1];
+  // looked up once per device (relaxed atomics: callers on several host threads
+  // at worst repeat the same lookup)
+  static std::atomic<int> cluster_cache[64][LIN_MAX_SPLIT + 1];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ECUDA;
   cudaLaunchConfig_t cfg = {};
@@ -727,7 +734,7 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
   long long split = 1;
   double best = 1e300;
   for (int c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
-    int held = dev < 64 ? cluster_cache[dev][c] : 0;
+    int held = dev < 64 ? cluster_cache[dev][c].load(std::memory_order_relaxed) : 0;
     if (held <= 0) {
       attr[0].val.clusterDim.x = (unsigned)c;
       cfg.gridDim = dim3((unsigned)c, 1, 1);
@@ -741,7 +748,7 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
       const int cap = sms * (per_sm > 0 ? per_sm : 1) / c;
       if (held > cap) held = cap;
       if (held <= 0) continue;
-      if (dev < 64) cluster_cache[dev][c] = held;
+      if (dev < 64) cluster_cache[dev][c].store(held, std::memory_order_relaxed);
     }
     const double cost = (double)((tiles + held - 1) / held) * ((double)stages / c + LIN_FIXED_STAGES);
     if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
@@ -765,7 +772,7 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
   if (cudaFuncSetAttribute(kda_linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM) !=
       cudaSuccess)
     return KDA_ECUDA;
-  static int cluster_cache[64][LIN_MAX_SPLIT + 1];  // by cluster size
+  static std::atomic<int> cluster_cache[64][LIN_MAX_SPLIT + 1];  // by cluster size, as above
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ECUDA;
   cudaLaunchConfig_t cfg = {};
@@ -790,7 +797,7 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
     return KDA_ECUDA;
   for (int c = 1; c * pair <= LIN_MAX_SPLIT && c <= stages; ++c) {
     const int cs = c * pair;  // cluster size
-    int held = dev < 64 ? cluster_cache[dev][cs] : 0;
+    int held = dev < 64 ? cluster_cache[dev][cs].load(std::memory_order_relaxed) : 0;
     if (held <= 0) {
       attr[0].val.clusterDim.x = (unsigned)cs;
       cfg.gridDim = dim3((unsigned)cs, 1, 1);
@@ -799,7 +806,7 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
       const int cap = sms * (per_sm > 0 ? per_sm : 1) / cs;
       if (held > cap) held = cap;
       if (held <= 0) continue;
-      if (dev < 64) cluster_cache[dev][cs] = held;
+      if (dev < 64) cluster_cache[dev][cs].store(held, std::memory_order_relaxed);
     }
     // waves of clusters: a last wave at least a quarter full counts by its share (its
     // CTAs run with the copy engines and L2 less loaded), a smaller one as a whole wave
