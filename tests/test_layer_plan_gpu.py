@@ -97,6 +97,46 @@ def test_layer_plan_equals_the_three_calls(w):
     ds.close()
 
 
+@pytest.mark.parametrize("variant", ["bf16_state", "softplus_gate", "conv_transposed"])
+def test_layer_plan_variants(variant):
+    # the layer graph on the core's variants (bf16 state pool, the second gate form, the
+    # [pool, W-1, 3D] conv layout), PDL on both edges, against the three separate calls
+    w = I.Workload("verify_24_rows_v", heads=2, requests=6, L=4, pool=32, verify=True, seed=2124)
+    si = I.make_step_inputs(w)
+    kw = {"bf16_state": dict(state_dtype="bf16"), "softplus_gate": dict(gate_mode=1),
+          "conv_transposed": dict(dim_first=False)}[variant]
+    ds = G.DeviceStep(si, **kw)
+    conv0, state0 = ds.conv.clone(), ds.state.clone()
+    gen = torch.Generator().manual_seed(w.seed)
+    x = _rand(gen, (w.rows, HIDDEN), 1.0)
+    w_in = _rand(gen, (w.pitch, HIDDEN), 0.02)
+    w_o = _rand(gen, (HIDDEN, w.dim), 0.05)
+    caches = (ds.conv, ds.state)
+    proj_r = kda.linear(x, w_in)
+    core_r = torch.empty((w.rows, w.dim), dtype=torch.bfloat16, device="cuda")
+    ds.prep.run(proj_r, core_r, caches=caches, slots=ds.slots, accepted=ds.accepted)
+    y_r = kda.linear(core_r, w_o)
+    torch.cuda.synchronize()
+    conv_r, state_r = ds.conv.clone(), ds.state.clone()
+    ds.conv.copy_(conv0)
+    ds.state.copy_(state0)
+    proj = torch.empty_like(proj_r)
+    core = torch.empty_like(core_r)
+    y = torch.empty_like(y_r)
+    plan = ds.prep.layer_plan(x, w_in, proj, core, w_o, y, caches=caches, slots=ds.slots, accepted=ds.accepted,
+                              pdl=True)
+    plan.launch()
+    torch.cuda.synchronize()
+    assert ds.prep.check() == 0 and kda.kda_linear_check() == 0
+    for name, a, b in (("projected", proj, proj_r), ("core_out", core, core_r), ("y", y, y_r),
+                       ("conv_state", ds.conv, conv_r), ("state", ds.state, state_r)):
+        va = a.view(torch.int32) if a.dtype == torch.float32 else _bits(a)
+        vb = b.view(torch.int32) if b.dtype == torch.float32 else _bits(b)
+        assert torch.equal(va, vb), f"{variant}: {name} differs"
+    plan.close()
+    ds.close()
+
+
 def test_layer_plan_rejects_inconsistent_shapes():
     w = I.WORKLOADS["tiny_decode"]
     si = I.make_step_inputs(w)
