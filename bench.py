@@ -379,7 +379,9 @@ def run_linear(args, w: I.Workload):
     t_host1 = time.time()
     time.sleep(0.25)
     sampler.stop()
-    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = sum(step_ms) / args.steps
+    median_ms = statistics.median(step_ms)
     # e2e: x up from pinned host memory, y back, every step (the weight is resident)
     hx = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).view(torch.bfloat16).pin_memory()
     hy = torch.empty((rows, N), dtype=torch.bfloat16).pin_memory()
@@ -404,7 +406,8 @@ def run_linear(args, w: I.Workload):
     roof["kernel"] = "kda_linear_kernel"
     line = {
         "metric": PROJ_METRIC, "value": rows / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": median_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 x bf16 -> f32 accumulate", "data": "synthetic",
         "config": {"workload": f"{args.op} for {w.name}", "op": args.op, "rows": rows, "in_features": K,
                    "out_features": N, "weight_bytes": N * K * 2, "algorithmic_bytes_per_step": nbytes,
@@ -510,6 +513,7 @@ def run_layer(args, w: I.Workload):
     if dw.prep.check() != 0 or kda.kda_linear_check() != 0:
         raise RuntimeError("device error bits set during the timed steps")
     ms = sum(t_head) / args.steps
+    median_ms = statistics.median(t_head)
 
     # e2e: x up from pinned host memory and y back every step, around the plan's launch
     hx = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -533,7 +537,8 @@ def run_layer(args, w: I.Workload):
     achieved = layer_b / (ms / 1e3) / 1e9
     line = {
         "metric": LAYER_METRIC, "value": w.rows / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": median_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 projections (fp32 accumulate), f32 core", "data": "synthetic",
         "config": dict(workload_config(w, args), workload=f"layer for {w.name}", op="layer", hidden=HIDDEN,
                        dependent_launch_edges=head,
@@ -655,7 +660,9 @@ def main():
             dw.step()
             ends[i].record(stream)
         barrier()
-        elapsed_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        elapsed_ms = sum(step_ms)
+        median_ms = statistics.median(step_ms)
     else:
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record(stream)
@@ -664,6 +671,7 @@ def main():
         ev1.record(stream)
         barrier()
         elapsed_ms = ev0.elapsed_time(ev1)
+        median_ms = None  # back-to-back steps (inputs larger than L2): one interval, no per-step times
     t_host1 = time.time()
     time.sleep(0.25)
     sampler.stop()
@@ -757,7 +765,8 @@ def main():
     state_gbs = state_b / (ms_step / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median": median_ms,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload_config(w, args),
         "state_gbs": state_gbs, "state_frac_of_peak": state_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
