@@ -328,6 +328,67 @@ def bf16_tflops_peak():
     return 1900.0, "fallback"
 
 
+def overlapped_e2e(device, steps, upload, compute, download, nb=2, graph=True):
+    """End-to-end time per step (ms) of `steps` steps, each: upload(b) (host -> device
+    copies of buffer set b) on a stream of its own, compute(b) on the compute stream,
+    download(b) (device -> host) on a third stream; two buffer sets, so step i+1's inputs
+    go up and step i-1's outputs come back while step i computes.  With `graph`, blocks
+    of E2E_BLOCK steps are recorded once as a CUDA graph and replayed, so the host does
+    not pace short steps; else the blocks are issued directly."""
+    import torch
+
+    up, down, cap = torch.cuda.Stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device)
+    in_ready = [torch.cuda.Event() for _ in range(nb)]
+    done = [torch.cuda.Event() for _ in range(nb)]
+    out_back = [torch.cuda.Event() for _ in range(nb)]
+
+    def block(n):
+        up.wait_stream(cap)
+        down.wait_stream(cap)
+        for i in range(n):
+            b = i % nb
+            with torch.cuda.stream(up):
+                if i >= nb:
+                    up.wait_event(done[b])  # the compute that read buffer set b is done
+                upload(b)
+                in_ready[b].record(up)
+            cap.wait_event(in_ready[b])
+            if i >= nb:
+                cap.wait_event(out_back[b])  # buffer set b's last output is home
+            with torch.cuda.stream(cap):
+                compute(b)
+            done[b].record(cap)
+            with torch.cuda.stream(down):
+                down.wait_event(done[b])
+                download(b)
+                out_back[b].record(down)
+        cap.wait_stream(up)
+        cap.wait_stream(down)
+
+    block(E2E_BLOCK)  # warm: allocations, first launches
+    torch.cuda.synchronize(device)
+    reps = max(1, -(-steps // E2E_BLOCK))
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            block(E2E_BLOCK)
+        with torch.cuda.stream(cap):  # replay() launches on the current stream
+            g.replay()
+        torch.cuda.synchronize(device)
+        run = g.replay
+    else:
+        def run():
+            block(E2E_BLOCK)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(cap):
+        e0.record(cap)
+        for _ in range(reps):
+            run()
+        e1.record(cap)
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) / (reps * E2E_BLOCK), reps * E2E_BLOCK
+
+
 def run_linear(args, w: I.Workload):
     """--op in_proj / o_proj: kda_linear on the layer's shape for the workload's
     rows (in_proj: x [rows, 7168] . W [pitch, 7168]^T; o_proj: core [rows, D] .
@@ -382,19 +443,17 @@ def run_linear(args, w: I.Workload):
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     ms = sum(step_ms) / args.steps
     median_ms = statistics.median(step_ms)
-    # e2e: x up from pinned host memory, y back, every step (the weight is resident)
+    # e2e: x up from pinned host memory and y back every step (the weight is resident),
+    # copies overlapped with the products on streams of their own
     hx = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).view(torch.bfloat16).pin_memory()
     hy = torch.empty((rows, N), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        x.copy_(hx, non_blocking=True)
-        kda.linear(x, W, y)
-        hy.copy_(y, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    dx = [torch.empty_like(x) for _ in range(2)]
+    dy = [torch.empty_like(y) for _ in range(2)]
+    e2e_ms, e2e_steps = overlapped_e2e(
+        device, args.e2e_steps or max(3, min(args.steps, 200)),
+        upload=lambda b: dx[b].copy_(hx, non_blocking=True),
+        compute=lambda b: kda.linear(dx[b], W, dy[b]),
+        download=lambda b: hy.copy_(dy[b], non_blocking=True))
     if tensor_bound:
         roof = {"bound": "tensor", "achieved": flops / (ms / 1e3) / 1e12, "peak": tf, "unit": "TFLOP/s",
                 "peak_source": f"{tf_src} bf16_tflops (MEASURED_PEAKS.json)"}
@@ -415,7 +474,9 @@ def run_linear(args, w: I.Workload):
                    "l2": "L2 flushed between timed steps (256 MiB write, then 256 MiB read; outside the events)"},
         "roofline": roof,
         "e2e": {"value": rows / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": rows * K * 2,
-                "d2h_bytes_per_step": rows * N * 2, "steps": e2e_steps},
+                "d2h_bytes_per_step": rows * N * 2, "steps": e2e_steps,
+                "overlap": f"uploads and downloads on streams of their own, two buffer sets; blocks of {E2E_BLOCK} "
+                           "steps recorded as a CUDA graph"},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(t_host0, t_host1),
     }
@@ -515,19 +576,20 @@ def run_layer(args, w: I.Workload):
     ms = sum(t_head) / args.steps
     median_ms = statistics.median(t_head)
 
-    # e2e: x up from pinned host memory and y back every step, around the plan's launch
+    # e2e: x up from pinned host memory and y back every step, copies overlapped with the
+    # layer on streams of their own: two buffer sets, a layer plan on each (the caches are
+    # shared, so the steps stay in order on the compute stream)
     hx = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).view(torch.bfloat16).pin_memory()
     hy = torch.empty((w.rows, HIDDEN), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        x.copy_(hx, non_blocking=True)
-        plans[head].launch()
-        hy.copy_(y, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    sets = [(torch.empty_like(x), torch.empty_like(dw.projected), torch.empty_like(dw.out), torch.empty_like(y))
+            for _ in range(2)]
+    e2e_plans = [dw.prep.layer_plan(bx, w_in, bp, bc, w_o, by, caches=caches, slots=dw.slots, accepted=dw.accepted,
+                                    pdl=masks[head]) for bx, bp, bc, by in sets]
+    e2e_ms, e2e_steps = overlapped_e2e(
+        device, args.e2e_steps or max(3, min(args.steps, 200)),
+        upload=lambda b: sets[b][0].copy_(hx, non_blocking=True),
+        compute=lambda b: e2e_plans[b].launch(),
+        download=lambda b: hy.copy_(sets[b][3], non_blocking=True), graph=False)
 
     state_b, step_b = algorithmic_bytes(w, args.state_dtype)
     proj_b = (w.pitch * HIDDEN + HIDDEN * w.dim) * 2 + w.rows * (HIDDEN * 2 + w.pitch + w.dim) * 2
@@ -551,7 +613,9 @@ def run_layer(args, w: I.Workload):
         "layer_ms": dict({f"graph_pdl_{head}": ms}, **{f"graph_pdl_{k}": v for k, v in others.items()},
                          three_calls=sum(t_sep) / args.steps),
         "e2e": {"value": w.rows / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": w.rows * HIDDEN * 2,
-                "d2h_bytes_per_step": w.rows * HIDDEN * 2, "steps": e2e_steps},
+                "d2h_bytes_per_step": w.rows * HIDDEN * 2, "steps": e2e_steps,
+                "overlap": "uploads and downloads on streams of their own, two buffer sets, each with a layer "
+                           "plan (a CUDA graph)"},
         "gpu_launches": 3 * args.steps,
         "clocks": sampler.summary(t_host0, t_host1),
     }

@@ -792,15 +792,15 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
   const long long stages = (a.K + TC_BK - 1) / TC_BK;
   long long split = 1;
   double best = 1e300;
-  int sms = 0, per_sm = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_tc_kernel, TC_THREADS, TC_SMEM) !=
-          cudaSuccess)
-    return KDA_ECUDA;
   for (int c = 1; c * pair <= LIN_MAX_SPLIT && c <= stages; ++c) {
     const int cs = c * pair;  // cluster size
     int held = dev < 64 ? cluster_cache[dev][cs].load(std::memory_order_relaxed) : 0;
     if (held <= 0) {
+      int sms = 0, per_sm = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_tc_kernel, TC_THREADS, TC_SMEM) !=
+              cudaSuccess)
+        return KDA_ECUDA;
       attr[0].val.clusterDim.x = (unsigned)cs;
       cfg.gridDim = dim3((unsigned)cs, 1, 1);
       if (cudaOccupancyMaxActiveClusters(&held, kda_linear_tc_kernel, &cfg) != cudaSuccess) return KDA_ECUDA;
