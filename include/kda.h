@@ -45,6 +45,10 @@
  *
  * Thread safety: one handle may be used from one host thread at a time.
  * Steps enqueued on different streams against the same caches race.
+ *
+ * Around the core: kda_linear computes the layer's projections y = x . W^T
+ * (in_proj in front of the step, o_proj after it), and kda_layer_plan_create
+ * records in_proj -> step -> o_proj on fixed buffers as one CUDA graph.
  */
 #ifndef KDA_H
 #define KDA_H
