@@ -48,6 +48,10 @@ MUTATIONS = [
      "beta[t * heads + h] = sigmoid(bf16_value(prow[4 * D + HEAD_DIM]));"),
     ("out_gate_dropped", "* sigmoid(bf16_value(gate[v]));", ";"),
     ("padding_not_detected", "if (slots[row0] == -1) {", "if (0) {"),
+    ("fb_transposed", "bf16_value(f_b[c * HEAD_DIM + j])", "bf16_value(f_b[j * D + c])"),
+    ("fa_offset_outgate", "bf16_value(prow[4 * D + j])", "bf16_value(prow[3 * D + j])"),
+    ("fa_offset_shifted", "bf16_value(prow[4 * D + j])", "bf16_value(prow[4 * D + (j + 1) % HEAD_DIM])"),
+    ("z_unrounded", "z = bf16_rounded(z);", "z = z + 0.0;"),
     ("no_round_to_even", "r = nearbyint(ax / quantum) * quantum;", "r = floor(ax / quantum + 0.5) * quantum;"),
 ]
 

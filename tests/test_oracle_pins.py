@@ -16,6 +16,7 @@ import torch
 
 import oracle
 from oracle import oracle_np
+from linear_attention_decode_03_gb300.inputs import to_bf16_bits as I_to_bf16
 from tests.helpers import (BF16_NEG_INF, BF16_POS_INF, HEAD_DIM, bf16_value, case, head_cols,
                            oracle_weights)
 
@@ -205,6 +206,84 @@ def test_gate_limits(run):
     *_, dg = run(W, si.projected, conv, pool, si.slots, 1, None, diag=True)
     g = dg[:, :, 3 * HEAD_DIM:4 * HEAD_DIM]
     assert np.all((g > lb) & (g < 0))
+
+
+def _zero_gate_weights(si, f_b):
+    """A_log = 0 and dt_bias = 0, so that the sigmoid gate is g = lb * sigmoid(z)."""
+    return oracle_weights(si, f_b=f_b, A_log=np.zeros_like(si.weights.A_log),
+                          dt_bias=np.zeros_like(si.weights.dt_bias), gate_lower_bound=-5.0)
+
+
+def _gates(run, si, W):
+    *_, err, dg = run(W, si.projected, si.full_conv_state(), si.full_state_pool(), si.slots, 1, None, diag=True)
+    assert err == 0
+    return dg[:, :, 3 * HEAD_DIM:4 * HEAD_DIM].reshape(si.workload.rows, -1)  # [rows, D], channel c = 128 h + i
+
+
+def _bf16_of_f32(x) -> np.ndarray:
+    """torch's fp32 -> bf16 (nearest even) of values exactly representable in fp32, as fp64."""
+    x32 = np.asarray(x, dtype=np.float32)
+    assert np.array_equal(x32.astype(np.float64), np.asarray(x, dtype=np.float64)), "not exact in fp32"
+    return torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def test_z_one_hot_rows_pick_f_a(run):
+    """z = f_b . f_a over the f_a columns [4D, 4D + 128) of the packed row
+    (PreparedKda._operands; K1 "f_b MFMA + lower-bound gate"): with row c of
+    f_b the unit vector e_{pi(c)} (pi a permutation per head), z[c] =
+    f_a[pi(c)] exactly, so with A_log = dt_bias = 0 the gate is
+    g[c] = lb * sigmoid(f_a[pi(c)]) in closed form.  A transposed f_b, another
+    column offset for f_a or a dropped product fails this."""
+    si, _, _ = _decode_case(heads=2, requests=3, seed=31)
+    D, H = si.workload.dim, si.workload.heads
+    rng = np.random.default_rng(31)
+    perm = np.concatenate([rng.permutation(HEAD_DIM) for _ in range(H)])   # pi(c) for c < D
+    f_b = np.zeros((D, HEAD_DIM), np.uint16)
+    f_b[np.arange(D), perm] = 0x3F80                                        # bf16 1.0
+    g = _gates(run, si, _zero_gate_weights(si, f_b))
+    f_a = bf16_value(si.projected[:, 4 * D:4 * D + HEAD_DIM])              # [rows, 128]
+    expect = -5.0 / (1.0 + np.exp(-f_a[:, perm]))
+    np.testing.assert_allclose(g, expect, rtol=1e-13, atol=0)
+
+
+def test_z_two_taps_rounded_once_to_bf16(run):
+    """Two taps a row, f_b[c, pi(c)] = 1 and f_b[c, pi'(c)] = 1/8, and f_a
+    entries of magnitude in [1, 2): z = f_a[pi(c)] + f_a[pi'(c)] / 8 is exact
+    in fp32 and is handed on rounded once to bf16 (nearest even; the hand-offs
+    of the unfused path, K1 rounding statement).  Most sums are not bf16
+    values, so a z kept unrounded, or rounded another way, fails."""
+    si, _, _ = _decode_case(heads=2, requests=4, seed=32)
+    D, H = si.workload.dim, si.workload.heads
+    rng = np.random.default_rng(32)
+    fa = rng.uniform(1.0, 2.0, size=(si.workload.rows, HEAD_DIM)) * rng.choice([-1.0, 1.0], size=(si.workload.rows, HEAD_DIM))
+    si.projected[:, 4 * D:4 * D + HEAD_DIM] = I_to_bf16(fa)
+    perm = np.concatenate([rng.permutation(HEAD_DIM) for _ in range(H)])
+    perm2 = np.concatenate([np.roll(perm[h * HEAD_DIM:(h + 1) * HEAD_DIM], 1) for h in range(H)])
+    f_b = np.zeros((D, HEAD_DIM), np.uint16)
+    f_b[np.arange(D), perm] = 0x3F80                                        # 1.0
+    f_b[np.arange(D), perm2] = 0x3E00                                       # 0.125
+    g = _gates(run, si, _zero_gate_weights(si, f_b))
+    f_a = bf16_value(si.projected[:, 4 * D:4 * D + HEAD_DIM])
+    z_exact = f_a[:, perm] + f_a[:, perm2] / 8.0
+    z = _bf16_of_f32(z_exact)
+    assert np.mean(z != z_exact) > 0.5                                      # the rounding is exercised
+    np.testing.assert_allclose(g, -5.0 / (1.0 + np.exp(-z)), rtol=1e-13, atol=0)
+
+
+def test_z_full_row_sum(run):
+    """Every tap nonzero: f_b[c, j] = 2^-(c mod 8) for all j and integer f_a
+    in [-8, 8], so z[c] = 2^-(c mod 8) * sum_j f_a[j] exactly before the bf16
+    rounding: the whole 128-term contraction is summed."""
+    si, _, _ = _decode_case(heads=1, requests=3, seed=33)
+    D = si.workload.dim
+    rng = np.random.default_rng(33)
+    fa = rng.integers(-8, 9, size=(si.workload.rows, HEAD_DIM)).astype(np.float64)
+    si.projected[:, 4 * D:4 * D + HEAD_DIM] = I_to_bf16(fa)
+    scale = 2.0 ** -(np.arange(D) % 8)
+    f_b = np.repeat(I_to_bf16(scale)[:, None], HEAD_DIM, axis=1)
+    g = _gates(run, si, _zero_gate_weights(si, f_b))
+    z = _bf16_of_f32(fa.sum(axis=1)[:, None] * scale[None, :])
+    np.testing.assert_allclose(g, -5.0 / (1.0 + np.exp(-z)), rtol=1e-13, atol=0)
 
 
 def test_gate_limits_softplus_form(run):
