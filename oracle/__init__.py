@@ -50,19 +50,27 @@ _LIB_OVERRIDE = os.environ.get("KDA_ORACLE_LIB_OVERRIDE")
 _lib = None
 
 
+GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off"]
+
+
 def build(force: bool = False) -> str:
-    """Compile the C oracle with gcc (plain -O2, no vectorisation flags)."""
+    """Compile the C oracle with gcc (plain -O2, no vectorisation flags), with
+    OpenMP over the (request, head) tasks where the compiler has it (the
+    results do not depend on the thread count)."""
     if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
         return _LIB
     os.makedirs(_LIB_DIR, exist_ok=True)
     tmp = _LIB + f".tmp{os.getpid()}"
-    subprocess.run(
-        ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off",
-         "-o", tmp, _SRC, "-lm"],
-        check=True,
-    )
+    res = subprocess.run(["gcc", *GCC_FLAGS, "-fopenmp", "-o", tmp, _SRC, "-lm"], capture_output=True, text=True)
+    if res.returncode != 0:  # no OpenMP runtime: the same source, serial
+        subprocess.run(["gcc", *GCC_FLAGS, "-o", tmp, _SRC, "-lm"], check=True)
     os.replace(tmp, _LIB)
     return _LIB
+
+
+def max_threads() -> int:
+    """Threads the oracle can run its (request, head) tasks on (1 without OpenMP)."""
+    return int(_load().kda_oracle_max_threads())
 
 
 def _load():
@@ -72,6 +80,7 @@ def _load():
         lib.kda_oracle_step.restype = ctypes.c_int
         lib.kda_oracle_bf16_round.restype = ctypes.c_uint16
         lib.kda_oracle_bf16_round.argtypes = [ctypes.c_double]
+        lib.kda_oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -112,12 +121,14 @@ def bf16_round(x: float) -> int:
 
 def step(w: Weights, projected, conv_state, state_pool, slots, L: int, accepted=None, *,
          dim_first: bool = True, act: str = "silu", gate_mode: int = 0, state_dtype: str = "f32",
-         diag: bool = False):
+         diag: bool = False, threads: int = 1):
     """One decode (accepted None, L = 1) or verify step of the C oracle.
 
     gate_mode 0: g = lb * sigmoid(e^A (z + dt)); 1: g = max(-e^A softplus(z + dt), lb).
     state_dtype "f32" (state_pool fp32) or "bf16" (state_pool uint16 bf16 bits,
     each stored state rounded to nearest even).
+    threads: OpenMP threads over the step's (request, head) tasks; each task
+    runs in the same order whatever the count, so the results are the same.
 
     conv_state and state_pool are copied, not modified.  Returns
     ``(out, conv_state, state_pool, err[, diag])`` where ``diag`` is
@@ -150,7 +161,7 @@ def step(w: Weights, projected, conv_state, state_pool, slots, L: int, accepted=
         ctypes.c_int64(rows), ctypes.c_int64(pitch), _ptr(conv_state), ctypes.c_int(1 if dim_first else 0),
         _ptr(state_pool), ctypes.c_int64(pool), ctypes.c_int(1 if bf16_state else 0), _ptr(slots), ctypes.c_int(L),
         _ptr(acc), _ptr(out),
-        ctypes.byref(err), _ptr(dg),
+        ctypes.byref(err), _ptr(dg), ctypes.c_int(int(threads)),
     )
     if rc != 0:
         raise ValueError(f"kda_oracle_step rejected its arguments (rc={rc})")

@@ -48,6 +48,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define HEAD_DIM 128
 
@@ -94,6 +97,181 @@ static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(e
 /* Exported so that tests can pin the rounding rule itself. */
 uint16_t kda_oracle_bf16_round(double x) { return bf16_round(x); }
 
+/* The arguments of one step, shared by its (request, head) tasks. */
+typedef struct {
+    int heads, W, act, gate_mode, dim_first, state_bf16, L;
+    const uint16_t *conv_w, *bias, *f_b;
+    const float *A_log, *dt_bias, *o_norm;
+    double lb, eps;
+    const uint16_t *projected;
+    int64_t pitch, pool;
+    uint16_t *conv_state;
+    float *state_pool;
+    const int32_t *slots;
+    uint16_t *out;
+    double *diag;
+} StepArgs;
+
+/* Working arrays of one task. */
+typedef struct {
+    double *qkv;    /* [L][3][128]: conv outputs of the head's q, k, v channels, bf16-rounded */
+    double *g;      /* [L][128]: the head's log-decays */
+    double *beta;   /* [L] */
+    double *S;      /* [128 (k)][128 (v)] */
+    double *window; /* [W-1] */
+} TaskBuf;
+
+/*
+ * Steps 2-6 for head h of request r (rows r L .. r L + L - 1), starting from
+ * slot `start`.  Every channel the task touches belongs to head h (its q, k
+ * and v conv channels, its 128 decay channels, its beta column, its state
+ * block and its output columns), so the tasks of one step are independent:
+ * they write disjoint cache entries (distinct slots per request; a step with
+ * duplicate slots is undefined).
+ */
+static void run_task(const StepArgs *a, int64_t r, int64_t h, int64_t start, TaskBuf *b) {
+    const int64_t D = (int64_t)HEAD_DIM * a->heads, C = 3 * D, SL = a->W - 1, W = a->W, L = a->L;
+    const int64_t row0 = r * L, heads = a->heads;
+    const int64_t DIAG = 5 * HEAD_DIM + 1;
+    const double q_scale = 1.0 / sqrt((double)HEAD_DIM);
+    const uint16_t *projected = a->projected, *conv_w = a->conv_w, *bias = a->bias, *f_b = a->f_b;
+    const int64_t pitch = a->pitch;
+    uint16_t *conv_state = a->conv_state;
+    const int dim_first = a->dim_first;
+    double *window = b->window;
+
+    /* Step 1+2: split the packed row; causal depthwise conv of the head's
+     * q|k|v channels against the window of the start slot. */
+    for (int kind = 0; kind < 3; ++kind)
+        for (int i = 0; i < HEAD_DIM; ++i) {
+            const int64_t c = kind * D + h * HEAD_DIM + i;
+            for (int64_t j = 0; j < SL; ++j) {
+                int64_t ix = dim_first ? (start * C + c) * SL + j : (start * SL + j) * C + c;
+                window[j] = bf16_value(conv_state[ix]);
+            }
+            for (int64_t t = 0; t < L; ++t) {
+                const double x_t = bf16_value(projected[(row0 + t) * pitch + c]);
+                double y = bias ? bf16_value(bias[c]) : 0.0;
+                for (int64_t j = 0; j < W; ++j) {
+                    const double x = (j < SL) ? window[j] : x_t; /* tap W-1 = current token */
+                    y += bf16_value(conv_w[c * W + j]) * x;
+                }
+                if (a->act) y = y * sigmoid(y); /* SiLU */
+                b->qkv[(t * 3 + kind) * HEAD_DIM + i] = bf16_rounded(y);
+                /* shift the window by one and store it in this token's slot */
+                for (int64_t j = 0; j + 1 < SL; ++j) window[j] = window[j + 1];
+                if (SL > 0) window[SL - 1] = x_t;
+                const int64_t dst = a->slots[row0 + t];
+                for (int64_t j = 0; j < SL; ++j) {
+                    int64_t ix = dim_first ? (dst * C + c) * SL + j : (dst * SL + j) * C + c;
+                    conv_state[ix] = bf16_round(window[j]);
+                }
+            }
+        }
+
+    /* Step 3: gates.  z = f_b . f_a (bf16 hand-off), lower-bounded decay, beta. */
+    const double lb = a->lb;
+    for (int64_t t = 0; t < L; ++t) {
+        const uint16_t *prow = projected + (row0 + t) * pitch;
+        for (int i = 0; i < HEAD_DIM; ++i) {
+            const int64_t c = h * HEAD_DIM + i;
+            double z = 0.0;
+            for (int64_t j = 0; j < HEAD_DIM; ++j)
+                z += bf16_value(f_b[c * HEAD_DIM + j]) * bf16_value(prow[4 * D + j]);
+            z = bf16_rounded(z);
+            if (a->gate_mode == 0)
+                b->g[t * HEAD_DIM + i] = (double)lb * sigmoid(exp((double)a->A_log[h]) * (z + (double)a->dt_bias[c]));
+            else
+                b->g[t * HEAD_DIM + i] = fmax(-exp((double)a->A_log[h]) * softplus(z + a->dt_bias[c]), (double)lb);
+        }
+        b->beta[t] = sigmoid(bf16_value(prow[4 * D + HEAD_DIM + h]));
+    }
+
+    /* Start state of (request, head), storage [v][k] -> S[k][v]. */
+    double *S = b->S;
+    const float *src = a->state_pool + (start * heads + h) * HEAD_DIM * HEAD_DIM;
+    const uint16_t *src16 = (const uint16_t *)a->state_pool + (start * heads + h) * HEAD_DIM * HEAD_DIM;
+    for (int v = 0; v < HEAD_DIM; ++v)
+        for (int k = 0; k < HEAD_DIM; ++k) {
+            if (a->state_bf16) S[k * HEAD_DIM + v] = bf16_value(src16[v * HEAD_DIM + k]);
+            else S[k * HEAD_DIM + v] = (double)src[v * HEAD_DIM + k];
+        }
+
+    for (int64_t t = 0; t < L; ++t) {
+        const double *qr = b->qkv + (t * 3 + 0) * HEAD_DIM;
+        const double *kr = b->qkv + (t * 3 + 1) * HEAD_DIM;
+        const double *vr = b->qkv + (t * 3 + 2) * HEAD_DIM;
+        const double *gr = b->g + t * HEAD_DIM;
+        const double bt = b->beta[t];
+
+        /* Step 4: L2 normalisation of q and k, q scaled by 128^-0.5. */
+        double qq = 0.0, kk = 0.0;
+        for (int i = 0; i < HEAD_DIM; ++i) { qq += qr[i] * qr[i]; kk += kr[i] * kr[i]; }
+        const double qn = 1.0 / sqrt(qq + 1e-6), kn = 1.0 / sqrt(kk + 1e-6);
+        double qh[HEAD_DIM], kh[HEAD_DIM], o[HEAD_DIM], u[HEAD_DIM];
+        for (int i = 0; i < HEAD_DIM; ++i) { qh[i] = qr[i] * qn * q_scale; kh[i] = kr[i] * kn; }
+
+        /* Step 5: gated delta rule.  S <- diag(e^g) S;  u = v - S^T k^;
+         * S <- S + beta k^ u^T;  o = S^T q^ (the updated state). */
+        for (int k = 0; k < HEAD_DIM; ++k) {
+            const double decay = exp(gr[k]);
+            for (int v = 0; v < HEAD_DIM; ++v) S[k * HEAD_DIM + v] *= decay;
+        }
+        for (int v = 0; v < HEAD_DIM; ++v) {
+            double s = 0.0;
+            for (int k = 0; k < HEAD_DIM; ++k) s += S[k * HEAD_DIM + v] * kh[k];
+            u[v] = vr[v] - s;
+        }
+        for (int k = 0; k < HEAD_DIM; ++k)
+            for (int v = 0; v < HEAD_DIM; ++v) S[k * HEAD_DIM + v] += bt * kh[k] * u[v];
+        for (int v = 0; v < HEAD_DIM; ++v) {
+            double s = 0.0;
+            for (int k = 0; k < HEAD_DIM; ++k) s += S[k * HEAD_DIM + v] * qh[k];
+            o[v] = bf16_rounded(s); /* bf16 hand-off into the norm */
+        }
+        /* one state written per token, into slots[r, t] */
+        float *dst = a->state_pool + ((int64_t)a->slots[row0 + t] * heads + h) * HEAD_DIM * HEAD_DIM;
+        uint16_t *dst16 = (uint16_t *)a->state_pool + ((int64_t)a->slots[row0 + t] * heads + h) * HEAD_DIM * HEAD_DIM;
+        for (int v = 0; v < HEAD_DIM; ++v)
+            for (int k = 0; k < HEAD_DIM; ++k) {
+                if (a->state_bf16) dst16[v * HEAD_DIM + k] = bf16_round(S[k * HEAD_DIM + v]);
+                else dst[v * HEAD_DIM + k] = (float)S[k * HEAD_DIM + v];
+            }
+
+        /* Step 6: gated RMSNorm over the head's 128 -> bf16 core_out. */
+        double ms = 0.0;
+        for (int v = 0; v < HEAD_DIM; ++v) ms += o[v] * o[v];
+        ms /= HEAD_DIM;
+        const double rstd = 1.0 / sqrt(ms + a->eps);
+        const uint16_t *gate = projected + (row0 + t) * pitch + 3 * D + h * HEAD_DIM;
+        for (int v = 0; v < HEAD_DIM; ++v) {
+            const double y = o[v] * rstd * (double)a->o_norm[v] * sigmoid(bf16_value(gate[v]));
+            a->out[(row0 + t) * D + h * HEAD_DIM + v] = bf16_round(y);
+        }
+
+        if (a->diag) {
+            double *dg = a->diag + ((row0 + t) * heads + h) * DIAG;
+            for (int i = 0; i < HEAD_DIM; ++i) {
+                dg[i] = qh[i];
+                dg[HEAD_DIM + i] = kh[i];
+                dg[2 * HEAD_DIM + i] = vr[i];
+                dg[3 * HEAD_DIM + i] = gr[i];
+                dg[4 * HEAD_DIM + i] = o[i];
+            }
+            dg[5 * HEAD_DIM] = bt;
+        }
+    }
+}
+
+/* Threads the OpenMP build may use (1 when built without OpenMP). */
+int kda_oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
 /*
  * One decode or verify step.
  *
@@ -115,6 +293,9 @@ uint16_t kda_oracle_bf16_round(double x) { return bf16_round(x); }
  *   out               [rows, D] bf16
  *   err               OR-ed error bits (ERR_SLOT, ERR_ACCEPTED)
  *   diag              NULL or [rows, H, 5*128 + 1] fp64: q^, k^, v, g, o (bf16), beta
+ *   threads           OpenMP threads over the (request, head) tasks (1 = serial);
+ *                     each task runs its steps in the same order whatever the
+ *                     count, so the results do not depend on it
  *
  * Returns 0, or -1 for arguments that make the step undefined.
  */
@@ -124,167 +305,64 @@ int kda_oracle_step(int heads, int W, const uint16_t *conv_w, const uint16_t *bi
                     const uint16_t *projected, int64_t rows, int64_t pitch,
                     uint16_t *conv_state, int dim_first, float *state_pool, int64_t pool, int state_bf16,
                     const int32_t *slots, int L, const int32_t *accepted, uint16_t *out,
-                    uint32_t *err, double *diag) {
-    if (heads < 1 || W < 2 || L < 1 || rows < 0 || pool < 0) return -1;
+                    uint32_t *err, double *diag, int threads) {
+    if (heads < 1 || W < 2 || L < 1 || rows < 0 || pool < 0 || threads < 1) return -1;
     if (rows % L != 0) return -1;
     if (accepted == NULL && L != 1) return -1;
-    const int64_t D = (int64_t)HEAD_DIM * heads, C = 3 * D, SL = W - 1;
+    const int64_t D = (int64_t)HEAD_DIM * heads;
     if (pitch < 4 * D + HEAD_DIM + heads) return -1;
     const int64_t R = rows / L;
-    const int64_t DIAG = 5 * HEAD_DIM + 1;
-    const double q_scale = 1.0 / sqrt((double)HEAD_DIM);
+    StepArgs a = {heads, W, act, gate_mode, dim_first, state_bf16, L, conv_w, bias, f_b, A_log, dt_bias, o_norm,
+                  (double)lb, (double)eps, projected, pitch, pool, conv_state, state_pool, slots, out, diag};
 
-    double *qkv = malloc(sizeof(double) * (size_t)(L * C)); /* conv outputs, bf16-rounded */
-    double *g = malloc(sizeof(double) * (size_t)(L * D));
-    double *beta = malloc(sizeof(double) * (size_t)(L * heads));
-    double *S = malloc(sizeof(double) * HEAD_DIM * HEAD_DIM); /* S[k][v] */
-    double *window = malloc(sizeof(double) * (size_t)(SL > 0 ? SL : 1));
-    if (!qkv || !g || !beta || !S || !window) {
-        free(qkv); free(g); free(beta); free(S); free(window);
-        return -1;
-    }
-
+    /* Step 1 per request: padding, accepted and slot checks, the start slot. */
+    int64_t *start_of = malloc(sizeof(int64_t) * (size_t)(R > 0 ? R : 1));
+    if (!start_of) return -1;
     for (int64_t r = 0; r < R; ++r) {
         const int64_t row0 = r * L;
-
+        start_of[r] = -1;
         /* Padding request: slot -1 in its first position. */
         if (slots[row0] == -1) {
             for (int64_t t = 0; t < L; ++t)
                 for (int64_t c = 0; c < D; ++c) out[(row0 + t) * D + c] = 0;
             continue;
         }
-        int a = 1;
+        int acc = 1;
         if (accepted != NULL) {
-            a = accepted[r];
-            if (a < 1 || a > L) { *err |= ERR_ACCEPTED; continue; }
+            acc = accepted[r];
+            if (acc < 1 || acc > L) { *err |= ERR_ACCEPTED; continue; }
         }
         int bad = 0;
         for (int64_t t = 0; t < L; ++t)
             if (slots[row0 + t] < 0 || slots[row0 + t] >= pool) bad = 1;
         if (bad) { *err |= ERR_SLOT; continue; }
-        const int64_t start = slots[row0 + a - 1];
-
-        /* Step 1+2: split the packed row; causal depthwise conv of the q|k|v
-         * channels against the window of the start slot. */
-        for (int64_t c = 0; c < C; ++c) {
-            for (int64_t j = 0; j < SL; ++j) {
-                int64_t ix = dim_first ? (start * C + c) * SL + j : (start * SL + j) * C + c;
-                window[j] = bf16_value(conv_state[ix]);
-            }
-            for (int64_t t = 0; t < L; ++t) {
-                const double x_t = bf16_value(projected[(row0 + t) * pitch + c]);
-                double y = bias ? bf16_value(bias[c]) : 0.0;
-                for (int64_t j = 0; j < W; ++j) {
-                    const double x = (j < SL) ? window[j] : x_t; /* tap W-1 = current token */
-                    y += bf16_value(conv_w[c * W + j]) * x;
-                }
-                if (act) y = y * sigmoid(y); /* SiLU */
-                qkv[t * C + c] = bf16_rounded(y);
-                /* shift the window by one and store it in this token's slot */
-                for (int64_t j = 0; j + 1 < SL; ++j) window[j] = window[j + 1];
-                if (SL > 0) window[SL - 1] = x_t;
-                const int64_t dst = slots[row0 + t];
-                for (int64_t j = 0; j < SL; ++j) {
-                    int64_t ix = dim_first ? (dst * C + c) * SL + j : (dst * SL + j) * C + c;
-                    conv_state[ix] = bf16_round(window[j]);
-                }
-            }
-        }
-
-        /* Step 3: gates.  z = f_b . f_a (bf16 hand-off), lower-bounded decay, beta. */
-        for (int64_t t = 0; t < L; ++t) {
-            const uint16_t *prow = projected + (row0 + t) * pitch;
-            for (int64_t c = 0; c < D; ++c) {
-                double z = 0.0;
-                for (int64_t j = 0; j < HEAD_DIM; ++j)
-                    z += bf16_value(f_b[c * HEAD_DIM + j]) * bf16_value(prow[4 * D + j]);
-                z = bf16_rounded(z);
-                const int64_t h = c / HEAD_DIM;
-                if (gate_mode == 0)
-                    g[t * D + c] = (double)lb * sigmoid(exp((double)A_log[h]) * (z + (double)dt_bias[c]));
-                else
-                    g[t * D + c] = fmax(-exp((double)A_log[h]) * softplus(z + dt_bias[c]), (double)lb);
-            }
-            for (int64_t h = 0; h < heads; ++h)
-                beta[t * heads + h] = sigmoid(bf16_value(prow[4 * D + HEAD_DIM + h]));
-        }
-
-        for (int64_t h = 0; h < heads; ++h) {
-            /* Start state of (request, head), storage [v][k] -> S[k][v]. */
-            const float *src = state_pool + (start * heads + h) * HEAD_DIM * HEAD_DIM;
-            const uint16_t *src16 = (const uint16_t *)state_pool + (start * heads + h) * HEAD_DIM * HEAD_DIM;
-            for (int v = 0; v < HEAD_DIM; ++v)
-                for (int k = 0; k < HEAD_DIM; ++k) {
-                    if (state_bf16) S[k * HEAD_DIM + v] = bf16_value(src16[v * HEAD_DIM + k]);
-                    else S[k * HEAD_DIM + v] = (double)src[v * HEAD_DIM + k];
-                }
-
-            for (int64_t t = 0; t < L; ++t) {
-                const double *qr = qkv + t * C + h * HEAD_DIM;
-                const double *kr = qkv + t * C + D + h * HEAD_DIM;
-                const double *vr = qkv + t * C + 2 * D + h * HEAD_DIM;
-                const double *gr = g + t * D + h * HEAD_DIM;
-                const double b = beta[t * heads + h];
-
-                /* Step 4: L2 normalisation of q and k, q scaled by 128^-0.5. */
-                double qq = 0.0, kk = 0.0;
-                for (int i = 0; i < HEAD_DIM; ++i) { qq += qr[i] * qr[i]; kk += kr[i] * kr[i]; }
-                const double qn = 1.0 / sqrt(qq + 1e-6), kn = 1.0 / sqrt(kk + 1e-6);
-                double qh[HEAD_DIM], kh[HEAD_DIM], o[HEAD_DIM], u[HEAD_DIM];
-                for (int i = 0; i < HEAD_DIM; ++i) { qh[i] = qr[i] * qn * q_scale; kh[i] = kr[i] * kn; }
-
-                /* Step 5: gated delta rule.  S <- diag(e^g) S;  u = v - S^T k^;
-                 * S <- S + beta k^ u^T;  o = S^T q^ (the updated state). */
-                for (int k = 0; k < HEAD_DIM; ++k) {
-                    const double decay = exp(gr[k]);
-                    for (int v = 0; v < HEAD_DIM; ++v) S[k * HEAD_DIM + v] *= decay;
-                }
-                for (int v = 0; v < HEAD_DIM; ++v) {
-                    double s = 0.0;
-                    for (int k = 0; k < HEAD_DIM; ++k) s += S[k * HEAD_DIM + v] * kh[k];
-                    u[v] = vr[v] - s;
-                }
-                for (int k = 0; k < HEAD_DIM; ++k)
-                    for (int v = 0; v < HEAD_DIM; ++v) S[k * HEAD_DIM + v] += b * kh[k] * u[v];
-                for (int v = 0; v < HEAD_DIM; ++v) {
-                    double s = 0.0;
-                    for (int k = 0; k < HEAD_DIM; ++k) s += S[k * HEAD_DIM + v] * qh[k];
-                    o[v] = bf16_rounded(s); /* bf16 hand-off into the norm */
-                }
-                /* one state written per token, into slots[r, t] */
-                float *dst = state_pool + ((int64_t)slots[row0 + t] * heads + h) * HEAD_DIM * HEAD_DIM;
-                uint16_t *dst16 = (uint16_t *)state_pool + ((int64_t)slots[row0 + t] * heads + h) * HEAD_DIM * HEAD_DIM;
-                for (int v = 0; v < HEAD_DIM; ++v)
-                    for (int k = 0; k < HEAD_DIM; ++k) {
-                        if (state_bf16) dst16[v * HEAD_DIM + k] = bf16_round(S[k * HEAD_DIM + v]);
-                        else dst[v * HEAD_DIM + k] = (float)S[k * HEAD_DIM + v];
-                    }
-
-                /* Step 6: gated RMSNorm over the head's 128 -> bf16 core_out. */
-                double ms = 0.0;
-                for (int v = 0; v < HEAD_DIM; ++v) ms += o[v] * o[v];
-                ms /= HEAD_DIM;
-                const double rstd = 1.0 / sqrt(ms + (double)eps);
-                const uint16_t *gate = projected + (row0 + t) * pitch + 3 * D + h * HEAD_DIM;
-                for (int v = 0; v < HEAD_DIM; ++v) {
-                    const double y = o[v] * rstd * (double)o_norm[v] * sigmoid(bf16_value(gate[v]));
-                    out[(row0 + t) * D + h * HEAD_DIM + v] = bf16_round(y);
-                }
-
-                if (diag) {
-                    double *dg = diag + ((row0 + t) * heads + h) * DIAG;
-                    for (int i = 0; i < HEAD_DIM; ++i) {
-                        dg[i] = qh[i];
-                        dg[HEAD_DIM + i] = kh[i];
-                        dg[2 * HEAD_DIM + i] = vr[i];
-                        dg[3 * HEAD_DIM + i] = gr[i];
-                        dg[4 * HEAD_DIM + i] = o[i];
-                    }
-                    dg[5 * HEAD_DIM] = b;
-                }
-            }
-        }
+        start_of[r] = slots[row0 + acc - 1];
     }
-    free(qkv); free(g); free(beta); free(S); free(window);
-    return 0;
+
+    /* Steps 2-6, one task per (request, head). */
+    const int64_t tasks = R * heads;
+    int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(threads) reduction(| : failed)
+#endif
+    {
+        TaskBuf b;
+        b.qkv = malloc(sizeof(double) * (size_t)(L * 3 * HEAD_DIM));
+        b.g = malloc(sizeof(double) * (size_t)(L * HEAD_DIM));
+        b.beta = malloc(sizeof(double) * (size_t)L);
+        b.S = malloc(sizeof(double) * HEAD_DIM * HEAD_DIM);
+        b.window = malloc(sizeof(double) * (size_t)W);
+        const int ok = b.qkv && b.g && b.beta && b.S && b.window;
+        if (!ok) failed = 1;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t k = 0; k < tasks; ++k) {
+            const int64_t r = k / heads, h = k % heads;
+            if (ok && start_of[r] >= 0) run_task(&a, r, h, start_of[r], &b);
+        }
+        free(b.qkv); free(b.g); free(b.beta); free(b.S); free(b.window);
+    }
+    free(start_of);
+    return failed ? -1 : 0;
 }

@@ -24,28 +24,28 @@ MUTATIONS = [
     ("readout_with_k", "for (int k = 0; k < HEAD_DIM; ++k) s += S[k * HEAD_DIM + v] * qh[k];",
      "for (int k = 0; k < HEAD_DIM; ++k) s += S[k * HEAD_DIM + v] * kh[k];"),
     ("readout_before_update", "for (int k = 0; k < HEAD_DIM; ++k) s += S[k * HEAD_DIM + v] * qh[k];",
-     "for (int k = 0; k < HEAD_DIM; ++k) s += (S[k * HEAD_DIM + v] - b * kh[k] * u[v]) * qh[k];"),
-    ("beta_dropped", "S[k * HEAD_DIM + v] += b * kh[k] * u[v];", "S[k * HEAD_DIM + v] += kh[k] * u[v];"),
+     "for (int k = 0; k < HEAD_DIM; ++k) s += (S[k * HEAD_DIM + v] - bt * kh[k] * u[v]) * qh[k];"),
+    ("beta_dropped", "S[k * HEAD_DIM + v] += bt * kh[k] * u[v];", "S[k * HEAD_DIM + v] += kh[k] * u[v];"),
     ("tap_order_reversed", "y += bf16_value(conv_w[c * W + j]) * x;",
      "y += bf16_value(conv_w[c * W + (W - 1 - j)]) * x;"),
     ("window_newest_first", "if (SL > 0) window[SL - 1] = x_t;", "if (SL > 0) window[0] = x_t;"),
-    ("start_slot_first", "const int64_t start = slots[row0 + a - 1];", "const int64_t start = slots[row0];"),
-    ("window_slot_first", "const int64_t dst = slots[row0 + t];", "const int64_t dst = slots[row0];"),
+    ("start_slot_first", "start_of[r] = slots[row0 + acc - 1];", "start_of[r] = slots[row0];"),
+    ("window_slot_first", "const int64_t dst = a->slots[row0 + t];", "const int64_t dst = a->slots[row0];"),
     ("q_scale_dropped", "qh[i] = qr[i] * qn * q_scale;", "qh[i] = qr[i] * qn;"),
-    ("gate_dt_sign", "(z + (double)dt_bias[c])", "(z - (double)dt_bias[c])"),
+    ("gate_dt_sign", "(z + (double)a->dt_bias[c])", "(z - (double)a->dt_bias[c])"),
     ("gate_bound_ignored", "(double)lb * sigmoid(", "-1.0 * sigmoid("),
-    ("softplus_gate_unclamped", "softplus(z + dt_bias[c]), (double)lb)", "softplus(z + dt_bias[c]), -1e300)"),
-    ("softplus_gate_no_scale", "fmax(-exp((double)A_log[h]) * softplus(", "fmax(-1.0 * softplus("),
+    ("softplus_gate_unclamped", "softplus(z + a->dt_bias[c]), (double)lb)", "softplus(z + a->dt_bias[c]), -1e300)"),
+    ("softplus_gate_no_scale", "fmax(-exp((double)a->A_log[h]) * softplus(", "fmax(-1.0 * softplus("),
     ("bf16_state_truncated", "dst16[v * HEAD_DIM + k] = bf16_round(S[k * HEAD_DIM + v]);",
      "dst16[v * HEAD_DIM + k] = (uint16_t)(bf16_round(S[k * HEAD_DIM + v]) & 0xFFFEu);"),
     ("bf16_state_transposed", "bf16_value(src16[v * HEAD_DIM + k])", "bf16_value(src16[k * HEAD_DIM + v])"),
-    ("gate_one_token", "const double *gr = g + t * D + h * HEAD_DIM;", "const double *gr = g + h * HEAD_DIM;"),
+    ("gate_one_token", "const double *gr = b->g + t * HEAD_DIM;", "const double *gr = b->g;"),
     ("rms_sum_not_mean", "ms /= HEAD_DIM;", "ms /= 1;"),
-    ("rms_eps_dropped", "const double rstd = 1.0 / sqrt(ms + (double)eps);", "const double rstd = 1.0 / sqrt(ms);"),
-    ("silu_dropped", "if (act) y = y * sigmoid(y);", "if (act) y = y;"),
+    ("rms_eps_dropped", "const double rstd = 1.0 / sqrt(ms + a->eps);", "const double rstd = 1.0 / sqrt(ms);"),
+    ("silu_dropped", "if (a->act) y = y * sigmoid(y);", "if (a->act) y = y;"),
     ("bias_ignored", "double y = bias ? bf16_value(bias[c]) : 0.0;", "double y = 0.0;"),
-    ("beta_of_head0", "beta[t * heads + h] = sigmoid(bf16_value(prow[4 * D + HEAD_DIM + h]));",
-     "beta[t * heads + h] = sigmoid(bf16_value(prow[4 * D + HEAD_DIM]));"),
+    ("beta_of_head0", "b->beta[t] = sigmoid(bf16_value(prow[4 * D + HEAD_DIM + h]));",
+     "b->beta[t] = sigmoid(bf16_value(prow[4 * D + HEAD_DIM]));"),
     ("out_gate_dropped", "* sigmoid(bf16_value(gate[v]));", ";"),
     ("padding_not_detected", "if (slots[row0] == -1) {", "if (0) {"),
     ("fb_transposed", "bf16_value(f_b[c * HEAD_DIM + j])", "bf16_value(f_b[j * D + c])"),

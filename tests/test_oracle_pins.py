@@ -505,3 +505,22 @@ def test_c_matches_numpy_on_random_shapes():
         fin = ~np.isnan(bf16_value(b16[2]))
         assert np.array_equal(np.isnan(bf16_value(a16[2])), ~fin)
         assert np.mean(a16[2][fin] != b16[2][fin]) < 1e-4
+
+
+def test_threaded_oracle_equals_serial():
+    """The C oracle's OpenMP path over (request, head) tasks gives the same bits
+    as one thread: every task runs its steps in the same order either way."""
+    n = max(2, oracle.max_threads())
+    for trial, (H, R, L) in enumerate([(3, 4, 1), (2, 5, 3), (4, 3, 8)]):
+        si = case(heads=H, requests=R, L=L, pool=R * L + 3, seed=200 + trial, with_bias=bool(trial % 2),
+                  verify=L > 1)
+        W = oracle_weights(si)
+        for sd in ("f32", "bf16"):
+            pool = si.full_state_pool_bf16() if sd == "bf16" else si.full_state_pool()
+            args = (W, si.projected, si.full_conv_state(), pool, si.slots, L, si.accepted)
+            a = oracle.step(*args, state_dtype=sd, diag=True, threads=1)
+            b = oracle.step(*args, state_dtype=sd, diag=True, threads=n)
+            assert a[3] == b[3] == 0
+            assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+            assert np.array_equal(a[2].view(np.uint8), b[2].view(np.uint8))
+            assert np.array_equal(a[4].view(np.uint64), b[4].view(np.uint64))
