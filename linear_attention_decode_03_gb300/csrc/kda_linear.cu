@@ -123,22 +123,6 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, in
       "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(bar), "l"(policy)
       : "memory");
 }
-// As tma_box, written to the same offset (and completing on the same mbarrier
-// offset) in every CTA of the cluster whose bit is set in `mask`.
-__device__ __forceinline__ void tma_box_multicast(uint32_t dst, const CUtensorMap* map, int k, int row, uint32_t bar,
-                                                  uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(bar), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
 __device__ __forceinline__ unsigned cluster_ctarank() {
   unsigned r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -169,15 +153,14 @@ __device__ __forceinline__ float4 ld_peer_f32x4(const float* local, unsigned ran
                : "r"(remote));
   return v;
 }
-// Sum of the `split` CTAs' four floats at `local` (CTA ranks q * stride + offset,
-// q < split), in rank order; every load is issued before the first add, so the
-// distributed-shared-memory round trips overlap.
-__device__ __forceinline__ float4 cluster_sum4(const float* local, unsigned split, unsigned stride = 1,
-                                               unsigned offset = 0) {
+// Sum of the `split` CTAs' four floats at `local` (CTA ranks q < split), in
+// rank order; every load is issued before the first add, so the distributed-
+// shared-memory round trips overlap.
+__device__ __forceinline__ float4 cluster_sum4(const float* local, unsigned split) {
   float4 t[LIN_MAX_SPLIT];
 #pragma unroll
   for (int q = 0; q < LIN_MAX_SPLIT; ++q)
-    t[q] = (unsigned)q < split ? ld_peer_f32x4(local, q * stride + offset) : make_float4(0.f, 0.f, 0.f, 0.f);
+    t[q] = (unsigned)q < split ? ld_peer_f32x4(local, q) : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 v = t[0];
 #pragma unroll
   for (int q = 1; q < LIN_MAX_SPLIT; ++q) {
@@ -369,11 +352,8 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
 // through distributed shared memory.  The operand bytes out of L2 (about
 // 8 TB/s for TMA reads on this part, the same for 100 or 152 reading SMs)
 // bound these tiles as much as the tensor pipe does, so the tile is as wide as
-// one MMA allows (x : W bytes = 1 : 2) and, with two or more row tiles, CTAs
-// come in pairs (two row tiles, one column tile) inside the cluster: each
-// loads half the 256-row weight box and multicasts it to both, so the pair
-// reads the weight from L2 once.  A slot is refilled only when both CTAs' MMAs
-// are done with it: every MMA group commits to the empty barriers of both.
+// one MMA allows (x : W bytes = 1 : 2).  Every CTA loads its own weight boxes:
+// the copies only ever read this GPU's memory through the caller's tensor maps.
 constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4, TC_THREADS = 128;
 constexpr int TC_ABYTES = TC_BM * 128, TC_BBYTES = TC_BN * 128;  // one 64-k box each
 constexpr int TC_STAGE = TC_ABYTES + TC_BBYTES;
@@ -407,7 +387,7 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
 
 __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __grid_constant__ CUtensorMap tmx,
                                                                     const __grid_constant__ CUtensorMap tmw,
-                                                                    const LinArgs a, int tiles_n, int pair) {
+                                                                    const LinArgs a, int tiles_n) {
   extern __shared__ __align__(128) unsigned char tsmem[];
   const uint32_t raw = smem_addr(tsmem);
   const uint32_t ring = (raw + 1023u) & ~1023u;
@@ -418,13 +398,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   volatile uint32_t* tmem_slot_p = reinterpret_cast<volatile uint32_t*>(ring_p + (tmem_slot - ring));
   volatile int* consumed_p = reinterpret_cast<volatile int*>(ring_p + (tmem_slot - ring) + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // cluster = pair x split CTAs: rank = kc * pair + p (p: row tile within the pair, kc: K part)
-  const unsigned csize = cluster_nctarank(), crank = cluster_ctarank();
-  const unsigned split = csize / (unsigned)pair, p = crank % (unsigned)pair, rank = crank / (unsigned)pair;
+  // cluster = the split CTAs of one output tile: rank = K part
+  const unsigned split = cluster_nctarank(), rank = cluster_ctarank();
   const long long grp = cluster_id_x();
-  const long long m0 = ((grp / tiles_n) * pair + p) * TC_BM, n0 = (grp % tiles_n) * TC_BN;
-  const uint16_t pair_mask = (uint16_t)(((1u << pair) - 1u) << (rank * (unsigned)pair));
-  const int wpart = TC_BN / pair;  // weight rows a CTA copies (and multicasts to its pair)
+  const long long m0 = (grp / tiles_n) * TC_BM, n0 = (grp % tiles_n) * TC_BN;
   const long long total = (a.K + TC_BK - 1) / TC_BK;
   const long long s_begin = total * rank / split;
   const long long stages = total * (rank + 1) / split - s_begin;
@@ -434,7 +411,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
     for (int i = 0; i < TC_STAGES; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, (unsigned)pair);  // both CTAs of a pair release a slot
+      mbar_init(empty0 + 8 * i, 1);
     }
     mbar_init(accum_bar, 1);
     *consumed_p = 0;
@@ -447,8 +424,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  // a pair's barriers are initialised before either CTA copies into or signals the other
-  if (pair > 1) cluster_sync();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot_p;
   // As a programmatic dependent (a layer plan's o_proj) the set-up above
@@ -477,22 +452,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
       if (lane == 0) {
         const uint32_t st = ring + slot * TC_STAGE, bar = full0 + 8 * slot;
         const int k = (int)((s_begin + s) * TC_BK);
-        mbar_expect_tx(bar, TC_STAGE);  // x, this CTA's weight part and the partner's
+        mbar_expect_tx(bar, TC_STAGE);  // the x box and the weight box
         tma_box(st, &tmx, k, (int)m0, bar, x_policy);
-        if (pair > 1)
-          tma_box_multicast(st + TC_ABYTES + p * wpart * 128, &tmw, k, (int)(n0 + p * wpart), bar, pair_mask);
-        else
-          tma_box(st + TC_ABYTES, &tmw, k, (int)n0, bar, w_policy);
+        tma_box(st + TC_ABYTES, &tmw, k, (int)n0, bar, w_policy);
       }
       __syncwarp();
       issued = s + 1;
     }
-    // a pair: the last releases of this CTA's slots (its own MMAs' and the partner's) have
-    // arrived before it goes on, so nothing signals its barriers after it exits
-    if (pair > 1 && ok_all)
-      for (long long q = issued > TC_STAGES ? issued - TC_STAGES : 0; q < issued; ++q)
-        if (!mbar_wait_bounded(empty0 + 8 * (uint32_t)(q % TC_STAGES), (unsigned)((q / TC_STAGES) & 1)))
-          ok_all = false;
   } else if (warp == 1) {  // MMA issuer
     long long s = 0;
     for (; s < stages; ++s) {
@@ -516,17 +482,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
               "l"(da), "l"(db), "r"(TC_IDESC), "r"(acc)
               : "memory");
         }
-        // the slot is free (in this CTA and, for a pair, in the partner) once these MMAs have read it
-        if (pair > 1)
-          asm volatile(
-              "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                  empty0 + 8 * slot),
-              "h"(pair_mask)
-              : "memory");
-        else
-          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 +
-                                                                                                         8 * slot)
-                       : "memory");
+        // the slot is free once these MMAs have read it
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 +
+                                                                                                       8 * slot)
+                     : "memory");
       }
       __syncwarp();
     }
@@ -598,7 +557,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
     }
-    if (pair > 1) cluster_sync();  // the partner is done with this CTA's barriers
     return;
   }
   // K split: accumulator -> shared memory (row-major, padded), 32 columns a load; rows past `rows` are not needed
@@ -640,7 +598,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   const int e_end = (int)((long long)E * (rank + 1) / split);
   for (int e = (int)((long long)E * rank / split) + threadIdx.x; e < e_end; e += TC_THREADS) {
     const int rr = e / CQ, cq = e % CQ;
-    const float4 v4 = cluster_sum4(red + rr * TC_RED_LD + 4 * cq, split, (unsigned)pair, p);
+    const float4 v4 = cluster_sum4(red + rr * TC_RED_LD + 4 * cq, split);
     const long long n = n0 + 4 * cq;
     __nv_bfloat16* yr = a.y + (m0 + rr) * a.ldy;
     if (a.y_vec8 && n + 4 <= a.N) {
@@ -659,6 +617,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
 }
 
 bool lin_aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+// True when p is device memory of the current device: the tensor maps and the
+// stores of these kernels address this GPU's own memory only.
+bool on_current_device(const void* p) {
+  int dev = 0;
+  cudaPointerAttributes at;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear a lookup failure (an unknown host pointer) from the thread's error state
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -765,11 +735,9 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
 
 int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl) {
   const long long tiles_m = (a.M + TC_BM - 1) / TC_BM, tiles_n = (a.N + TC_BN - 1) / TC_BN;
-  // two or more row tiles: CTAs in pairs that share (multicast) the weight box
-  const int pair = tiles_m >= 2 ? 2 : 1;
-  const long long groups = ((tiles_m + pair - 1) / pair) * tiles_n;  // clusters of one K part
+  const long long groups = tiles_m * tiles_n;  // output tiles: clusters of one K part
   CUtensorMap tmx, tmw;
-  if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, TC_BN / pair))
+  if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, TC_BN))
     return KDA_ECUDA;
   if (cudaFuncSetAttribute(kda_linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM) !=
       cudaSuccess)
@@ -792,8 +760,8 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
   const long long stages = (a.K + TC_BK - 1) / TC_BK;
   long long split = 1;
   double best = 1e300;
-  for (int c = 1; c * pair <= LIN_MAX_SPLIT && c <= stages; ++c) {
-    const int cs = c * pair;  // cluster size
+  for (int c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
+    const int cs = c;  // cluster size
     int held = dev < 64 ? cluster_cache[dev][cs].load(std::memory_order_relaxed) : 0;
     if (held <= 0) {
       int sms = 0, per_sm = 0;
@@ -818,11 +786,11 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
     const double cost = waves * ((double)stages / c) + TC_FIXED_STAGES + (c > 1 ? TC_REDUCE_STAGES : 0.0);
     if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
   }
-  if (groups * pair * split > 0x7fffffffLL) return KDA_EINVAL;
-  cfg.gridDim = dim3((unsigned)(groups * pair * split), 1, 1);
-  attr[0].val.clusterDim.x = (unsigned)(pair * split);
+  if (groups * split > 0x7fffffffLL) return KDA_EINVAL;
+  cfg.gridDim = dim3((unsigned)(groups * split), 1, 1);
+  attr[0].val.clusterDim.x = (unsigned)split;
   cfg.numAttrs = pdl ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel, tmx, tmw, a, (int)tiles_n, pair) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel, tmx, tmw, a, (int)tiles_n) != cudaSuccess)
     return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
@@ -837,6 +805,7 @@ int kda_linear_enqueue(const void* x, long long rows, long long ldx, const void*
   // tensor maps: 16-byte aligned bases and row strides; coordinates fit 32 bits
   if (!lin_aligned(x, 16) || !lin_aligned(w, 16) || (ldx % 8) != 0 || !lin_aligned(y, 2)) return KDA_EINVAL;
   if (K > 0x7fffffffLL || N > 0x7fffffffLL || rows > 0x7fffffffLL) return KDA_EINVAL;
+  if (!on_current_device(x) || !on_current_device(w) || !on_current_device(y)) return KDA_EINVAL;
   // rows <= 16: the one-tile mma.sync shape (the bytes are the weight);
   // beyond: tcgen05 tiles (at 64 rows they beat 64 x 128 mma.sync tiles,
   // 30.8 against 35.8 us for the 12-head in_proj, although half their x box

@@ -81,3 +81,24 @@ def test_rejects_bad_shapes():
     w = torch.zeros((8, 100), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(kda.KdaError):
         kda.linear(x, w)  # K = 100: weight rows of 200 bytes, not a multiple of 16
+
+
+def test_host_memory_rejected():
+    """kda_linear reads x and W through tensor maps and writes y with plain
+    stores, on this GPU's own memory only: pinned or pageable host buffers,
+    for any operand, are rejected with KDA_EINVAL before anything is enqueued."""
+    rows, K, N = 4, 256, 64
+    xd = torch.zeros((rows, K), dtype=torch.bfloat16, device="cuda")
+    wd = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+    yd = torch.zeros((rows, N), dtype=torch.bfloat16, device="cuda")
+    for host in (torch.zeros((rows * N + N * K,), dtype=torch.bfloat16).pin_memory(),
+                 torch.zeros((rows * N + N * K,), dtype=torch.bfloat16)):
+        hp = host.data_ptr()
+        for args in ((hp, wd.data_ptr(), yd.data_ptr()), (xd.data_ptr(), hp, yd.data_ptr()),
+                     (xd.data_ptr(), wd.data_ptr(), hp)):
+            x, w, y = args
+            with pytest.raises(kda.KdaError) as ei:
+                kda.kda_linear(x, rows, K, w, N, K, y, N)
+            assert ei.value.code == -1
+    kda.linear(xd, wd, yd)
+    assert kda.kda_linear_check() == 0
