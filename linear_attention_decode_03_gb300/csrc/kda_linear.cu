@@ -123,6 +123,12 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, in
       "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(bar), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
 __device__ __forceinline__ unsigned cluster_ctarank() {
   unsigned r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -93,7 +93,7 @@ class DeviceStep:
         self.prep.close()
 
 
-def oracle_requests(si: I.StepInputs, reqs, dim_first=True, gate_mode=0, state_dtype="f32"):
+def oracle_requests(si: I.StepInputs, reqs, dim_first=True, gate_mode=0, state_dtype="f32", threads=1):
     """The C oracle on requests `reqs` only, with a pool compacted to the slots
     they touch.  Returns (out rows, used slots, pool [n_used], conv [n_used], err)."""
     w = si.workload
@@ -124,7 +124,7 @@ def oracle_requests(si: I.StepInputs, reqs, dim_first=True, gate_mode=0, state_d
     if not dim_first:
         cconv = np.ascontiguousarray(cconv.transpose(0, 2, 1))
     out, nconv, npool, err = oracle.step(W, si.projected[rows], cconv, cpool, cslots, L, acc, dim_first=dim_first,
-                                         gate_mode=gate_mode, state_dtype=state_dtype)
+                                         gate_mode=gate_mode, state_dtype=state_dtype, threads=threads)
     return out, rows, used, npool[: len(used)], nconv[: len(used)], err
 
 
@@ -170,3 +170,28 @@ def assert_state_close(gpu: np.ndarray, ref: np.ndarray):
     print(f"state max-abs diff {diff.max():.3e}")
     assert diff.max() <= STATE_ATOL, f"state max-abs diff {diff.max()}"
     assert diff.max() <= STATE_ATOL_TIGHT, f"state max-abs diff {diff.max()} (a bf16 hand-off flipped?)"
+
+
+def compare_streamed(ds: "DeviceStep", si: I.StepInputs, chunk: int = 8, threads: int = 0):
+    """Compare every request of a step that ran on the device with the oracle,
+    `chunk` requests at a time, so that host memory holds only those requests'
+    caches (a 96-head request at L = 8 touches 8 slots x 96 heads x 64 KiB).
+    threads = 0: all the oracle's threads."""
+    w = si.workload
+    th = threads or oracle.max_threads()
+    worst = 0.0
+    for r0 in range(0, w.requests, chunk):
+        reqs = np.arange(r0, min(r0 + chunk, w.requests))
+        out_ref, rows, used, pool_ref, conv_ref, err = oracle_requests(si, reqs, threads=th)
+        assert err == 0
+        out = torch_bf16_to_np(ds.out[torch.from_numpy(rows).to(ds.device)])
+        assert_out_close(out, out_ref)
+        uidx = torch.from_numpy(used).to(ds.device)
+        st = ds.state[uidx].cpu().numpy()
+        assert np.isfinite(st).all()
+        d = float(np.abs(st.astype(np.float64) - pool_ref.astype(np.float64)).max())
+        worst = max(worst, d)
+        assert d <= STATE_ATOL_TIGHT, f"requests {r0}..: state max-abs diff {d}"
+        assert np.array_equal(torch_bf16_to_np(ds.conv[uidx]), conv_ref)
+    print(f"streamed parity over {w.requests} requests: state max-abs diff {worst:.3e}")
+    return worst

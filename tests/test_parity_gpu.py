@@ -72,15 +72,24 @@ def test_large_decode_full_parity():
     _check_full(I.make_step_inputs(I.WORKLOADS["large_decode"]))
 
 
-def test_full_width_verify_sampled_parity():
+def test_full_width_verify_full_parity():
     """96 heads, R = 128 x L = 8 on a 2048-slot pool (12.9 GB of state): the
-    whole step runs on the GPU; 6 requests (chosen to cover every accepted
-    value present) are recomputed by the oracle; the untouched slots of the
-    whole pool are checked on the device."""
+    whole step runs on the GPU and every request is recomputed by the oracle,
+    streamed 8 requests at a time so that host memory holds one chunk's
+    caches; the untouched slots of the whole pool are checked on the device."""
     si = I.make_step_inputs(I.WORKLOADS["full_width_verify"])
-    rng = np.random.default_rng(0)
-    reqs = sorted(set([0, si.workload.requests - 1] + list(rng.choice(si.workload.requests, 4, replace=False))))
-    _check_full(si, reqs=np.array(reqs))
+    w = si.workload
+    ds = G.DeviceStep(si)
+    assert ds.run() == 0
+    G.compare_streamed(ds, si, chunk=8)
+    written = np.zeros(w.pool, dtype=bool)
+    written[si.slots[si.slots >= 0]] = True
+    untouched = torch.from_numpy(np.nonzero(~written)[0]).to(ds.device)
+    st = ds.state[untouched].view(torch.int32)
+    assert bool((st == int(I.STATE_SENTINEL.view(np.int32))).all())
+    cv = ds.conv[untouched].view(torch.int16)
+    assert bool((cv == int(np.array(I.CONV_SENTINEL).view(np.int16))).all())
+    ds.close()
 
 
 @pytest.mark.parametrize("L", [1, 2, 3, 5, 6, 7, 8])
