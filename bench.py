@@ -5,15 +5,22 @@ decode, B = 512 rows x 12 heads x 128, conv width 4, a 1024-slot pool;
 805 MB of fp32 state read and written per step, larger than L2).
 
 Prints ONE JSON line:
-  value      tokens/s with every input resident in HBM (CUDA events on the
-             launching stream, around exactly --steps steps)
+  value      tokens/s with every input resident in HBM: blocks of exactly
+             --steps steps (CUDA events on the launching stream) repeated
+             until --min-timed-s seconds of timed work; ms_per_step is the
+             median block
   e2e        the same metric through the public API with host buffers:
              each step copies its projected rows, slots (and accepted) from
              pinned host memory and reads `out` back
   roofline   the step kernel's algorithmic bytes / its average launch time
              against the measured HBM copy bandwidth
-  cpu_baseline  the CPU oracle (plain fp64 C, 1 thread) on a bounded sample
-             of the same workload
+  per_workload  the other workloads (tiny decode, batched decode, spec-verify,
+             full-width verify), each timed the same way in the same process:
+             step time, tokens/s, and the fractions of the HBM peak for the
+             state bytes and for all algorithmic bytes
+  cpu_baseline  the CPU oracle (plain fp64 C) on a bounded sample of the same
+             workload, on every host core (OpenMP over (request, head)) and on
+             one thread (one_thread)
   clocks     nvidia-smi samples taken during the timed region
 
 `--impl reference` times the CPU oracle as the reference arm instead.
@@ -242,8 +249,16 @@ def oracle_sample_inputs(si: I.StepInputs, reqs, state_dtype: str = "f32"):
     return si.projected[rows], cconv, cpool, cslots, acc
 
 
-def time_oracle(si: I.StepInputs, n_requests: int, repeats: int = 1, state_dtype: str = "f32"):
-    """Seconds per token of the C oracle over `n_requests` requests (1 thread)."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def time_oracle(si: I.StepInputs, n_requests: int, repeats: int = 1, state_dtype: str = "f32", threads: int = 1):
+    """Seconds and tokens of the C oracle over the first `n_requests` requests,
+    `repeats` passes, on `threads` OpenMP threads over (request, head)."""
     import oracle
 
     W = oracle.Weights(**si.weights.as_dict())
@@ -251,39 +266,62 @@ def time_oracle(si: I.StepInputs, n_requests: int, repeats: int = 1, state_dtype
     proj, cconv, cpool, cslots, acc = oracle_sample_inputs(si, reqs, state_dtype)
     t0 = time.perf_counter()
     for _ in range(repeats):
-        oracle.step(W, proj, cconv, cpool, cslots, si.workload.L, acc, state_dtype=state_dtype)
+        oracle.step(W, proj, cconv, cpool, cslots, si.workload.L, acc, state_dtype=state_dtype, threads=threads)
     dt = time.perf_counter() - t0
     return dt, len(reqs) * si.workload.L * repeats
 
 
-def cpu_baseline(si: I.StepInputs, budget_s: float = 12.0, state_dtype: str = "f32"):
-    """The oracle on a bounded sample of about `budget_s` seconds: as many
-    whole requests (in order) as fit, repeated over the whole batch when the
-    batch alone takes less; estimated from one request."""
-    dt1, tok1 = time_oracle(si, 1, state_dtype=state_dtype)
-    n = int(max(1, min(si.workload.requests, budget_s / max(dt1, 1e-6))))
-    repeats = int(max(1, budget_s / max(dt1 * n, 1e-6)))
-    dt, tok = time_oracle(si, n, repeats, state_dtype)
-    return {"value": tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {n} of {si.workload.requests} requests of the {si.workload.name} workload "
-                      f"x {repeats} passes ({tok} tokens x {si.workload.heads} heads), fp64 C oracle, "
-                      f"1 thread, {dt:.1f} s"}
+def oracle_sample_size(si: I.StepInputs, budget_s: float, state_dtype: str, threads: int):
+    """Whole requests (in order) whose oracle pass takes about `budget_s`,
+    measured on a calibration pass of enough requests to give every thread a
+    (request, head) task; and the passes that fill the budget."""
+    w = si.workload
+    n0 = min(w.requests, max(1, -(-threads // w.heads)))
+    dt0, _ = time_oracle(si, n0, state_dtype=state_dtype, threads=threads)
+    n = int(max(1, min(w.requests, n0 * budget_s / max(dt0, 1e-6))))
+    repeats = int(max(1, budget_s / max(dt0 * n / n0, 1e-6)))
+    return n, repeats
+
+
+def cpu_baseline(si: I.StepInputs, budget_s: float = 10.0, state_dtype: str = "f32"):
+    """The oracle on a bounded sample of the workload (about `budget_s` of CPU
+    work each): on every host core (OpenMP over (request, head); the
+    headline), and on one thread."""
+    import oracle
+
+    w = si.workload
+    res = {}
+    for threads in sorted({host_cores(), 1}, reverse=True):
+        used = min(threads, oracle.max_threads()) if threads > 1 else 1
+        n, repeats = oracle_sample_size(si, budget_s, state_dtype, used)
+        dt, tok = time_oracle(si, n, repeats, state_dtype, used)
+        res[used] = {"value": tok / dt, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                     "sample": f"first {n} of {w.requests} requests of the {w.name} workload x {repeats} passes "
+                               f"({tok} tokens x {w.heads} heads), fp64 C oracle, {used} thread(s), {dt:.1f} s"}
+    top = res[max(res)]
+    if 1 in res and max(res) != 1:
+        top = dict(top, one_thread=res[1])
+    return top
 
 
 def run_reference(args, w: I.Workload):
+    """The reference arm: the oracle, as it stands, on every host core (OpenMP
+    over (request, head)), each step a bounded sample of the workload."""
+    import oracle
+
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     si = I.make_step_inputs(w)
     sd = args.state_dtype
-    dt1, _ = time_oracle(si, 1, state_dtype=sd)
+    threads = min(host_cores(), oracle.max_threads())
     per_step_budget = 150.0 / max(args.steps + args.warmup, 1)
-    n = int(max(1, min(w.requests, per_step_budget / max(dt1, 1e-6))))
+    n, _ = oracle_sample_size(si, per_step_budget, sd, threads)
     for _ in range(args.warmup):
-        time_oracle(si, n, state_dtype=sd)
+        time_oracle(si, n, state_dtype=sd, threads=threads)
     total_t, total_tok = 0.0, 0
     for _ in range(args.steps):
-        dt, tok = time_oracle(si, n, state_dtype=sd)
+        dt, tok = time_oracle(si, n, state_dtype=sd, threads=threads)
         total_t += dt
         total_tok += tok
     value = total_tok / total_t
@@ -292,9 +330,9 @@ def run_reference(args, w: I.Workload):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w, args),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"each step: first {n} of {w.requests} requests of {w.name} "
-                                   f"({n * w.L} tokens x {w.heads} heads), fp64 C oracle, 1 thread"},
+                                   f"({n * w.L} tokens x {w.heads} heads), fp64 C oracle, {threads} thread(s)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -633,6 +671,91 @@ def run_layer(args, w: I.Workload):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- step timing
+MIN_TIMED_S = 0.5
+PER_WORKLOAD = ["tiny_decode", "batched_decode", "spec_verify", "large_decode", "full_width_verify"]
+
+
+def make_flush(device):
+    """Two 256 MiB buffers: writing one and reading the other between timed
+    steps leaves L2 holding neither the step's data nor dirty lines."""
+    import torch
+
+    return (torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device),
+            torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device))
+
+
+def time_blocks(step, steps, stream, flush_bufs, min_s=MIN_TIMED_S):
+    """Blocks of `steps` steps, repeated until `min_s` seconds of timed work.
+    With flush_bufs each step is timed alone (CUDA events on `stream`) after an
+    L2 flush outside the events; otherwise a block is `steps` back-to-back
+    steps between two events (inputs larger than L2).  Returns the ms per step
+    of every block and the single-step times (flushed case only)."""
+    import torch
+
+    blocks, step_ms, total = [], [], 0.0
+    while total < min_s * 1e3 or not blocks:
+        if flush_bufs is not None:
+            fw, fr = flush_bufs
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            for i in range(steps):
+                fw.fill_(float(i))
+                fr.sum()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+            ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+            step_ms.extend(ms)
+            block = sum(ms)
+        else:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            block = e0.elapsed_time(e1)
+        blocks.append(block / steps)
+        total += block
+    return blocks, step_ms
+
+
+def measure_workload(w: I.Workload, device, args):
+    """One more workload in the same process: step time (median block), tokens/s
+    and the fractions of the measured HBM peak, for the state bytes alone and
+    for all algorithmic bytes."""
+    import torch
+
+    si = I.make_step_inputs(w)
+    dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=args.plan,
+                        state_dtype=args.state_dtype)
+    state_b, all_b = algorithmic_bytes(w, args.state_dtype)
+    flush_bufs = make_flush(device) if state_b <= L2_BYTES else None
+    for _ in range(max(args.warmup, 3)):
+        dw.step()
+    if dw.prep.check() != 0:
+        raise RuntimeError(f"device error bits set during warm-up ({w.name})")
+    blocks, step_ms = time_blocks(dw.step, args.steps, torch.cuda.current_stream(device), flush_bufs,
+                                  args.min_timed_s)
+    if dw.prep.check() != 0:
+        raise RuntimeError(f"device error bits set during the timed steps ({w.name})")
+    ms = statistics.median(blocks)
+    peak, _ = load_peaks()
+    rec = {"ms_per_step": ms, "tokens_per_s": w.rows / (ms / 1e3), "rows": w.rows, "heads": w.heads, "L": w.L,
+           "state_bytes_per_step": state_b, "algorithmic_bytes_per_step": all_b,
+           "state_gbs": state_b / (ms / 1e3) / 1e9, "state_frac_of_peak": state_b / (ms / 1e3) / 1e9 / peak,
+           "achieved_gbs": all_b / (ms / 1e3) / 1e9, "frac": all_b / (ms / 1e3) / 1e9 / peak,
+           "blocks": len(blocks), "launches": args.steps * len(blocks),
+           "ms_per_step_median_single_step": statistics.median(step_ms) if step_ms else None,
+           "l2": "inputs larger than L2" if flush_bufs is None else "L2 flushed between timed steps",
+           "traffic": measured_traffic(w.name)}
+    del dw, flush_bufs
+    torch.cuda.empty_cache()
+    return rec
+
+
 # -------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -643,6 +766,11 @@ def main():
     ap.add_argument("--workload", default="large_decode", choices=sorted(I.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
+                    help="blocks of --steps steps are repeated until this much timed work; "
+                         "ms_per_step is the median block")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the other workloads (per_workload) measured after the main one")
     ap.add_argument("--plan", action="store_true",
                     help="launch every step through a launch plan (the step recorded once as a CUDA graph)")
     ap.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32",
@@ -688,15 +816,10 @@ def main():
     kda.load_library()
 
     si = I.make_step_inputs(w)
-    dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=args.plan,
-                        state_dtype=args.state_dtype)
+    gm = 0 if args.gate_mode == "sigmoid" else 1
+    dw = DeviceWorkload(si, device, gate_mode=gm, plan=args.plan, state_dtype=args.state_dtype)
     state_b, all_b = algorithmic_bytes(w, args.state_dtype)
-    flush = state_b <= L2_BYTES
-    # L2 flush between timed steps: write a buffer larger than L2, then read a
-    # second one so that the written lines are back in HBM (clean) before the
-    # step starts instead of being written back during it
-    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device) if flush else None
-    scratch_rd = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device) if flush else None
+    flush_bufs = make_flush(device) if state_b <= L2_BYTES else None
     stream = torch.cuda.current_stream(device)
 
     def barrier():
@@ -714,31 +837,15 @@ def main():
     time.sleep(0.3)
     barrier()
     t_host0 = time.time()
-    if flush:
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        for i in range(args.steps):
-            scratch.fill_(float(i))
-            scratch_rd.sum()
-            starts[i].record(stream)
-            dw.step()
-            ends[i].record(stream)
-        barrier()
-        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-        elapsed_ms = sum(step_ms)
-        median_ms = statistics.median(step_ms)
-    else:
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            dw.step()
-        ev1.record(stream)
-        barrier()
-        elapsed_ms = ev0.elapsed_time(ev1)
-        median_ms = None  # back-to-back steps (inputs larger than L2): one interval, no per-step times
+    blocks, step_ms = time_blocks(dw.step, args.steps, stream, flush_bufs, args.min_timed_s)
+    barrier()
     t_host1 = time.time()
     time.sleep(0.25)
     sampler.stop()
+    # the median block (each block is --steps steps) is the step time; the mean is kept beside it
+    block_ms = statistics.median(blocks)
+    elapsed_ms = block_ms * args.steps
+    median_ms = statistics.median(step_ms) if step_ms else None
     flags = dw.prep.check()
     if flags != 0:
         raise RuntimeError(f"device error bits {flags} during the timed steps")
@@ -824,14 +931,20 @@ def main():
 
     ms_step = elapsed_ms / args.steps
     tokens_per_s = whole_job_rate(world, w.rows, args.steps, elapsed_ms)
+    timing = {"blocks": len(blocks), "steps_per_block": args.steps, "timed_s": sum(blocks) * args.steps / 1e3,
+              "block_ms_per_step_min": min(blocks), "block_ms_per_step_max": max(blocks),
+              "ms_per_step_mean_over_blocks": statistics.mean(blocks),
+              "rule": f"blocks of --steps steps repeated until {args.min_timed_s} s of timed work; "
+                      "ms_per_step = the median block / steps"}
     peak, peak_kind = load_peaks()
     achieved = all_b / (ms_step / 1e3) / 1e9
     state_gbs = state_b / (ms_step / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median": median_ms,
-        "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": workload_config(w, args),
+        "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median_single_step": median_ms,
+        "timing": timing, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if args.state_dtype == "f32" else "f32 compute, bf16 state storage",
+        "data": "synthetic", "config": workload_config(w, args),
         "state_gbs": state_gbs, "state_frac_of_peak": state_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": measured_traffic(w.name), "kernel": "kda_step_kernel",
@@ -841,11 +954,16 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "overlap": "uploads and downloads on streams of their own, two buffer sets; blocks of "
                            f"{E2E_BLOCK} steps recorded as a CUDA graph"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * len(blocks),
         "clocks": sampler.summary(t_host0, t_host1),
     }
     if dist is not None:
         dist.destroy_process_group()
+    if world == 1 and not args.no_per_workload:
+        del dw
+        torch.cuda.empty_cache()
+        line["per_workload"] = {name: measure_workload(I.WORKLOADS[name], device, args)
+                                for name in PER_WORKLOAD if name != w.name}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(si, state_dtype=args.state_dtype)
     print(json.dumps(line), flush=True)

@@ -41,9 +41,11 @@ def build(force: bool = False, verbose: bool = False, debug: bool = False) -> st
     if not force and up_to_date(out):
         return out
     tmp = out + f".tmp{os.getpid()}"
+    # --threads: the translation units compile in parallel (--split-compile, which also
+    # splits a unit's kernels across processes, gives slower step kernels)
     cmd = [nvcc_path(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-cudart", "static", "-I", os.path.join(ROOT, "include"), *(["-DKDA_DEBUG"] if debug else []),
-           "-o", tmp, *SOURCES]
+           "-cudart", "static", "--threads", "0", "-I", os.path.join(ROOT, "include"),
+           *(["-DKDA_DEBUG"] if debug else []), "-o", tmp, *SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     res = subprocess.run(cmd, capture_output=True, text=True)

@@ -274,13 +274,6 @@ __device__ __forceinline__ float bf16_round_pair(float hi, float lo) {
   return ((e > 0.0f) == (s > 0.0f)) ? up : down;
 }
 
-// Element (slot, ch, j) of the conv cache is at conv_base + j * conv_step.
-__device__ __forceinline__ long long conv_base(const StepArgs& a, long long slot, int ch) {
-  const long long C = 3LL * a.D;
-  const int SL = a.W - 1;
-  return a.conv_dim_first ? (slot * C + ch) * SL : slot * SL * C + ch;
-}
-__device__ __forceinline__ long long conv_step(const StepArgs& a) { return a.conv_dim_first ? 1 : 3LL * a.D; }
 
 
 // Wait for phase `parity` of an mbarrier, giving up after WAIT_LIMIT_CYCLES SM
@@ -441,7 +434,8 @@ __device__ __forceinline__ float silu_bf16_exact(float b, unsigned wp0, unsigned
   return bf16_round_f64(yd * __drcp_rn(1.0 + exp(-yd)));  // y / (1 + e^-y) within 2 fp64 ulp
 }
 // The same out of line: with many tokens the unrolled conv is long enough for
-// instruction fetch to matter, and the rare path is better kept out of it.
+// instruction fetch to matter, and the rare path is better kept out of it (up
+// to four tokens the call's register saves cost more than the fetch).
 __device__ __noinline__ float silu_bf16_exact_ool(float b, unsigned wp0, unsigned wp1, unsigned s01, unsigned s23) {
   return silu_bf16_exact(b, wp0, wp1, s01, s23);
 }
@@ -481,7 +475,8 @@ __device__ __forceinline__ float conv_dot(const ConvLane<N>& q, float& run) {
   return y;
 }
 
-template <int L, bool BS>
+// DF: conv_state laid out [pool, 3D, W-1] (true) or [pool, W-1, 3D] (false).
+template <int L, bool BS, bool DF>
 __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(const StepArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using S = Smem<L, BS>;
@@ -551,7 +546,8 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   // conv work: channel c of the head; the first half of the CTA takes q and k
   // over tokens [0, A) and v over [0, B), the second half q and k over [A, L)
   // and v over [B, L) (A = ceil(L/2), B = floor(L/2)): 1.5 L outputs a thread
-  // for even L.
+  // for even L.  One code path serves both halves (a second copy of the conv
+  // costs more in instruction fetch than its constant token offsets save).
   constexpr int CA = (L + 1) / 2, CB = L / 2;
   const int c = tid & (HD - 1);
   const bool second = tid >= HD;
@@ -597,23 +593,32 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   // The conv inputs of the thread's tokens (projected x from position 3 on, the
   // start window below it) go out first so that they do not queue behind the
   // state's bulk copies; they are packed once the copies are issued.
+  // Conv cache addressing (elements): slot s, channel ch, window slot j at
+  // s * slot_elems + ch * CHS + j * JS.
+  const long long slot_elems = 3LL * D * SL;
+  const long long CHS = DF ? SL : 1, JS = DF ? 1 : 3LL * D;
+  // the thread's q channel: column h * 128 + c; k and v are D and 2 D further
+  const long long cch = (long long)(h * HD + c) * CHS;
   unsigned short xin[3][CA + 3];
   {
-    const unsigned short* proj16 = reinterpret_cast<const unsigned short*>(a.projected);
-    const unsigned short* cs16 = reinterpret_cast<const unsigned short*>(a.conv_state);
-    const long long cstep = conv_step(a);
+    const unsigned short* prow =
+        reinterpret_cast<const unsigned short*>(a.projected) + row0 * a.pitch + h * HD + c;
+    const unsigned short* win =
+        reinterpret_cast<const unsigned short*>(a.conv_state) + (long long)start * slot_elems + cch;
 #pragma unroll
     for (int kind = 0; kind < 3; ++kind) {
       const int t0 = conv_t0(kind), n = conv_n(kind);
-      const int ch = kind * D + h * HD + c;
-      const unsigned short* cs = cs16 + conv_base(a, start, ch);
 #pragma unroll
       for (int i = 0; i < CA + 3; ++i) {
         const int pos = t0 + i;  // sequence position; pos - 3 < t0 + n <= L
         unsigned short v = 0;
         if (n > 0 && i < n + 3) {
-          if (pos >= 3) v = proj16[(row0 + pos - 3) * a.pitch + ch];
-          else if (pos - (3 - SL) >= 0) v = cs[(pos - (3 - SL)) * cstep];
+          if (pos >= 3) {
+            v = prow[(long long)(pos - 3) * a.pitch + kind * D];
+          } else {
+            const int j = pos + SL - 3;  // window slot of the position
+            if (j >= 0) v = win[(long long)kind * D * CHS + j * JS];
+          }
         }
         xin[kind][i] = v;
       }
@@ -668,16 +673,14 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   }
   __syncthreads();  // barriers initialised, f_a, its squares and the slots staged
 
-  // ---- causal conv of the thread's channels (correctly rounded), window stores -
+  // ---- causal conv of the thread's channels (correctly rounded) ---------------
   // It runs before z: its inputs arrived with round trips 1 and 2, which the
   // recurrence waits for anyway, and they are dead before z needs registers.
   {
-    const long long cstep = conv_step(a);
 #pragma unroll
     for (int kind = 0; kind < 3; ++kind) {
       const ConvLane<CA>& q = cv[kind];
       const int t0 = conv_t0(kind), n = conv_n(kind);
-      const int ch = kind * D + h * HD + c;
 #pragma unroll
       for (int i = 0; i < CA; ++i) {
         if (i >= n) continue;
@@ -706,21 +709,36 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
         if (kind == 0) qh[t * HD + c] = yb;
         else if (kind == 1) kh[t * HD + c] = yb;
         else vv[t * HD + c] = __float2bfloat16_rn(yb);
-        // the window after token t: inputs at seq positions t + 1 .. t + 3, of
-        // which the last SL go to window slots 0 .. SL - 1 of slots[r, t]
-        unsigned short* cs = reinterpret_cast<unsigned short*>(a.conv_state) + conv_base(a, slot_s[t], ch);
-#pragma unroll
-        for (int p = 1; p <= 3; ++p) {
-          const int j = p - 4 + SL;
-          if (j >= 0) cs[j * cstep] = q.get(i + p);
-        }
       }
     }
   }
+  // The windows after each token (copies of the conv inputs, still in the
+  // thread's registers) go out after z and the l2norm: scattered 2-byte stores
+  // queue in the SM's memory pipeline, and shuffles and shared-memory loads
+  // issued behind them wait until they drain.
+  auto store_windows = [&]() {
+    unsigned short* conv16 = reinterpret_cast<unsigned short*>(a.conv_state);
+#pragma unroll
+    for (int kind = 0; kind < 3; ++kind) {
+      const ConvLane<CA>& q = cv[kind];
+      const int t0 = conv_t0(kind), n = conv_n(kind);
+      // sequence position t + p (p = 1..3) goes to window slot p + SL - 4 of slots[r, t]
+      const long long wk = cch + (long long)kind * D * CHS + (long long)(SL - 4) * JS;
+#pragma unroll
+      for (int i = 0; i < CA; ++i) {
+        if (i >= n) continue;
+        const long long cb = wk + (long long)slot_s[t0 + i] * slot_elems;
+#pragma unroll
+        for (int p = 1; p <= 3; ++p)
+          if (p + SL >= 4) conv16[cb + p * JS] = q.get(i + p);
+      }
+    }
+  };
   // ---- z = f_b . f_a (correctly rounded), lower-bound gate, e^g ---------------
   {
     const float expA = expf(a_log);
-#pragma unroll 1
+    // unrolled for short verifies; rolled above four tokens (instruction fetch)
+#pragma unroll(L <= 4 ? 2 : 1)
     for (int t = 0; t < L; t += 2) {
       const bool pair = (t + 1 < L);
       const uint4* f0 = reinterpret_cast<const uint4*>(fa_b + t * HD);
@@ -746,14 +764,18 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       const bool unsure = bf16_rounding_uncertain(z, bound);
       unsigned redo = __ballot_sync(0xffffffffu, unsure) & (pair ? 0xffffffffu : 0x55555555u);
       z = bf_round(z);
+      // Each 8-lane group resolves its own first undecided lane per round (the
+      // exact sum runs within a group), so a round settles up to four.
+      const int g8 = lane & 24;
       while (redo) {
-        const int li = __ffs(redo) - 1;
-        redo &= redo - 1;
+        const unsigned mine = (redo >> g8) & 0xffu;
+        const int li = g8 + (mine ? __ffs(mine) - 1 : 0);
+        redo &= ~__ballot_sync(0xffffffffu, mine != 0 && lane == li);
         const uint4* fr = reinterpret_cast<const uint4*>(fa_b + (pair ? t + (li & 1) : t) * HD);
         uint4 w0, w1;
         fb_row(fbw, (li >> 1) & 3, w0, w1);
         const float ex = z_exact(w0, w1, fr[lane & 7], fr[8 + (lane & 7)]);
-        if (lane == li) z = ex;
+        if (mine != 0 && lane == li) z = ex;
       }
       if (pair || (lane & 1) == 0) {
         const float x = z + dtc;
@@ -767,8 +789,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   __syncthreads();  // raw q, k, v and e^g of every channel written
 
   // ---- l2norm of q and k, k^.q^: one warp per token -----------------------------
-  if (warp < L) {
-    const int t = warp;
+  // Every warp runs it (warp w on token w mod L) and warps < L store: with one
+  // warp alone on this short stretch (the others parked at the barrier) it
+  // took ~1.6 us, with all warps on it ~0.1 us (measured, globaltimer stamps).
+  {
+    const int t = warp % L;
     float4 q = *reinterpret_cast<float4*>(qh + t * HD + lane * 4);
     float4 k = *reinterpret_cast<float4*>(kh + t * HD + lane * 4);
     const float sq = warp_sum(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
@@ -778,11 +803,15 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     const float fq = rq * a.q_scale;
     q.x *= fq; q.y *= fq; q.z *= fq; q.w *= fq;
     k.x *= rk; k.y *= rk; k.z *= rk; k.w *= rk;
-    *reinterpret_cast<float4*>(qh + t * HD + lane * 4) = q;
-    *reinterpret_cast<float4*>(kh + t * HD + lane * 4) = k;
-    if (lane == 0) kq_s[t] = sqk * fq * rk;
+    __syncthreads();  // every warp has read q and k before they are overwritten
+    if (warp < L) {
+      *reinterpret_cast<float4*>(qh + t * HD + lane * 4) = q;
+      *reinterpret_cast<float4*>(kh + t * HD + lane * 4) = k;
+      if (lane == 0) kq_s[t] = sqk * fq * rk;
+    }
   }
   __syncthreads();
+  store_windows();
 
   // ---- recurrence: 2 passes of 2 quarters; 16 lanes per v row, 8 k values a lane --
   // Lane l: half hs = l >> 4 of the warp, kl = l & 15 owns k = 64 m + 4 kl + (0..3)
@@ -925,7 +954,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   // a dependent launch (the o_proj of a layer plan) may start its CTAs now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the RMSNorm weights of this lane, in flight across the barrier
-  const float4 onw = (warp < L) ? *reinterpret_cast<const float4*>(a.o_norm + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 onw = *reinterpret_cast<const float4*>(a.o_norm + lane * 4);
   if (timed_out && lane == 0) {
     ctl[0] = 1;
     atomicOr(a.err, KDA_ERR_TIMEOUT);
@@ -941,9 +970,9 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     return;
   }
 
-  // ---- gated RMSNorm: one warp per token -----------------------------------------
-  if (warp < L) {
-    const int t = warp;
+  // ---- gated RMSNorm: one warp per token (all warps run it, as the l2norm) --------
+  {
+    const int t = warp % L;
     float o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[e] = bf(ob[t * HD + lane * 4 + e]);
@@ -954,7 +983,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       y[e] = __float2bfloat16_rn(o[e] * rstd * wn[e] * __half2float(gsig_s[t * HD + lane * 4 + e]));
-    *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
+    if (warp < L) *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
   }
   if constexpr (L == 1) {
     if (tid == 0) bulk_wait_read();  // shared memory stays until the bulk stores have read it
@@ -1008,11 +1037,18 @@ __global__ void row_norms(const __nv_bfloat16* m, float* norms, int rows) {
 
 template <int L>
 cudaError_t set_smem_attr() {
-  const cudaError_t e1 = cudaFuncSetAttribute(kda_step_kernel<L, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              Smem<L, false>::bytes);
-  const cudaError_t e2 = cudaFuncSetAttribute(kda_step_kernel<L, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              Smem<L, true>::bytes);
-  return e1 != cudaSuccess ? e1 : e2;
+  const cudaError_t e[4] = {
+      cudaFuncSetAttribute(kda_step_kernel<L, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Smem<L, false>::bytes),
+      cudaFuncSetAttribute(kda_step_kernel<L, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Smem<L, true>::bytes),
+      cudaFuncSetAttribute(kda_step_kernel<L, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Smem<L, false>::bytes),
+      cudaFuncSetAttribute(kda_step_kernel<L, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Smem<L, true>::bytes)};
+  for (cudaError_t x : e)
+    if (x != cudaSuccess) return x;
+  return cudaSuccess;
 }
 
 cudaError_t set_all_smem_attrs() {
@@ -1036,14 +1072,19 @@ cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream, bool 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  const cudaError_t e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true>, a)
-                                   : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false>, a);
+  cudaError_t e;
+  if (a.conv_dim_first)
+    e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true, true>, a)
+                   : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false, true>, a);
+  else
+    e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true, false>, a)
+                   : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false, false>, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int L>
 const void* kernel_fn() {
-  return reinterpret_cast<const void*>(kda_step_kernel<L, false>);
+  return reinterpret_cast<const void*>(kda_step_kernel<L, false, true>);
 }
 
 bool aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
