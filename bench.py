@@ -169,7 +169,8 @@ class DeviceWorkload:
     """One workload's inputs resident on the device (pools sentinel-filled,
     read slots filled from the seeded generator)."""
 
-    def __init__(self, si: I.StepInputs, device, gate_mode: int = 0, plan: bool = False, state_dtype: str = "f32"):
+    def __init__(self, si: I.StepInputs, device, gate_mode: int = 0, plan: bool = False, state_dtype: str = "f32",
+                 prep=None):
         import torch
         import linear_attention_decode_03_gb300 as kda
 
@@ -181,10 +182,12 @@ class DeviceWorkload:
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
 
         wt = si.weights
-        self.prep = kda.PreparedKda(bf16(wt.conv_w), None if wt.bias is None else bf16(wt.bias), bf16(wt.f_b),
-                                    torch.from_numpy(wt.A_log).to(device), torch.from_numpy(wt.dt_bias).to(device),
-                                    torch.from_numpy(wt.o_norm).to(device), gate_lower_bound=wt.gate_lower_bound,
-                                    eps=wt.eps, conv_dim_first=True, gate_mode=gate_mode, state_dtype=state_dtype)
+        self.own_prep = prep is None
+        self.prep = prep if prep is not None else kda.PreparedKda(
+            bf16(wt.conv_w), None if wt.bias is None else bf16(wt.bias), bf16(wt.f_b),
+            torch.from_numpy(wt.A_log).to(device), torch.from_numpy(wt.dt_bias).to(device),
+            torch.from_numpy(wt.o_norm).to(device), gate_lower_bound=wt.gate_lower_bound,
+            eps=wt.eps, conv_dim_first=True, gate_mode=gate_mode, state_dtype=state_dtype)
         self.projected = bf16(si.projected)
         idx = torch.from_numpy(si.read_slots).to(device)
         if state_dtype == "bf16":
@@ -342,11 +345,17 @@ def run_reference(args, w: I.Workload):
 def workload_config(w: I.Workload, args):
     state, allb = algorithmic_bytes(w, getattr(args, "state_dtype", "f32"))
     big = state > L2_BYTES
+    n_copies = getattr(args, "rotation_copies", 0)
+    if n_copies:
+        l2 = (f"inputs larger than L2: {n_copies} independent copies of the workload's caches and inputs "
+              f"({n_copies * allb / 1e6:.0f} MB touched a round), stepped through in turn back to back")
+    elif big:
+        l2 = "inputs larger than L2 (%.0f MB of state per step)" % (state / 1e6)
+    else:
+        l2 = "L2 flushed between timed steps (256 MiB write, then 256 MiB read; outside the per-step events)"
     return {"workload": w.name, "heads": w.heads, "head_dim": HEAD_DIM, "requests": w.requests, "tokens_per_request": w.L,
             "rows": w.rows, "pool_slots": w.pool, "conv_width": w.width, "state_bytes_per_step": state,
-            "algorithmic_bytes_per_step": allb,
-            "l2": ("inputs larger than L2 (%.0f MB of state per step)" % (state / 1e6)) if big
-            else "L2 flushed between timed steps (256 MiB write, then 256 MiB read; outside the per-step events)",
+            "algorithmic_bytes_per_step": allb, "l2": l2,
             "parallelism": "replicas" if args.gpus > 1 else "single GPU",
             "gate": getattr(args, "gate_mode", "sigmoid"),
             "launch": "plan (CUDA graph)" if getattr(args, "plan", False) else "kda_step",
@@ -722,6 +731,53 @@ def time_blocks(step, steps, stream, flush_bufs, min_s=MIN_TIMED_S):
     return blocks, step_ms
 
 
+def touched_bytes(w: I.Workload, state_dtype: str = "f32") -> int:
+    """Bytes one step reads or writes (state, projected rows, out, conv windows)."""
+    return algorithmic_bytes(w, state_dtype)[1]
+
+
+def rotation_copies(w: I.Workload, state_dtype: str = "f32") -> int:
+    """Independent copies of a workload's caches and inputs that a run steps
+    through in turn so that each step finds none of its data in L2: the other
+    copies' steps in between touch at least three times the L2 size.  0 when
+    one step's own bytes already exceed L2 (no copies needed) or are too few
+    for copies to be sensible (a latency case: its steps are flushed)."""
+    t = touched_bytes(w, state_dtype)
+    if t > L2_BYTES or t < L2_BYTES // 8:
+        return 0
+    return 1 + -(-3 * L2_BYTES // t)
+
+
+def make_copies(si: I.StepInputs, device, args, n: int):
+    """n device copies of one workload's caches and inputs sharing one prepared
+    weight handle (the layer's weights are the same for every copy)."""
+    first = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=args.plan,
+                           state_dtype=args.state_dtype)
+    return [first] + [DeviceWorkload(si, device, plan=args.plan, state_dtype=args.state_dtype, prep=first.prep)
+                      for _ in range(n - 1)]
+
+
+def time_rotating(copies, steps, stream, min_s=MIN_TIMED_S):
+    """Blocks of `steps` back-to-back steps, step i on copy i mod len(copies),
+    between two CUDA events; repeated until `min_s` seconds of timed work.
+    Returns the ms per step of every block."""
+    import torch
+
+    blocks, total, i = [], 0.0, 0
+    while total < min_s * 1e3 or not blocks:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            copies[i % len(copies)].step()
+            i += 1
+        e1.record(stream)
+        torch.cuda.synchronize()
+        block = e0.elapsed_time(e1)
+        blocks.append(block / steps)
+        total += block
+    return blocks
+
+
 def measure_workload(w: I.Workload, device, args):
     """One more workload in the same process: step time (median block), tokens/s
     and the fractions of the measured HBM peak, for the state bytes alone and
@@ -729,16 +785,30 @@ def measure_workload(w: I.Workload, device, args):
     import torch
 
     si = I.make_step_inputs(w)
-    dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=args.plan,
-                        state_dtype=args.state_dtype)
     state_b, all_b = algorithmic_bytes(w, args.state_dtype)
-    flush_bufs = make_flush(device) if state_b <= L2_BYTES else None
+    n_copies = rotation_copies(w, args.state_dtype)
+    copies = make_copies(si, device, args, max(n_copies, 1))
+    dw = copies[0]
+    stream = torch.cuda.current_stream(device)
     for _ in range(max(args.warmup, 3)):
-        dw.step()
+        for c in copies:
+            c.step()
     if dw.prep.check() != 0:
         raise RuntimeError(f"device error bits set during warm-up ({w.name})")
-    blocks, step_ms = time_blocks(dw.step, args.steps, torch.cuda.current_stream(device), flush_bufs,
-                                  args.min_timed_s)
+    flush_rec = None
+    flush_bufs = None
+    if n_copies:
+        blocks = time_rotating(copies, args.steps, stream, args.min_timed_s)
+        step_ms = []
+        # the same steps one at a time after an L2 flush, for comparison
+        flush_bufs = make_flush(device)
+        fb, fms = time_blocks(dw.step, args.steps, stream, flush_bufs, args.min_timed_s)
+        flush_rec = {"ms_per_step": statistics.median(fb), "ms_per_step_median_single_step": statistics.median(fms),
+                     "rule": "each step alone, L2 flushed before it (256 MiB write, then 256 MiB read), "
+                             "CUDA events around the step"}
+    else:
+        flush_bufs = make_flush(device) if state_b <= L2_BYTES else None
+        blocks, step_ms = time_blocks(dw.step, args.steps, stream, flush_bufs, args.min_timed_s)
     if dw.prep.check() != 0:
         raise RuntimeError(f"device error bits set during the timed steps ({w.name})")
     ms = statistics.median(blocks)
@@ -749,9 +819,17 @@ def measure_workload(w: I.Workload, device, args):
            "achieved_gbs": all_b / (ms / 1e3) / 1e9, "frac": all_b / (ms / 1e3) / 1e9 / peak,
            "blocks": len(blocks), "launches": args.steps * len(blocks),
            "ms_per_step_median_single_step": statistics.median(step_ms) if step_ms else None,
-           "l2": "inputs larger than L2" if flush_bufs is None else "L2 flushed between timed steps",
+           "l2": (f"inputs larger than L2: {n_copies} independent copies of the workload's caches and inputs "
+                  f"({n_copies * touched_bytes(w, args.state_dtype) / 1e6:.0f} MB touched a round), stepped "
+                  "through in turn back to back" if n_copies else
+                  "inputs larger than L2" if flush_bufs is None else "L2 flushed between timed steps"),
            "traffic": measured_traffic(w.name)}
-    del dw, flush_bufs
+    if flush_rec is not None:
+        flush_rec["tokens_per_s"] = w.rows / (flush_rec["ms_per_step"] / 1e3)
+        flush_rec["state_frac_of_peak"] = state_b / (flush_rec["ms_per_step"] / 1e3) / 1e9 / peak
+        flush_rec["frac"] = all_b / (flush_rec["ms_per_step"] / 1e3) / 1e9 / peak
+        rec["flushed_single_step"] = flush_rec
+    del dw, copies, flush_bufs
     torch.cuda.empty_cache()
     return rec
 
@@ -769,6 +847,9 @@ def main():
     ap.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
                     help="blocks of --steps steps are repeated until this much timed work; "
                          "ms_per_step is the median block")
+    ap.add_argument("--l2-flush", action="store_true",
+                    help="time a workload whose step fits L2 as single steps after an L2 flush instead of on "
+                         "independent copies stepped through in turn")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the other workloads (per_workload) measured after the main one")
     ap.add_argument("--plan", action="store_true",
@@ -816,10 +897,14 @@ def main():
     kda.load_library()
 
     si = I.make_step_inputs(w)
-    gm = 0 if args.gate_mode == "sigmoid" else 1
-    dw = DeviceWorkload(si, device, gate_mode=gm, plan=args.plan, state_dtype=args.state_dtype)
     state_b, all_b = algorithmic_bytes(w, args.state_dtype)
-    flush_bufs = make_flush(device) if state_b <= L2_BYTES else None
+    # a workload whose step fits L2 is timed on independent copies stepped through in
+    # turn (inputs larger than L2), unless --l2-flush asks for flushed single steps
+    n_copies = 0 if args.l2_flush else rotation_copies(w, args.state_dtype)
+    args.rotation_copies = n_copies
+    copies = make_copies(si, device, args, max(n_copies, 1))
+    dw = copies[0]
+    flush_bufs = make_flush(device) if (not n_copies and state_b <= L2_BYTES) else None
     stream = torch.cuda.current_stream(device)
 
     def barrier():
@@ -828,7 +913,8 @@ def main():
         torch.cuda.synchronize(device)
 
     for _ in range(args.warmup):
-        dw.step()
+        for c in copies:
+            c.step()
     if dw.prep.check() != 0:
         raise RuntimeError("device error bits set during warm-up")
 
@@ -837,7 +923,10 @@ def main():
     time.sleep(0.3)
     barrier()
     t_host0 = time.time()
-    blocks, step_ms = time_blocks(dw.step, args.steps, stream, flush_bufs, args.min_timed_s)
+    if n_copies:
+        blocks, step_ms = time_rotating(copies, args.steps, stream, args.min_timed_s), []
+    else:
+        blocks, step_ms = time_blocks(dw.step, args.steps, stream, flush_bufs, args.min_timed_s)
     barrier()
     t_host1 = time.time()
     time.sleep(0.25)
@@ -960,7 +1049,7 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
     if world == 1 and not args.no_per_workload:
-        del dw
+        del dw, copies
         torch.cuda.empty_cache()
         line["per_workload"] = {name: measure_workload(I.WORKLOADS[name], device, args)
                                 for name in PER_WORKLOAD if name != w.name}
