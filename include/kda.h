@@ -68,8 +68,17 @@ typedef struct kda_handle kda_handle;
  * returned (then cleared) by kda_check. */
 #define KDA_ERR_SLOT 1u     /* a slot outside [0, pool) other than a padding -1: request skipped */
 #define KDA_ERR_ACCEPTED 2u /* accepted[r] outside 1..L: request skipped                         */
-#define KDA_ERR_TIMEOUT 4u  /* a bounded wait for a state tile gave up: that tile is not written  */
+#define KDA_ERR_TIMEOUT 4u  /* a bounded wait (about 1 s) for the start state gave up: see below */
 #define KDA_ERR_DUPLICATE 8u /* KDA_DEBUG builds only: two rows of the step write the same slot    */
+
+/* KDA_ERR_TIMEOUT: the step reads a (request, head)'s start state in two
+ * halves of 64 v rows (one wait each) and finishes each half over all L tokens
+ * before it waits for the next.  If the first wait gives up, no state row of
+ * that (request, head) is written; if the second does, rows 0..63 of the
+ * states may already be in every slots[r, t] (decode: in slots[b]) while rows
+ * 64..127 are not.  Either way its out rows are not written, and the conv
+ * windows (stored before the state is needed) are.  Treat the request's
+ * caches as undefined after a timeout. */
 
 /* Maximum verify tokens per request. */
 #define KDA_MAX_TOKENS 8
@@ -247,10 +256,12 @@ void kda_destroy(kda_handle* handle);
 const char* kda_strerror(int code);
 
 /*
- * kda_launch_info -- the launch shape kda_step uses for L tokens: CTAs per
- * (request, head), threads per CTA, dynamic shared memory bytes and the
- * resident CTAs per SM the occupancy calculator reports.  Returns KDA_OK,
- * KDA_EINVAL or KDA_ECUDA.  Needs a current CUDA device.
+ * kda_launch_info -- the launch shape kda_step uses for L tokens (one CTA per
+ * (request, head), fp32 state pool, window-first conv cache): threads per
+ * CTA, dynamic shared memory bytes per CTA and the resident CTAs per SM the
+ * occupancy calculator reports (each output pointer may be NULL).  Returns
+ * KDA_OK, KDA_EINVAL (L outside 1..KDA_MAX_TOKENS) or KDA_ECUDA.  Needs a
+ * current CUDA device when ctas_per_sm is not NULL.
  */
 int kda_launch_info(int L, int* threads, int* smem_bytes, int* ctas_per_sm);
 

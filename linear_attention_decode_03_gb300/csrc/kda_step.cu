@@ -12,30 +12,34 @@
 // SM, every global access issued as early as its address is known, so that a
 // CTA spends two memory round trips before its compute:
 //   * round trip 1 (issued at entry, by every thread, with no dependence):
-//       the request's slots / accepted, this warp's 16 rows of the head's f_b
-//       (256 contiguous bytes a row, 8 bytes a lane), the f_a, out-gate and
-//       beta values, the q/k/v inputs, conv taps and bias of the thread's
-//       channels.
-//   * round trip 2 (once the slots are in): thread 0 validates them and puts
-//       the 64 KiB start state of (slot, head) in flight as four 16 KiB bulk
-//       async copies (cp.async.bulk, L2 evict-first) on four mbarriers; every
-//       thread loads the start conv windows of its channels.
+//       the request's slots / accepted, the lane's share of the head's f_b
+//       (4 rows x 16 k, two 16-byte loads a row), the f_a, out-gate and beta
+//       values, the packed conv taps and bias of the thread's channels.
+//   * round trip 2 (once the slots are in): every thread validates them and
+//       loads the conv inputs of its channels (projected x and the start
+//       window); thread 0 puts the 64 KiB start state of (slot, head) in
+//       flight as four 16 KiB bulk async copies (cp.async.bulk, L2
+//       evict-first) on four mbarriers -- decode at once, verify once its own
+//       conv inputs are in.
 //   * while the state lands: the causal conv of the q, k, v channels over the
-//       L tokens (window stores into slots[r, t]); z = f_b . f_a per warp (16
-//       channels, 4 products a lane, a transposed xor butterfly over the warp,
-//       and a closed-form bound on its fp32 error), the lower-bound gate and
-//       e^g; one warp per token l2-normalises q and k and forms k^.q^ and beta.
+//       L tokens; z = f_b . f_a (4 channels x 16 k a lane with mixed-precision
+//       bf16 FMAs, a reduce-scatter over 8 lanes, a closed-form bound on the
+//       fp32 error), the lower-bound gate and e^g; the l2norm of q and k and
+//       k^.q^ (one warp per token, run by every warp); then the windows after
+//       each token go to slots[r, t].
 //   * recurrence: two passes over pairs of 32-row quarters of the state
-//       (rows = v; each pass waits on its two copies); a group of 8 lanes owns
-//       one v row of each quarter, 16 k values per lane in registers across
-//       the L tokens; S'^T k^ and S'^T q^ are reduced with 3 xor shuffles;
-//       every token's rows go out with 128-bit streaming stores to slots[r, t].
-//   * gated RMSNorm, one warp per token -> bf16 core_out.
+//       (rows = v; each pass waits on its two copies); 16 lanes own a v row,
+//       8 k values a lane, four rows a thread in registers across the L
+//       tokens; S'^T k^ and S'^T q^ are reduced with one 16-lane
+//       reduce-scatter; decode writes the rows back to shared memory and sends
+//       each quarter with a TMA bulk store, verify sends every token's rows to
+//       slots[r, t] with 128-bit stores.
+//   * gated RMSNorm, one warp per token (run by every warp) -> bf16 core_out.
 // The bf16 hand-offs (conv outputs, z) are rounded correctly: each fp32 value
 // carries a bound on its error and is recomputed exactly (fp64, or a
-// compensated TwoSum butterfly) when the bound straddles a bf16 rounding
-// boundary.  Every wait is bounded (about 1 s of SM clock cycles); a wait that
-// gives up sets KDA_ERR_TIMEOUT and the request's outputs are not written.
+// compensated TwoSum sum) when the bound straddles a bf16 rounding boundary.
+// Every wait is bounded (about 1 s of SM clock cycles); a wait that gives up
+// sets KDA_ERR_TIMEOUT (see include/kda.h for what is then written).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -1093,7 +1097,7 @@ bool aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p)
 
 struct kda_handle {
   int device;
-  int sms;  // multiprocessors of the device: one persistent CTA each
+  int sms;  // multiprocessors of the device
   int heads, W;
   uint2* conv_w;
   __nv_bfloat16* bias;
