@@ -358,21 +358,34 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
 // through distributed shared memory.  The operand bytes out of L2 (about
 // 8 TB/s for TMA reads on this part, the same for 100 or 152 reading SMs)
 // bound these tiles as much as the tensor pipe does, so the tile is as wide as
-// one MMA allows (x : W bytes = 1 : 2).  Every CTA loads its own weight boxes:
-// the copies only ever read this GPU's memory through the caller's tensor maps.
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4, TC_THREADS = 128;
+// one MMA allows (x : W bytes = 1 : 2), and with more than 128 rows a CTA may
+// take two 128-row halves against each weight box (see TcShape).  Every CTA
+// loads its own boxes: the copies only ever read this GPU's memory through the
+// caller's tensor maps.
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_THREADS = 128;
 constexpr int TC_ABYTES = TC_BM * 128, TC_BBYTES = TC_BN * 128;  // one 64-k box each
-constexpr int TC_STAGE = TC_ABYTES + TC_BBYTES;
-constexpr int TC_RING = TC_STAGES * TC_STAGE;
 constexpr int TC_RED_LD = TC_BN + 4;  // partial tile, row-major: element (r, c) at r * 260 + c (16-byte stores, no bank conflicts)
-constexpr int TC_SMEM = 1024 + TC_RING + 8 * (2 * TC_STAGES + 1) + 16;
+// MH row halves a CTA: 1 = a 128 x 256 tile, four stages of 48 KB; 2 = a 256 x 256
+// tile whose two 128-row halves share each weight box (two M128 MMAs a k step into
+// two 256-column accumulators), three stages of 64 KB.  The two-half tile takes a
+// third fewer bytes into the SM per product (64 KB a stage for 256 x 256 x 64 against
+// 48 KB for 128 x 256 x 64), the intake that bounds these tiles.
+template <int MH>
+struct TcShape {
+  static constexpr int BM = TC_BM * MH;
+  static constexpr int STAGES = MH == 1 ? 4 : 3;
+  static constexpr int STAGE = MH * TC_ABYTES + TC_BBYTES;
+  static constexpr int RING = STAGES * STAGE;
+  static constexpr int SMEM = 1024 + RING + 8 * (2 * STAGES + 1) + 16;
+  static constexpr int TMEM_COLS = TC_BN * MH;  // one 256-column fp32 accumulator a half
+  static_assert(TC_BM * TC_RED_LD * 4 <= RING, "a half's partials overlay the ring");
+};
 // split model for these tiles, in stages (~0.4 us each under load): a CTA's fixed
 // part (launch ramp, first copies, epilogue) and the extra of a K split (partials
 // through shared memory and the cluster reduction), fitted to splits 1..8 of
 // the 64-, 128- and 512-row in_proj and o_proj shapes
 constexpr double TC_FIXED_STAGES = 16.0;
 constexpr double TC_REDUCE_STAGES = 10.0;
-static_assert(TC_BM * TC_RED_LD * 4 <= TC_RING, "partials overlay the ring");
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1),
 // bf16 A and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
@@ -391,9 +404,12 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
          (2ull << 61);
 }
 
+template <int MH>
 __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __grid_constant__ CUtensorMap tmx,
                                                                     const __grid_constant__ CUtensorMap tmw,
                                                                     const LinArgs a, int tiles_n) {
+  using T = TcShape<MH>;
+  constexpr int TC_STAGES = T::STAGES, TC_STAGE = T::STAGE, TC_RING = T::RING;
   extern __shared__ __align__(128) unsigned char tsmem[];
   const uint32_t raw = smem_addr(tsmem);
   const uint32_t ring = (raw + 1023u) & ~1023u;
@@ -407,7 +423,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   // cluster = the split CTAs of one output tile: rank = K part
   const unsigned split = cluster_nctarank(), rank = cluster_ctarank();
   const long long grp = cluster_id_x();
-  const long long m0 = (grp / tiles_n) * TC_BM, n0 = (grp % tiles_n) * TC_BN;
+  const long long m0 = (grp / tiles_n) * T::BM, n0 = (grp % tiles_n) * TC_BN;
   const long long total = (a.K + TC_BK - 1) / TC_BK;
   const long long s_begin = total * rank / split;
   const long long stages = total * (rank + 1) / split - s_begin;
@@ -423,8 +439,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
     *consumed_p = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {  // the accumulator: 128 lanes x 128 fp32 columns of tensor memory
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(TC_BN)
+  if (warp == 0) {  // the accumulators: 128 lanes x 256 fp32 columns of tensor memory a half
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot),
+                 "r"(T::TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -443,7 +460,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   if (warp == 0) {  // producer
     // the weight tile is read once when there is one row tile (evict first), else kept for the others
     unsigned long long w_policy, x_policy;
-    if (a.M <= TC_BM)
+    if (a.M <= T::BM)
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w_policy));
     else
       asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(w_policy));
@@ -458,9 +475,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
       if (lane == 0) {
         const uint32_t st = ring + slot * TC_STAGE, bar = full0 + 8 * slot;
         const int k = (int)((s_begin + s) * TC_BK);
-        mbar_expect_tx(bar, TC_STAGE);  // the x box and the weight box
-        tma_box(st, &tmx, k, (int)m0, bar, x_policy);
-        tma_box(st + TC_ABYTES, &tmw, k, (int)n0, bar, w_policy);
+        mbar_expect_tx(bar, TC_STAGE);  // the x box of each half and the weight box
+#pragma unroll
+        for (int hf = 0; hf < MH; ++hf) tma_box(st + hf * TC_ABYTES, &tmx, k, (int)(m0 + hf * TC_BM), bar, x_policy);
+        tma_box(st + MH * TC_ABYTES, &tmw, k, (int)n0, bar, w_policy);
       }
       __syncwarp();
       issued = s + 1;
@@ -479,14 +497,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
         const uint32_t st = ring + slot * TC_STAGE;
 #pragma unroll
         for (int k = 0; k < TC_BK / 16; ++k) {  // 16 k = 32 bytes along the swizzled row
-          const uint64_t da = tc_desc(st + 32 * k), db = tc_desc(st + TC_ABYTES + 32 * k);
+          const uint64_t db = tc_desc(st + MH * TC_ABYTES + 32 * k);
           const uint32_t acc = (s > 0 || k > 0) ? 1u : 0u;
-          asm volatile(
-              "{\n\t.reg .pred p;\n\t"
-              "setp.ne.u32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-              "l"(da), "l"(db), "r"(TC_IDESC), "r"(acc)
-              : "memory");
+#pragma unroll
+          for (int hf = 0; hf < MH; ++hf) {  // each half's rows against the shared weight box
+            const uint64_t da = tc_desc(st + hf * TC_ABYTES + 32 * k);
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "setp.ne.u32 p, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + (uint32_t)(hf * TC_BN)),
+                "l"(da), "l"(db), "r"(TC_IDESC), "r"(acc)
+                : "memory");
+          }
         }
         // the slot is free once these MMAs have read it
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty0 +
@@ -517,109 +539,120 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   }
   __syncthreads();
   const int r = warp * 32 + lane;
-  const int rows_here = (int)(a.M - m0 < TC_BM ? a.M - m0 : TC_BM);
+  // the rows of half hf of the tile that exist (0 past the end)
+  auto rows_of = [&](int hf) {
+    const long long left = a.M - (m0 + (long long)hf * TC_BM);
+    return (int)(left <= 0 ? 0 : (left < TC_BM ? left : TC_BM));
+  };
+  // 32 accumulator columns c0.. of half hf for the warp's 32 lanes (rows)
+  auto tmem_load = [&](int hf, int c0, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+          "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+          "=r"(v[30]), "=r"(v[31])
+        : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(hf * TC_BN + c0)));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  };
   if (split == 1) {
-    // accumulator -> bf16 -> global: thread (warp w, lane l) owns row 32w + l, 32 columns a load
-    __nv_bfloat16* yr = a.y + (m0 + r) * a.ldy;
+    // accumulator -> bf16 -> global: thread (warp w, lane l) owns row 32w + l of each half, 32 columns a load
 #pragma unroll 1
-    for (int c0 = 0; c0 < TC_BN; c0 += 32) {
-      uint32_t v[32];
-      if (have && !dead) {
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-            "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
-              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
-              "=r"(v[30]), "=r"(v[31])
-            : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      } else {
+    for (int hf = 0; hf < MH; ++hf) {
+      const int rows_here = rows_of(hf);
+      if (rows_here == 0) break;  // uniform across the CTA
+      __nv_bfloat16* yr = a.y + (m0 + hf * TC_BM + r) * a.ldy;
+#pragma unroll 1
+      for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+        uint32_t v[32];
+        if (have && !dead) {
+          tmem_load(hf, c0, v);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0u;
-      }
-      if (r >= rows_here) continue;
-      const long long n = n0 + c0;
-      if (a.y_vec && n + 32 <= a.N) {
-        uint32_t p[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-          p[j] = *reinterpret_cast<const uint32_t*>(&b2);
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
         }
-        uint4* dst = reinterpret_cast<uint4*>(yr + n);
+        if (r >= rows_here) continue;
+        const long long n = n0 + c0;
+        if (a.y_vec && n + 32 <= a.N) {
+          uint32_t p[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
-      } else {
+          for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            p[j] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(yr + n);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (n + j < a.N) yr[n + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n + j < a.N) yr[n + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
       }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp == 0) {  // the accumulator is read: give the tensor memory back
+    if (warp == 0) {  // the accumulators are read: give the tensor memory back
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(T::TMEM_COLS) : "memory");
     }
     return;
   }
-  // K split: accumulator -> shared memory (row-major, padded), 32 columns a load; rows past `rows` are not needed
+  // K split, one half at a time: accumulator -> shared memory (row-major, padded), 32
+  // columns a load; rows past `rows` are not needed.  Every CTA of the cluster takes
+  // part in both barriers of every half.
 #pragma unroll 1
-  for (int c0 = 0; c0 < TC_BN; c0 += 32) {
-    uint32_t v[32];
-    if (have && !dead) {
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-          "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-            "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-            "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-          : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    } else {
+  for (int hf = 0; hf < MH; ++hf) {
+    const int rows_here = rows_of(hf);
+#pragma unroll 1
+    for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+      uint32_t v[32];
+      if (have && !dead && rows_here > 0) {
+        tmem_load(hf, c0, v);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0u;
-    }
-    if (r < rows_here) {
-      float4* dst = reinterpret_cast<float4*>(red + r * TC_RED_LD + c0);
+        for (int j = 0; j < 32; ++j) v[j] = 0u;
+      }
+      if (r < rows_here) {
+        float4* dst = reinterpret_cast<float4*>(red + r * TC_RED_LD + c0);
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                             __uint_as_float(v[4 * q + 3]));
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
     }
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  cluster_sync();
-  if (warp == 0) {  // the accumulator is read: give the tensor memory back
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
-  }
-  // this CTA's share of the tile: (row, 4-column group) pairs in row-major order, each summed
-  // over the cluster's partials with 16-byte loads and stored as 4 bf16
-  constexpr int CQ = TC_BN / 4;
-  const int E = rows_here * CQ;
-  const int e_end = (int)((long long)E * (rank + 1) / split);
-  for (int e = (int)((long long)E * rank / split) + threadIdx.x; e < e_end; e += TC_THREADS) {
-    const int rr = e / CQ, cq = e % CQ;
-    const float4 v4 = cluster_sum4(red + rr * TC_RED_LD + 4 * cq, split);
-    const long long n = n0 + 4 * cq;
-    __nv_bfloat16* yr = a.y + (m0 + rr) * a.ldy;
-    if (a.y_vec8 && n + 4 <= a.N) {
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(v4.x, v4.y), hi = __floats2bfloat162_rn(v4.z, v4.w);
-      *reinterpret_cast<uint2*>(yr + n) =
-          make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-    } else {
-      const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    cluster_sync();
+    if (hf == MH - 1 && warp == 0) {  // the accumulators are read: give the tensor memory back
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(T::TMEM_COLS) : "memory");
+    }
+    // this CTA's share of the half: (row, 4-column group) pairs in row-major order, each
+    // summed over the cluster's partials with 16-byte loads and stored as 4 bf16
+    constexpr int CQ = TC_BN / 4;
+    const int E = rows_here * CQ;
+    const int e_end = (int)((long long)E * (rank + 1) / split);
+    for (int e = (int)((long long)E * rank / split) + threadIdx.x; e < e_end; e += TC_THREADS) {
+      const int rr = e / CQ, cq = e % CQ;
+      const float4 v4 = cluster_sum4(red + rr * TC_RED_LD + 4 * cq, split);
+      const long long n = n0 + 4 * cq;
+      __nv_bfloat16* yr = a.y + (m0 + hf * TC_BM + rr) * a.ldy;
+      if (a.y_vec8 && n + 4 <= a.N) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(v4.x, v4.y), hi = __floats2bfloat162_rn(v4.z, v4.w);
+        *reinterpret_cast<uint2*>(yr + n) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      } else {
+        const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (n + i < a.N) yr[n + i] = __float2bfloat16_rn(vv[i]);
+        for (int i = 0; i < 4; ++i)
+          if (n + i < a.N) yr[n + i] = __float2bfloat16_rn(vv[i]);
+      }
     }
+    // the peers have read this CTA's partials before they are overwritten or it exits
+    cluster_sync();
   }
-  // the peers have read this CTA's partials before it exits
-  cluster_sync();
 }
 
 bool lin_aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
@@ -739,45 +772,54 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
-int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl) {
-  const long long tiles_m = (a.M + TC_BM - 1) / TC_BM, tiles_n = (a.N + TC_BN - 1) / TC_BN;
+// A two-half stage moves 64 KB into the SM against 48 KB for a one-half stage, for
+// twice the products: its stage time relative to a one-half stage (measured on the
+// 512- and 1024-row in_proj and o_proj shapes).
+constexpr double TC_MH2_STAGE_COST = 1.5;
+
+// The launch of the tcgen05 tile with MH row halves: the K split (cluster size) the
+// cost model picks and its cost, in one-half stage units.
+struct TcPlan {
+  long long tiles_n = 0, groups = 0, split = 1;
+  double cost = 1e300;
+};
+
+template <int MH>
+int tc_plan(const LinArgs& a, TcPlan* plan) {
+  using T = TcShape<MH>;
+  const long long tiles_m = (a.M + T::BM - 1) / T::BM, tiles_n = (a.N + TC_BN - 1) / TC_BN;
   const long long groups = tiles_m * tiles_n;  // output tiles: clusters of one K part
-  CUtensorMap tmx, tmw;
-  if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, TC_BN))
-    return KDA_ECUDA;
-  if (cudaFuncSetAttribute(kda_linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM) !=
+  if (cudaFuncSetAttribute(kda_linear_tc_kernel<MH>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
       cudaSuccess)
     return KDA_ECUDA;
-  static std::atomic<int> cluster_cache[64][LIN_MAX_SPLIT + 1];  // by cluster size, as above
+  static std::atomic<int> cluster_cache[64][LIN_MAX_SPLIT + 1];  // by cluster size, as above (per tile shape)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(TC_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = TC_SMEM;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cfg.dynamicSmemBytes = T::SMEM;
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the previous kernel ends
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const long long stages = (a.K + TC_BK - 1) / TC_BK;
-  long long split = 1;
-  double best = 1e300;
+  const double stage_cost = MH == 1 ? 1.0 : TC_MH2_STAGE_COST;
+  plan->tiles_n = tiles_n;
+  plan->groups = groups;
   for (int c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
     const int cs = c;  // cluster size
     int held = dev < 64 ? cluster_cache[dev][cs].load(std::memory_order_relaxed) : 0;
     if (held <= 0) {
       int sms = 0, per_sm = 0;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_tc_kernel, TC_THREADS, TC_SMEM) !=
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_tc_kernel<MH>, TC_THREADS, T::SMEM) !=
               cudaSuccess)
         return KDA_ECUDA;
       attr[0].val.clusterDim.x = (unsigned)cs;
       cfg.gridDim = dim3((unsigned)cs, 1, 1);
-      if (cudaOccupancyMaxActiveClusters(&held, kda_linear_tc_kernel, &cfg) != cudaSuccess) return KDA_ECUDA;
+      if (cudaOccupancyMaxActiveClusters(&held, kda_linear_tc_kernel<MH>, &cfg) != cudaSuccess) return KDA_ECUDA;
       // never more clusters than the resident CTA slots hold
       const int cap = sms * (per_sm > 0 ? per_sm : 1) / cs;
       if (held > cap) held = cap;
@@ -789,16 +831,49 @@ int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaSt
     const double w = (double)groups / held;
     const double whole = (double)((groups + held - 1) / held), tail = w - (whole - 1.0);
     const double waves = w <= 1.0 ? 1.0 : (tail >= 0.25 ? w : whole);
-    const double cost = waves * ((double)stages / c) + TC_FIXED_STAGES + (c > 1 ? TC_REDUCE_STAGES : 0.0);
-    if (cost < best * (1.0 - 1e-9)) best = cost, split = c;
+    const double cost =
+        waves * ((double)stages / c) * stage_cost + TC_FIXED_STAGES + (c > 1 ? TC_REDUCE_STAGES * MH : 0.0);
+    if (cost < plan->cost * (1.0 - 1e-9)) plan->cost = cost, plan->split = c;
   }
-  if (groups * split > 0x7fffffffLL) return KDA_EINVAL;
-  cfg.gridDim = dim3((unsigned)(groups * split), 1, 1);
-  attr[0].val.clusterDim.x = (unsigned)split;
+  return KDA_OK;
+}
+
+template <int MH>
+int tc_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl, const TcPlan& p) {
+  CUtensorMap tmx, tmw;
+  if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, TC_BN)) return KDA_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(TC_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = TcShape<MH>::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the previous kernel ends
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel, tmx, tmw, a, (int)tiles_n) != cudaSuccess)
+  if (p.groups * p.split > 0x7fffffffLL) return KDA_EINVAL;
+  cfg.gridDim = dim3((unsigned)(p.groups * p.split), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel<MH>, tmx, tmw, a, (int)p.tiles_n) != cudaSuccess)
     return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+// The tcgen05 tiles: one or two 128-row halves a CTA, whichever the cost model rates
+// faster for this shape (two halves cut the bytes a product but halve the tiles).
+int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl) {
+  TcPlan p1, p2;
+  int rc = tc_plan<1>(a, &p1);
+  if (rc != KDA_OK) return rc;
+  if (a.M > TC_BM) {
+    rc = tc_plan<2>(a, &p2);
+    if (rc != KDA_OK) return rc;
+  }
+  if (p2.cost < p1.cost) return tc_launch<2>(x, ldx, w, a, st, pdl, p2);
+  return tc_launch<1>(x, ldx, w, a, st, pdl, p1);
 }
 
 }  // namespace
