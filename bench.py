@@ -358,7 +358,7 @@ def workload_config(w: I.Workload, args):
             "algorithmic_bytes_per_step": allb, "l2": l2,
             "parallelism": "replicas" if args.gpus > 1 else "single GPU",
             "gate": getattr(args, "gate_mode", "sigmoid"),
-            "launch": "plan (CUDA graph)" if getattr(args, "plan", False) else "kda_step",
+            "launch": getattr(args, "launch", "direct"),
             "state_storage": getattr(args, "state_dtype", "f32")}
 
 
@@ -751,16 +751,17 @@ def rotation_copies(w: I.Workload, state_dtype: str = "f32") -> int:
 def make_copies(si: I.StepInputs, device, args, n: int):
     """n device copies of one workload's caches and inputs sharing one prepared
     weight handle (the layer's weights are the same for every copy)."""
-    first = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=args.plan,
+    plan = args.launch == "plan"
+    first = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=plan,
                            state_dtype=args.state_dtype)
-    return [first] + [DeviceWorkload(si, device, plan=args.plan, state_dtype=args.state_dtype, prep=first.prep)
+    return [first] + [DeviceWorkload(si, device, plan=plan, state_dtype=args.state_dtype, prep=first.prep)
                       for _ in range(n - 1)]
 
 
 def time_rotating(copies, steps, stream, min_s=MIN_TIMED_S):
     """Blocks of `steps` back-to-back steps, step i on copy i mod len(copies),
-    between two CUDA events; repeated until `min_s` seconds of timed work.
-    Returns the ms per step of every block."""
+    launched one by one between two CUDA events; repeated until `min_s`
+    seconds of timed work.  Returns the ms per step of every block."""
     import torch
 
     blocks, total, i = [], 0.0, 0
@@ -776,6 +777,84 @@ def time_rotating(copies, steps, stream, min_s=MIN_TIMED_S):
         blocks.append(block / steps)
         total += block
     return blocks
+
+
+def record_block(copies, steps, device):
+    """One CUDA graph holding a block of `steps` steps, step i on copy
+    i mod len(copies): the same kernel launches, with the same arguments, that
+    the direct loop makes, so that a replay runs them with no host in between."""
+    import torch
+
+    cur = torch.cuda.current_stream(device)
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(cur)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        for i in range(steps):
+            copies[i % len(copies)].step()
+    cur.wait_stream(cap)
+    torch.cuda.synchronize(device)
+    return g
+
+
+def time_graph(graph, steps, stream, min_s=MIN_TIMED_S):
+    """Replays of a recorded block of `steps` steps between two CUDA events on
+    `stream`, repeated until `min_s` seconds of timed work.  Returns the ms per
+    step of every replay."""
+    import torch
+
+    blocks, total = [], 0.0
+    while total < min_s * 1e3 or not blocks:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        block = e0.elapsed_time(e1)
+        blocks.append(block / steps)
+        total += block
+    return blocks
+
+
+def time_steps(copies, steps, stream, flush_bufs, launch, device, min_s=MIN_TIMED_S):
+    """The step time of one workload under the chosen launch mode.
+
+    Steps back to back (on rotating copies, or on one copy whose inputs exceed
+    L2): with launch == "graph" each block is one replay of the block recorded
+    as a CUDA graph, and the same blocks launched one step at a time are timed
+    too (returned as `direct`); otherwise the steps are launched one by one
+    (kda_step calls, or plan launches).  Flushed single steps are always
+    launched one by one.  Returns (blocks, single-step times, direct blocks)."""
+    if flush_bufs is not None:
+        blocks, step_ms = time_blocks(copies[0].step, steps, stream, flush_bufs, min_s)
+        return blocks, step_ms, None
+    if launch != "graph":
+        return time_rotating(copies, steps, stream, min_s), [], None
+    graph = record_block(copies, steps, device)
+    graph.replay()  # first replay uploads the graph
+    blocks = time_graph(graph, steps, stream, min_s)
+    del graph
+    direct = time_rotating(copies, steps, stream, min_s)
+    return blocks, [], direct
+
+
+def launch_rule(args, flushed: bool) -> str:
+    if flushed:
+        return "each step launched directly (kda_step) between its own CUDA events"
+    if args.launch == "graph":
+        return (f"each block of {args.steps} steps recorded once as a CUDA graph and replayed "
+                "(the same kda_step launches, no host between them)")
+    if args.launch == "plan":
+        return "every step launched through a launch plan (the step recorded once as a CUDA graph)"
+    return "every step launched directly (kda_step)"
+
+
+def direct_record(direct, w: I.Workload, state_b: int, all_b: int, peak: float) -> dict:
+    """The same blocks launched one step at a time, for comparison."""
+    ms = statistics.median(direct)
+    return {"ms_per_step": ms, "tokens_per_s": w.rows / (ms / 1e3), "blocks": len(direct),
+            "state_frac_of_peak": state_b / (ms / 1e3) / 1e9 / peak, "frac": all_b / (ms / 1e3) / 1e9 / peak,
+            "rule": "the same blocks, every step launched directly (kda_step) from the host loop"}
 
 
 def measure_workload(w: I.Workload, device, args):
@@ -796,19 +875,16 @@ def measure_workload(w: I.Workload, device, args):
     if dw.prep.check() != 0:
         raise RuntimeError(f"device error bits set during warm-up ({w.name})")
     flush_rec = None
-    flush_bufs = None
+    flush_bufs = None if (n_copies or state_b > L2_BYTES) else make_flush(device)
+    blocks, step_ms, direct = time_steps(copies, args.steps, stream, flush_bufs, args.launch, device,
+                                         args.min_timed_s)
     if n_copies:
-        blocks = time_rotating(copies, args.steps, stream, args.min_timed_s)
-        step_ms = []
         # the same steps one at a time after an L2 flush, for comparison
         flush_bufs = make_flush(device)
         fb, fms = time_blocks(dw.step, args.steps, stream, flush_bufs, args.min_timed_s)
         flush_rec = {"ms_per_step": statistics.median(fb), "ms_per_step_median_single_step": statistics.median(fms),
-                     "rule": "each step alone, L2 flushed before it (256 MiB write, then 256 MiB read), "
-                             "CUDA events around the step"}
-    else:
-        flush_bufs = make_flush(device) if state_b <= L2_BYTES else None
-        blocks, step_ms = time_blocks(dw.step, args.steps, stream, flush_bufs, args.min_timed_s)
+                     "rule": "each step alone, launched directly, L2 flushed before it (256 MiB write, then "
+                             "256 MiB read), CUDA events around the step"}
     if dw.prep.check() != 0:
         raise RuntimeError(f"device error bits set during the timed steps ({w.name})")
     ms = statistics.median(blocks)
@@ -818,12 +894,15 @@ def measure_workload(w: I.Workload, device, args):
            "state_gbs": state_b / (ms / 1e3) / 1e9, "state_frac_of_peak": state_b / (ms / 1e3) / 1e9 / peak,
            "achieved_gbs": all_b / (ms / 1e3) / 1e9, "frac": all_b / (ms / 1e3) / 1e9 / peak,
            "blocks": len(blocks), "launches": args.steps * len(blocks),
+           "launch": launch_rule(args, flush_bufs is not None and not n_copies),
            "ms_per_step_median_single_step": statistics.median(step_ms) if step_ms else None,
            "l2": (f"inputs larger than L2: {n_copies} independent copies of the workload's caches and inputs "
                   f"({n_copies * touched_bytes(w, args.state_dtype) / 1e6:.0f} MB touched a round), stepped "
                   "through in turn back to back" if n_copies else
                   "inputs larger than L2" if flush_bufs is None else "L2 flushed between timed steps"),
            "traffic": measured_traffic(w.name)}
+    if direct is not None:
+        rec["direct_launch"] = direct_record(direct, w, state_b, all_b, peak)
     if flush_rec is not None:
         flush_rec["tokens_per_s"] = w.rows / (flush_rec["ms_per_step"] / 1e3)
         flush_rec["state_frac_of_peak"] = state_b / (flush_rec["ms_per_step"] / 1e3) / 1e9 / peak
@@ -852,8 +931,10 @@ def main():
                          "independent copies stepped through in turn")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the other workloads (per_workload) measured after the main one")
-    ap.add_argument("--plan", action="store_true",
-                    help="launch every step through a launch plan (the step recorded once as a CUDA graph)")
+    ap.add_argument("--launch", choices=["graph", "direct", "plan"], default="graph",
+                    help="graph: each timed block of --steps steps recorded once as a CUDA graph and replayed "
+                         "(the direct launches are timed too and reported beside); direct: every step launched "
+                         "from the host loop; plan: every step launched through a launch plan")
     ap.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32",
                     help="state pool storage type (kda_set_state_dtype); the step computes in fp32 either way")
     ap.add_argument("--op", choices=["step", "in_proj", "o_proj", "layer"], default="step",
@@ -923,10 +1004,8 @@ def main():
     time.sleep(0.3)
     barrier()
     t_host0 = time.time()
-    if n_copies:
-        blocks, step_ms = time_rotating(copies, args.steps, stream, args.min_timed_s), []
-    else:
-        blocks, step_ms = time_blocks(dw.step, args.steps, stream, flush_bufs, args.min_timed_s)
+    blocks, step_ms, direct = time_steps(copies, args.steps, stream, flush_bufs, args.launch, device,
+                                         args.min_timed_s)
     barrier()
     t_host1 = time.time()
     time.sleep(0.25)
@@ -1023,6 +1102,7 @@ def main():
     timing = {"blocks": len(blocks), "steps_per_block": args.steps, "timed_s": sum(blocks) * args.steps / 1e3,
               "block_ms_per_step_min": min(blocks), "block_ms_per_step_max": max(blocks),
               "ms_per_step_mean_over_blocks": statistics.mean(blocks),
+              "launch": launch_rule(args, flush_bufs is not None),
               "rule": f"blocks of --steps steps repeated until {args.min_timed_s} s of timed work; "
                       "ms_per_step = the median block / steps"}
     peak, peak_kind = load_peaks()
@@ -1046,6 +1126,8 @@ def main():
         "gpu_launches": args.steps * len(blocks),
         "clocks": sampler.summary(t_host0, t_host1),
     }
+    if direct is not None:
+        line["direct_launch"] = direct_record(direct, w, state_b, all_b, peak)
     if dist is not None:
         dist.destroy_process_group()
     if world == 1 and not args.no_per_workload:

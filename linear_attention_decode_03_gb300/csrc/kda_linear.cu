@@ -407,7 +407,7 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
 template <int MH>
 __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __grid_constant__ CUtensorMap tmx,
                                                                     const __grid_constant__ CUtensorMap tmw,
-                                                                    const LinArgs a, int tiles_n) {
+                                                                    const LinArgs a, int tiles_m) {
   using T = TcShape<MH>;
   constexpr int TC_STAGES = T::STAGES, TC_STAGE = T::STAGE, TC_RING = T::RING;
   extern __shared__ __align__(128) unsigned char tsmem[];
@@ -423,7 +423,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   // cluster = the split CTAs of one output tile: rank = K part
   const unsigned split = cluster_nctarank(), rank = cluster_ctarank();
   const long long grp = cluster_id_x();
-  const long long m0 = (grp / tiles_n) * T::BM, n0 = (grp % tiles_n) * TC_BN;
+  // the row tiles of one column tile are neighbours in launch order, so they run
+  // together and all but the first find the weight boxes in L2
+  const long long m0 = (grp % tiles_m) * T::BM, n0 = (grp / tiles_m) * TC_BN;
   const long long total = (a.K + TC_BK - 1) / TC_BK;
   const long long s_begin = total * rank / split;
   const long long stages = total * (rank + 1) / split - s_begin;
@@ -780,7 +782,7 @@ constexpr double TC_MH2_STAGE_COST = 1.5;
 // The launch of the tcgen05 tile with MH row halves: the K split (cluster size) the
 // cost model picks and its cost, in one-half stage units.
 struct TcPlan {
-  long long tiles_n = 0, groups = 0, split = 1;
+  long long tiles_m = 0, groups = 0, split = 1;
   double cost = 1e300;
 };
 
@@ -806,7 +808,7 @@ int tc_plan(const LinArgs& a, TcPlan* plan) {
   cfg.numAttrs = 1;
   const long long stages = (a.K + TC_BK - 1) / TC_BK;
   const double stage_cost = MH == 1 ? 1.0 : TC_MH2_STAGE_COST;
-  plan->tiles_n = tiles_n;
+  plan->tiles_m = tiles_m;
   plan->groups = groups;
   for (int c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
     const int cs = c;  // cluster size
@@ -857,7 +859,7 @@ int tc_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStream
   cfg.numAttrs = pdl ? 2 : 1;
   if (p.groups * p.split > 0x7fffffffLL) return KDA_EINVAL;
   cfg.gridDim = dim3((unsigned)(p.groups * p.split), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel<MH>, tmx, tmw, a, (int)p.tiles_n) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel<MH>, tmx, tmw, a, (int)p.tiles_m) != cudaSuccess)
     return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
