@@ -380,12 +380,22 @@ struct TcShape {
   static constexpr int TMEM_COLS = TC_BN * MH;  // one 256-column fp32 accumulator a half
   static_assert(TC_BM * TC_RED_LD * 4 <= RING, "a half's partials overlay the ring");
 };
-// split model for these tiles, in stages (~0.4 us each under load): a CTA's fixed
-// part (launch ramp, first copies, epilogue) and the extra of a K split (partials
-// through shared memory and the cluster reduction), fitted to splits 1..8 of
-// the 64-, 128- and 512-row in_proj and o_proj shapes
-constexpr double TC_FIXED_STAGES = 16.0;
-constexpr double TC_REDUCE_STAGES = 10.0;
+// Time model of these tiles, in microseconds, for picking MH and the K split C
+// (fitted to 23 in_proj / o_proj shapes, 32 to 1024 rows, K 256 to 12288, every
+// MH and C, on this part): a CTA runs its S / C stages of 64 k at
+//   s = max(MMA time, the SM's own intake time, n x the share of the GPU's L2
+//       intake a CTA takes)                      (n = CTAs running at once)
+// plus a fixed part (first copies, accumulator read-out, stores) that grows with
+// the tile's rows, plus the split's partial-tile reduction when C > 1; the
+// kernel's time is that CTA time x the waves of clusters.
+struct TcModel {
+  double mma, sm_intake, l2_share;  // us a stage; us a stage per running CTA
+  double fixed, fixed_row, reduce;  // us; us a tile row; us
+};
+constexpr TcModel TC_MODEL[2] = {
+    {0.213, 0.406, 0.0021, 8.76, 0.0128, 1.83},   // MH = 1: 48 KB stages
+    {0.710, 0.423, 0.0042, 10.06, 0.0128, 1.32},  // MH = 2: 64 KB stages
+};
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1),
 // bf16 A and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
@@ -774,13 +784,8 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
-// A two-half stage moves 64 KB into the SM against 48 KB for a one-half stage, for
-// twice the products: its stage time relative to a one-half stage (measured on the
-// 512- and 1024-row in_proj and o_proj shapes).
-constexpr double TC_MH2_STAGE_COST = 1.5;
-
 // The launch of the tcgen05 tile with MH row halves: the K split (cluster size) the
-// cost model picks and its cost, in one-half stage units.
+// time model picks and its modelled time (us).
 struct TcPlan {
   long long tiles_m = 0, groups = 0, split = 1;
   double cost = 1e300;
@@ -807,7 +812,8 @@ int tc_plan(const LinArgs& a, TcPlan* plan) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const long long stages = (a.K + TC_BK - 1) / TC_BK;
-  const double stage_cost = MH == 1 ? 1.0 : TC_MH2_STAGE_COST;
+  const TcModel& m = TC_MODEL[MH - 1];
+  const double tile_rows = (double)(a.M < T::BM ? a.M : T::BM);
   plan->tiles_m = tiles_m;
   plan->groups = groups;
   for (int c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
@@ -828,13 +834,16 @@ int tc_plan(const LinArgs& a, TcPlan* plan) {
       if (held <= 0) continue;
       if (dev < 64) cluster_cache[dev][cs].store(held, std::memory_order_relaxed);
     }
-    // waves of clusters: a last wave at least a quarter full counts by its share (its
-    // CTAs run with the copy engines and L2 less loaded), a smaller one as a whole wave
+    // waves of clusters: a last wave at least half full counts by its share, a smaller
+    // one as a whole wave
     const double w = (double)groups / held;
     const double whole = (double)((groups + held - 1) / held), tail = w - (whole - 1.0);
-    const double waves = w <= 1.0 ? 1.0 : (tail >= 0.25 ? w : whole);
+    const double waves = w <= 1.0 ? 1.0 : (tail >= 0.5 ? w : whole);
+    const double running = (double)(groups < held ? groups : held) * c;
+    double s = m.mma > m.sm_intake ? m.mma : m.sm_intake;
+    if (running * m.l2_share > s) s = running * m.l2_share;
     const double cost =
-        waves * ((double)stages / c) * stage_cost + TC_FIXED_STAGES + (c > 1 ? TC_REDUCE_STAGES * MH : 0.0);
+        waves * ((double)stages / c * s + m.fixed + m.fixed_row * tile_rows + (c > 1 ? m.reduce : 0.0));
     if (cost < plan->cost * (1.0 - 1e-9)) plan->cost = cost, plan->split = c;
   }
   return KDA_OK;
