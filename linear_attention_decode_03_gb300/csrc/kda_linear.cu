@@ -346,22 +346,21 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
 
 // ---------------------------------------------------------------------------
 // rows > 16: tcgen05 (5th-generation tensor core) tiles.  A CTA owns a
-// 128 x 256 output tile (rows past `rows` are the copy engine's zeros), K in
-// stages of 64 through a four-deep ring (x box 16 KB + weight box 32 KB, both
-// 128-byte swizzled: the canonical K-major layout of the MMA's shared-memory
-// descriptors).  Warp 0's lane 0 issues the TMA copies, warp 1's lane 0 the
-// MMAs (M 128, N 256, K 16; four a stage) into a 256-column fp32 accumulator
-// in tensor memory; each MMA group's commit frees its ring slot.  After the
-// last stage the four warps read the accumulator (warp w: lanes = rows 32w ..
-// 32w + 31), stage it in shared memory (column-major, padded) and write bf16.
-// K split over a cluster as in the kernel above, the partial tiles summed
-// through distributed shared memory.  The operand bytes out of L2 (about
-// 8 TB/s for TMA reads on this part, the same for 100 or 152 reading SMs)
-// bound these tiles as much as the tensor pipe does, so the tile is as wide as
-// one MMA allows (x : W bytes = 1 : 2), and with more than 128 rows a CTA may
-// take two 128-row halves against each weight box (see TcShape).  Every CTA
-// loads its own boxes: the copies only ever read this GPU's memory through the
-// caller's tensor maps.
+// 128 x 256 output tile, or 256 x 256 as two 128-row halves (rows past `rows`
+// are the copy engine's zeros), K in stages of 64 through a ring of x boxes
+// (16 KB a half) and a weight box (32 KB), all 128-byte swizzled: the
+// canonical K-major layout of the MMA's shared-memory descriptors.  Warp 0's
+// lane 0 issues the TMA copies, warp 1's lane 0 the MMAs (M 128, N 256, K 16;
+// four a stage and half) into a 256-column fp32 accumulator a half in tensor
+// memory; each stage's commit frees its ring slot.  After the last stage the
+// four warps read the accumulators (warp w: lanes = rows 32w .. 32w + 31) and
+// write bf16 rows, or, with K split over a cluster as in the kernel above, put
+// the fp32 partial tile in shared memory (row-major, padded) and sum it over the
+// cluster through distributed shared memory.  Few rows make the weight the
+// bytes (x : W = 1 : 2 a stage); with many rows the bytes each SM takes in per
+// product bound the tiles as much as the tensor pipe does, which the two-half
+// tile cuts by a third (see TcShape).  Every CTA loads its own boxes: the copies
+// only ever read this GPU's memory through the caller's tensor maps.
 constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_THREADS = 128;
 constexpr int TC_ABYTES = TC_BM * 128, TC_BBYTES = TC_BN * 128;  // one 64-k box each
 constexpr int TC_RED_LD = TC_BN + 4;  // partial tile, row-major: element (r, c) at r * 260 + c (16-byte stores, no bank conflicts)
@@ -873,7 +872,7 @@ int tc_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStream
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
-// The tcgen05 tiles: one or two 128-row halves a CTA, whichever the cost model rates
+// The tcgen05 tiles: one or two 128-row halves a CTA, whichever the time model rates
 // faster for this shape (two halves cut the bytes a product but halve the tiles).
 int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl) {
   TcPlan p1, p2;
