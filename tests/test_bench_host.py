@@ -1,0 +1,76 @@
+"""Host-side accounting of the benchmark, on the CPU: the algorithmic bytes that
+the roofline divides by, written out from the method's units (a decode
+token-head moves its 64 KiB state in and out; a verify request-head reads one
+state and writes one per token; a projected row, an out row and a conv window
+move their bf16 elements), and the rule that decides how a workload is kept
+out of L2 between timed steps."""
+from __future__ import annotations
+
+import pytest
+
+import bench
+from linear_attention_decode_03_gb300 import inputs as I
+
+STATE = 128 * 128 * 4  # one (slot, head) fp32 state
+
+
+def _by_hand(w: I.Workload):
+    reads = w.requests * w.heads * STATE  # one start state a (request, head)
+    writes = w.requests * w.L * w.heads * STATE  # one state a token
+    d = 128 * w.heads
+    pitch = 4 * d + 128 + w.heads
+    window = 3 * d * (w.width - 1) * 2  # q, k, v channels x (W - 1) bf16
+    other = (w.requests * w.L * pitch * 2  # projected rows in
+             + w.requests * w.L * d * 2  # out rows
+             + w.requests * window  # one start window read a request
+             + w.requests * w.L * window)  # one window written a token
+    return reads + writes, other
+
+
+@pytest.mark.parametrize("name,state", [
+    ("tiny_decode", 262_144),
+    ("batched_decode", 100_663_296),
+    ("spec_verify", 125_829_120),
+    ("large_decode", 805_306_368),
+    ("full_width_verify", 7_247_757_312),
+])
+def test_state_bytes_per_workload(name, state):
+    w = I.WORKLOADS[name]
+    s, a = bench.algorithmic_bytes(w)
+    assert s == state
+    hs, ho = _by_hand(w)
+    assert s == hs and a == hs + ho
+
+
+def test_large_decode_all_bytes():
+    # 512 rows, 12 heads: projected 512 x 6284 x 2, out 512 x 1536 x 2, and 512 + 512
+    # windows of 3 x 1536 x 3 bf16
+    s, a = bench.algorithmic_bytes(I.WORKLOADS["large_decode"])
+    assert a - s == 6_434_816 + 1_572_864 + 1024 * 27_648 == 36_319_232
+
+
+def test_bf16_state_halves_only_the_state():
+    w = I.WORKLOADS["spec_verify"]
+    s32, a32 = bench.algorithmic_bytes(w, "f32")
+    s16, a16 = bench.algorithmic_bytes(w, "bf16")
+    assert s16 * 2 == s32 and a32 - s32 == a16 - s16
+
+
+@pytest.mark.parametrize("name", sorted(I.WORKLOADS))
+def test_rotation_keeps_each_step_out_of_l2(name):
+    w = I.WORKLOADS[name]
+    t = bench.touched_bytes(w)
+    n = bench.rotation_copies(w)
+    if t > bench.L2_BYTES or t < bench.L2_BYTES // 8:
+        assert n == 0  # larger than L2 already, or a latency case timed after a flush
+    else:
+        # between two uses of one copy the other copies touch at least 3x L2
+        assert (n - 1) * t >= 3 * bench.L2_BYTES
+        assert (n - 2) * t < 3 * bench.L2_BYTES  # and no more copies than that needs
+
+
+def test_rotation_applies_to_the_mid_sized_workloads():
+    assert bench.rotation_copies(I.WORKLOADS["batched_decode"]) > 0
+    assert bench.rotation_copies(I.WORKLOADS["spec_verify"]) > 0
+    assert bench.rotation_copies(I.WORKLOADS["large_decode"]) == 0
+    assert bench.rotation_copies(I.WORKLOADS["tiny_decode"]) == 0
