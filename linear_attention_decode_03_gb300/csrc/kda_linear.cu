@@ -361,46 +361,59 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
 // product bound the tiles as much as the tensor pipe does, which the two-half
 // tile cuts by a third (see TcShape).  Every CTA loads its own boxes: the copies
 // only ever read this GPU's memory through the caller's tensor maps.
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_THREADS = 128;
-constexpr int TC_ABYTES = TC_BM * 128, TC_BBYTES = TC_BN * 128;  // one 64-k box each
-constexpr int TC_RED_LD = TC_BN + 4;  // partial tile, row-major: element (r, c) at r * 260 + c (16-byte stores, no bank conflicts)
-// MH row halves a CTA: 1 = a 128 x 256 tile, four stages of 48 KB; 2 = a 256 x 256
-// tile whose two 128-row halves share each weight box (two M128 MMAs a k step into
-// two 256-column accumulators), three stages of 64 KB.  The two-half tile takes a
-// third fewer bytes into the SM per product (64 KB a stage for 256 x 256 x 64 against
-// 48 KB for 128 x 256 x 64), the intake that bounds these tiles.
-template <int MH>
+constexpr int TC_BM = 128, TC_BK = 64, TC_THREADS = 128;
+constexpr int TC_ABYTES = TC_BM * 128;  // one 64-k x box
+// MH row halves a CTA, BN weight rows (tile columns): MH = 1 a 128 x BN tile, MH = 2 a
+// 256 x BN tile whose two 128-row halves share each weight box (two M128 MMAs a k
+// step into two BN-column accumulators).  The two-half tile takes a third fewer
+// bytes into the SM per product (64 KB a stage for 256 x 256 x 64 against 48 KB for
+// 128 x 256 x 64), the intake that bounds these tiles with many rows; narrower
+// tiles give more CTAs where the tiles are few.
+template <int MH, int BN>
 struct TcShape {
   static constexpr int BM = TC_BM * MH;
-  static constexpr int STAGES = MH == 1 ? 4 : 3;
-  static constexpr int STAGE = MH * TC_ABYTES + TC_BBYTES;
+  static constexpr int BBYTES = BN * 128;  // one 64-k weight box
+  static constexpr int STAGE = MH * TC_ABYTES + BBYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;  // ring <= 200 KB
   static constexpr int RING = STAGES * STAGE;
   static constexpr int SMEM = 1024 + RING + 8 * (2 * STAGES + 1) + 16;
-  static constexpr int TMEM_COLS = TC_BN * MH;  // one 256-column fp32 accumulator a half
-  static_assert(TC_BM * TC_RED_LD * 4 <= RING, "a half's partials overlay the ring");
+  // one fp32 accumulator of BN columns a half; the allocation a power of two >= 32
+  static constexpr int TMEM_COLS = BN * MH <= 32    ? 32
+                                   : BN * MH <= 64  ? 64
+                                   : BN * MH <= 128 ? 128
+                                   : BN * MH <= 256 ? 256
+                                                    : 512;
+  // partial tile, row-major: element (r, c) at r * RED_LD + c (16-byte stores, no bank conflicts)
+  static constexpr int RED_LD = BN + 4;
+  // tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+  // and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
+  // M >> 4 at bits 24-28.
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                    ((uint32_t)(TC_BM >> 4) << 24);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "an M128 MMA takes N = 16..256 in steps of 16");
+  static_assert(STAGE % 1024 == 0, "stages start on 1024-byte swizzle atoms");
+  static_assert(STAGES >= 3, "at least three stages in flight");
+  static_assert(TC_BM * RED_LD * 4 <= RING, "a half's partials overlay the ring");
+  static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
-// Time model of these tiles, in microseconds, for picking MH and the K split C
-// (fitted to 23 in_proj / o_proj shapes, 32 to 1024 rows, K 256 to 12288, every
-// MH and C, on this part): a CTA runs its S / C stages of 64 k at
-//   s = max(MMA time, the SM's own intake time, n x the share of the GPU's L2
-//       intake a CTA takes)                      (n = CTAs running at once)
-// plus a fixed part (first copies, accumulator read-out, stores) that grows with
-// the tile's rows, plus the split's partial-tile reduction when C > 1; the
+// Time model of these tiles, in microseconds, for picking MH, BN and the K split C
+// (fitted to 45 measured in_proj / o_proj shapes -- 2, 12 and 96 heads, 17 to 1024
+// rows, K 256 to 12288 -- at every MH, BN and C, each constant held to a
+// physically plausible range): a CTA runs its S / C stages of 64 k at
+//   s = max(MMA time (~ MH x BN), the SM's own intake time (~ the stage's bytes),
+//           n x the share of the GPU's L2 intake a CTA takes (~ the stage's bytes))
+// (n = CTAs running at once), plus a fixed part (first copies, accumulator
+// read-out, stores; more for two halves, and growing with the tile's rows x
+// columns), plus the split's partial-tile reduction (~ MH x BN) when C > 1; the
 // kernel's time is that CTA time x the waves of clusters.
 struct TcModel {
-  double mma, sm_intake, l2_share;  // us a stage; us a stage per running CTA
-  double fixed, fixed_row, reduce;  // us; us a tile row; us
+  double mma;        // us a stage of 128 x 256 x 64 products
+  double sm_intake;  // us a 48 KB stage
+  double l2_share;   // us a 48 KB stage per running CTA
+  double fixed, fixed_two_halves, fixed_row;  // us; us more with MH = 2; us a tile row of 256 columns
+  double reduce;     // us a 128 x 256 partial tile
 };
-constexpr TcModel TC_MODEL[2] = {
-    {0.213, 0.406, 0.0021, 8.76, 0.0128, 1.83},   // MH = 1: 48 KB stages
-    {0.710, 0.423, 0.0042, 10.06, 0.0128, 1.32},  // MH = 2: 64 KB stages
-};
-
-// tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1),
-// bf16 A and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
-// at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t TC_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TC_BN >> 3) << 17) |
-                              ((uint32_t)(TC_BM >> 4) << 24);
+constexpr TcModel TC_MODEL = {0.287, 0.413, 0.00306, 11.05, 5.05, 0.0233, 1.71};
 
 // Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
 // whose 8-row x 128-byte swizzle atoms are stacked every 1024 bytes: start
@@ -413,11 +426,11 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
          (2ull << 61);
 }
 
-template <int MH>
+template <int MH, int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __grid_constant__ CUtensorMap tmx,
                                                                     const __grid_constant__ CUtensorMap tmw,
                                                                     const LinArgs a, int tiles_m) {
-  using T = TcShape<MH>;
+  using T = TcShape<MH, BN>;
   constexpr int TC_STAGES = T::STAGES, TC_STAGE = T::STAGE, TC_RING = T::RING;
   extern __shared__ __align__(128) unsigned char tsmem[];
   const uint32_t raw = smem_addr(tsmem);
@@ -434,7 +447,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   const long long grp = cluster_id_x();
   // the row tiles of one column tile are neighbours in launch order, so they run
   // together and all but the first find the weight boxes in L2
-  const long long m0 = (grp % tiles_m) * T::BM, n0 = (grp / tiles_m) * TC_BN;
+  const long long m0 = (grp % tiles_m) * T::BM, n0 = (grp / tiles_m) * BN;
   const long long total = (a.K + TC_BK - 1) / TC_BK;
   const long long s_begin = total * rank / split;
   const long long stages = total * (rank + 1) / split - s_begin;
@@ -516,8 +529,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
             asm volatile(
                 "{\n\t.reg .pred p;\n\t"
                 "setp.ne.u32 p, %4, 0;\n\t"
-                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + (uint32_t)(hf * TC_BN)),
-                "l"(da), "l"(db), "r"(TC_IDESC), "r"(acc)
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + (uint32_t)(hf * BN)),
+                "l"(da), "l"(db), "r"(T::IDESC), "r"(acc)
                 : "memory");
           }
         }
@@ -565,7 +578,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
           "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
           "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
           "=r"(v[30]), "=r"(v[31])
-        : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(hf * TC_BN + c0)));
+        : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(hf * BN + c0)));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
   };
   if (split == 1) {
@@ -576,7 +589,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
       if (rows_here == 0) break;  // uniform across the CTA
       __nv_bfloat16* yr = a.y + (m0 + hf * TC_BM + r) * a.ldy;
 #pragma unroll 1
-      for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        const int cw = BN - c0 < 32 ? BN - c0 : 32;  // columns of the tile in this load
         uint32_t v[32];
         if (have && !dead) {
           tmem_load(hf, c0, v);
@@ -586,7 +600,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
         }
         if (r >= rows_here) continue;
         const long long n = n0 + c0;
-        if (a.y_vec && n + 32 <= a.N) {
+        if (a.y_vec && n + cw <= a.N) {
           uint32_t p[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -595,11 +609,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
           }
           uint4* dst = reinterpret_cast<uint4*>(yr + n);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)
+            if (8 * q < cw) dst[q] = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (n + j < a.N) yr[n + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            if (j < cw && n + j < a.N) yr[n + j] = __float2bfloat16_rn(__uint_as_float(v[j]));
         }
       }
     }
@@ -618,7 +633,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   for (int hf = 0; hf < MH; ++hf) {
     const int rows_here = rows_of(hf);
 #pragma unroll 1
-    for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      const int cw = BN - c0 < 32 ? BN - c0 : 32;  // columns of the tile in this load
       uint32_t v[32];
       if (have && !dead && rows_here > 0) {
         tmem_load(hf, c0, v);
@@ -627,11 +643,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
         for (int j = 0; j < 32; ++j) v[j] = 0u;
       }
       if (r < rows_here) {
-        float4* dst = reinterpret_cast<float4*>(red + r * TC_RED_LD + c0);
+        float4* dst = reinterpret_cast<float4*>(red + r * T::RED_LD + c0);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          if (4 * q < cw)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
       }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -642,12 +659,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
     }
     // this CTA's share of the half: (row, 4-column group) pairs in row-major order, each
     // summed over the cluster's partials with 16-byte loads and stored as 4 bf16
-    constexpr int CQ = TC_BN / 4;
+    constexpr int CQ = BN / 4;
     const int E = rows_here * CQ;
     const int e_end = (int)((long long)E * (rank + 1) / split);
     for (int e = (int)((long long)E * rank / split) + threadIdx.x; e < e_end; e += TC_THREADS) {
       const int rr = e / CQ, cq = e % CQ;
-      const float4 v4 = cluster_sum4(red + rr * TC_RED_LD + 4 * cq, split);
+      const float4 v4 = cluster_sum4(red + rr * T::RED_LD + 4 * cq, split);
       const long long n = n0 + 4 * cq;
       __nv_bfloat16* yr = a.y + (m0 + hf * TC_BM + rr) * a.ldy;
       if (a.y_vec8 && n + 4 <= a.N) {
@@ -783,19 +800,20 @@ int lin_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStrea
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
-// The launch of the tcgen05 tile with MH row halves: the K split (cluster size) the
-// time model picks and its modelled time (us).
+// The launch of one tcgen05 tile shape (MH row halves, BN columns): the K split
+// (cluster size) the time model picks and its modelled time (us).
 struct TcPlan {
+  int mh = 1, bn = 256;
   long long tiles_m = 0, groups = 0, split = 1;
   double cost = 1e300;
 };
 
-template <int MH>
+template <int MH, int BN>
 int tc_plan(const LinArgs& a, TcPlan* plan) {
-  using T = TcShape<MH>;
-  const long long tiles_m = (a.M + T::BM - 1) / T::BM, tiles_n = (a.N + TC_BN - 1) / TC_BN;
+  using T = TcShape<MH, BN>;
+  const long long tiles_m = (a.M + T::BM - 1) / T::BM, tiles_n = (a.N + BN - 1) / BN;
   const long long groups = tiles_m * tiles_n;  // output tiles: clusters of one K part
-  if (cudaFuncSetAttribute(kda_linear_tc_kernel<MH>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
+  if (cudaFuncSetAttribute(kda_linear_tc_kernel<MH, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
       cudaSuccess)
     return KDA_ECUDA;
   static std::atomic<int> cluster_cache[64][LIN_MAX_SPLIT + 1];  // by cluster size, as above (per tile shape)
@@ -811,8 +829,12 @@ int tc_plan(const LinArgs& a, TcPlan* plan) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const long long stages = (a.K + TC_BK - 1) / TC_BK;
-  const TcModel& m = TC_MODEL[MH - 1];
+  constexpr TcModel m = TC_MODEL;
   const double tile_rows = (double)(a.M < T::BM ? a.M : T::BM);
+  constexpr double area = MH * BN / 256.0, bytes = T::STAGE / 49152.0;  // relative to 128 x 256 x 64, 48 KB
+  const double fixed = m.fixed + (MH == 2 ? m.fixed_two_halves : 0.0) + m.fixed_row * tile_rows * (BN / 256.0);
+  plan->mh = MH;
+  plan->bn = BN;
   plan->tiles_m = tiles_m;
   plan->groups = groups;
   for (int c = 1; c <= LIN_MAX_SPLIT && c <= stages; ++c) {
@@ -821,12 +843,12 @@ int tc_plan(const LinArgs& a, TcPlan* plan) {
     if (held <= 0) {
       int sms = 0, per_sm = 0;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_tc_kernel<MH>, TC_THREADS, T::SMEM) !=
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_linear_tc_kernel<MH, BN>, TC_THREADS, T::SMEM) !=
               cudaSuccess)
         return KDA_ECUDA;
       attr[0].val.clusterDim.x = (unsigned)cs;
       cfg.gridDim = dim3((unsigned)cs, 1, 1);
-      if (cudaOccupancyMaxActiveClusters(&held, kda_linear_tc_kernel<MH>, &cfg) != cudaSuccess) return KDA_ECUDA;
+      if (cudaOccupancyMaxActiveClusters(&held, kda_linear_tc_kernel<MH, BN>, &cfg) != cudaSuccess) return KDA_ECUDA;
       // never more clusters than the resident CTA slots hold
       const int cap = sms * (per_sm > 0 ? per_sm : 1) / cs;
       if (held > cap) held = cap;
@@ -839,22 +861,21 @@ int tc_plan(const LinArgs& a, TcPlan* plan) {
     const double whole = (double)((groups + held - 1) / held), tail = w - (whole - 1.0);
     const double waves = w <= 1.0 ? 1.0 : (tail >= 0.5 ? w : whole);
     const double running = (double)(groups < held ? groups : held) * c;
-    double s = m.mma > m.sm_intake ? m.mma : m.sm_intake;
-    if (running * m.l2_share > s) s = running * m.l2_share;
-    const double cost =
-        waves * ((double)stages / c * s + m.fixed + m.fixed_row * tile_rows + (c > 1 ? m.reduce : 0.0));
+    double s = m.mma * area > m.sm_intake * bytes ? m.mma * area : m.sm_intake * bytes;
+    if (running * m.l2_share * bytes > s) s = running * m.l2_share * bytes;
+    const double cost = waves * ((double)stages / c * s + fixed + (c > 1 ? m.reduce * area : 0.0));
     if (cost < plan->cost * (1.0 - 1e-9)) plan->cost = cost, plan->split = c;
   }
   return KDA_OK;
 }
 
-template <int MH>
+template <int MH, int BN>
 int tc_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl, const TcPlan& p) {
   CUtensorMap tmx, tmw;
-  if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, TC_BN)) return KDA_ECUDA;
+  if (!encode_map(&tmx, x, a.M, a.K, ldx, TC_BM) || !encode_map(&tmw, w, a.N, a.K, a.K, BN)) return KDA_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(TC_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = TcShape<MH>::SMEM;
+  cfg.dynamicSmemBytes = TcShape<MH, BN>::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -867,23 +888,45 @@ int tc_launch(const void* x, long long ldx, const void* w, LinArgs a, cudaStream
   cfg.numAttrs = pdl ? 2 : 1;
   if (p.groups * p.split > 0x7fffffffLL) return KDA_EINVAL;
   cfg.gridDim = dim3((unsigned)(p.groups * p.split), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel<MH>, tmx, tmw, a, (int)p.tiles_m) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, kda_linear_tc_kernel<MH, BN>, tmx, tmw, a, (int)p.tiles_m) != cudaSuccess)
     return KDA_ECUDA;
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
-// The tcgen05 tiles: one or two 128-row halves a CTA, whichever the time model rates
-// faster for this shape (two halves cut the bytes a product but halve the tiles).
-int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl) {
-  TcPlan p1, p2;
-  int rc = tc_plan<1>(a, &p1);
-  if (rc != KDA_OK) return rc;
-  if (a.M > TC_BM) {
-    rc = tc_plan<2>(a, &p2);
-    if (rc != KDA_OK) return rc;
+int tc_dispatch(const void* x, long long ldx, const void* w, const LinArgs& a, cudaStream_t st, bool pdl,
+                const TcPlan& p) {
+  if (p.mh == 2) {
+    if (p.bn == 192) return tc_launch<2, 192>(x, ldx, w, a, st, pdl, p);
+    return tc_launch<2, 256>(x, ldx, w, a, st, pdl, p);
   }
-  if (p2.cost < p1.cost) return tc_launch<2>(x, ldx, w, a, st, pdl, p2);
-  return tc_launch<1>(x, ldx, w, a, st, pdl, p1);
+  if (p.bn == 192) return tc_launch<1, 192>(x, ldx, w, a, st, pdl, p);
+  if (p.bn == 128) return tc_launch<1, 128>(x, ldx, w, a, st, pdl, p);
+  return tc_launch<1, 256>(x, ldx, w, a, st, pdl, p);
+}
+
+template <int MH, int BN>
+int tc_consider(const LinArgs& a, TcPlan* best) {
+  TcPlan p;
+  const int rc = tc_plan<MH, BN>(a, &p);
+  if (rc == KDA_OK && p.cost < best->cost) *best = p;
+  return rc;
+}
+
+// The tcgen05 tiles: the shape and K split the time model rates fastest -- one or
+// two 128-row halves (two halves cut the bytes a product but halve the tiles) of
+// 256, 192 or (one half) 128 columns (narrower tiles give more CTAs where the tiles
+// are few).  Two halves of 128 columns move the bytes of one half of 256 with a
+// larger fixed part, and never measured faster, so they are not built.
+int lin_launch_tc(const void* x, long long ldx, const void* w, LinArgs a, cudaStream_t st, bool pdl) {
+  TcPlan best;
+  int rc = KDA_OK;
+  if ((rc = tc_consider<1, 256>(a, &best)) != KDA_OK || (rc = tc_consider<1, 192>(a, &best)) != KDA_OK ||
+      (rc = tc_consider<1, 128>(a, &best)) != KDA_OK)
+    return rc;
+  if (a.M > TC_BM) {
+    if ((rc = tc_consider<2, 256>(a, &best)) != KDA_OK || (rc = tc_consider<2, 192>(a, &best)) != KDA_OK) return rc;
+  }
+  return tc_dispatch(x, ldx, w, a, st, pdl, best);
 }
 
 }  // namespace

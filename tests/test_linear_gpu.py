@@ -1,9 +1,9 @@
 """kda_linear (the in_proj / o_proj projections) against the projection
 oracle: bf16 outputs within one bf16 step of the correctly rounded product,
 plus the fp32 accumulation's share (2^-14 of sum |x_k w_k|); the in_proj and
-o_proj shapes of the 12-head layer through all three kernels (rows <= 16,
-17..64, > 64 on tcgen05), ragged column tails (odd N), ragged K, K splits, a
-strided x."""
+o_proj shapes of the 12-head layer through the 16-row mma.sync tile (rows <=
+16) and every tcgen05 tile shape (more rows), ragged column tails (odd N),
+ragged K, K splits, a strided x."""
 from __future__ import annotations
 
 import numpy as np
@@ -74,6 +74,15 @@ def test_row_tile_boundaries_ragged_k_and_k_splits(rows, K, N):
     # split K eight ways; K = 128 is a single stage, so no split; 300 and 257 rows: three
     # tcgen05 row tiles, the last one mostly past the end
     _check(rows, K, N, seed=rows * 1000 + N, xcols=K + 8)
+
+
+@pytest.mark.parametrize("rows,K,N", [(17, 1536, 7168), (130, 256, 20000), (520, 256, 12000)])
+def test_each_tile_shape(rows, K, N):
+    # shapes that the launcher's time model sends (on 152 SMs) to the 128 x 256 tile with a
+    # five-way K split, the 256 x 192 two-half tile, and the 256 x 256 two-half tile, so that
+    # every tcgen05 instance is compared with the oracle (the other shapes in this file take
+    # the 128 x 192 and 128 x 128 tiles and the 16-row mma.sync tile)
+    _check(rows, K, N, seed=rows + N, xcols=K + 8)
 
 
 def test_rejects_bad_shapes():
