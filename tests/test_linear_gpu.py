@@ -76,12 +76,25 @@ def test_row_tile_boundaries_ragged_k_and_k_splits(rows, K, N):
     _check(rows, K, N, seed=rows * 1000 + N, xcols=K + 8)
 
 
-@pytest.mark.parametrize("rows,K,N", [(17, 1536, 7168), (130, 256, 20000), (520, 256, 12000)])
+# Shapes that the launcher's time model sends (on 152 SMs) to each tcgen05 tile instance,
+# unsplit and with a K split, every one with a ragged last column tile and (most) a ragged
+# last k stage, so that every instance and both epilogues are compared with the oracle:
+# rows x columns of the tile, K split
+TILE_SHAPES = [
+    (17, 328, 1000),      # 128 x 128, C = 6
+    (17, 200, 19648),     # 128 x 192, C = 1
+    (17, 1000, 6439),     # 128 x 192, C = 4
+    (130, 200, 14986),    # 128 x 256, C = 1
+    (17, 1000, 10324),    # 128 x 256, C = 3
+    (130, 200, 19648),    # 256 x 192, C = 1
+    (130, 8200, 4829),    # 256 x 192, C = 5
+    (257, 200, 16540),    # 256 x 256, C = 1
+    (130, 7176, 7160),    # 256 x 256, C = 5
+]
+
+
+@pytest.mark.parametrize("rows,K,N", TILE_SHAPES)
 def test_each_tile_shape(rows, K, N):
-    # shapes that the launcher's time model sends (on 152 SMs) to the 128 x 256 tile with a
-    # five-way K split, the 256 x 192 two-half tile, and the 256 x 256 two-half tile, so that
-    # every tcgen05 instance is compared with the oracle (the other shapes in this file take
-    # the 128 x 192 and 128 x 128 tiles and the 16-row mma.sync tile)
     _check(rows, K, N, seed=rows + N, xcols=K + 8)
 
 
