@@ -452,6 +452,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   const long long s_begin = total * rank / split;
   const long long stages = total * (rank + 1) / split - s_begin;
 
+  // Thread 0 is also the producer's issuing lane (warp 0, lane 0): its cache policies, and
+  // the stages whose weight box it puts in flight at once.
+  unsigned long long w_policy = 0, x_policy = 0;
+  const long long early = stages < TC_STAGES ? stages : TC_STAGES;
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
@@ -462,6 +466,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
     mbar_init(accum_bar, 1);
     *consumed_p = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the weight tile is read once when there is one row tile (evict first), else kept for the others
+    if (a.M <= T::BM)
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w_policy));
+    else
+      asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(w_policy));
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(x_policy));
+    // The weight boxes of the first stages depend on no earlier kernel: they go out
+    // before the tensor memory, the barrier and (as a dependent launch) the wait for x.
+    // Each stage's barrier expects the whole stage; its x boxes follow in the loop below.
+    for (long long s0 = 0; s0 < early; ++s0) {
+      const uint32_t bar = full0 + 8 * (uint32_t)s0;
+      mbar_expect_tx(bar, TC_STAGE);
+      tma_box(ring + (uint32_t)s0 * TC_STAGE + MH * TC_ABYTES, &tmw, (int)((s_begin + s0) * TC_BK), (int)n0, bar,
+              w_policy);
+    }
   }
   if (warp == 0) {  // the accumulators: 128 lanes x 256 fp32 columns of tensor memory a half
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot),
@@ -473,22 +492,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot_p;
-  // As a programmatic dependent (a layer plan's o_proj) the set-up above
-  // overlaps the previous kernel's tail; x is its output. Otherwise a no-op.
+  // As a programmatic dependent (a layer plan's o_proj) the set-up above and the
+  // first weight boxes overlap the previous kernel's tail; x is its output.
+  // Otherwise a no-op.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Warps 0 and 1 run their loops whole (converged, spinning on the barrier
   // without the sleep hint: a suspended thread wakes late), lane 0 issuing.
   bool ok_all = true;
   long long issued = 0;
-  if (warp == 0) {  // producer
-    // the weight tile is read once when there is one row tile (evict first), else kept for the others
-    unsigned long long w_policy, x_policy;
-    if (a.M <= T::BM)
-      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w_policy));
-    else
-      asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(w_policy));
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(x_policy));
+  if (warp == 0) {  // producer (the first round's empty waits pass at once: every early stage gets its x)
     for (long long s = 0; s < stages; ++s) {
       const uint32_t slot = (uint32_t)(s % TC_STAGES);
       const bool ok = mbar_wait_bounded(empty0 + 8 * slot, (unsigned)(((s / TC_STAGES) & 1) ^ 1));
@@ -499,10 +512,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_linear_tc_kernel(const __gr
       if (lane == 0) {
         const uint32_t st = ring + slot * TC_STAGE, bar = full0 + 8 * slot;
         const int k = (int)((s_begin + s) * TC_BK);
-        mbar_expect_tx(bar, TC_STAGE);  // the x box of each half and the weight box
+        if (s >= early) {  // the x box of each half and the weight box
+          mbar_expect_tx(bar, TC_STAGE);
+          tma_box(st + MH * TC_ABYTES, &tmw, k, (int)n0, bar, w_policy);
+        }
 #pragma unroll
         for (int hf = 0; hf < MH; ++hf) tma_box(st + hf * TC_ABYTES, &tmx, k, (int)(m0 + hf * TC_BM), bar, x_policy);
-        tma_box(st + MH * TC_ABYTES, &tmw, k, (int)n0, bar, w_policy);
       }
       __syncwarp();
       issued = s + 1;
