@@ -196,21 +196,35 @@ struct LinArgs {
   int y_vec8;            // y and ldy allow 8-byte stores (y 8-byte aligned, ldy % 4 == 0)
 };
 
-// Issued by one thread: the x and weight boxes of stage k0 .. k0 + KS into
-// ring slot `st`, all completing on `bar`.
+// Issued by one thread: the weight boxes of stage k0 .. k0 + KS into ring slot
+// `st`, with `bar` told to expect the whole stage (weight and x boxes).
+template <int MB, int NB>
+__device__ __forceinline__ void issue_stage_w(const LinArgs& a, const CUtensorMap* tmw, uint32_t st, uint32_t bar,
+                                              long long n0, long long k0) {
+  using T = LinShape<MB, NB>;
+  unsigned long long w_policy;  // the weight is read once
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w_policy));
+  mbar_expect_tx(bar, T::NBOX * (a.x_box_bytes + T::WBOX));
+#pragma unroll
+  for (int b = 0; b < T::NBOX; ++b)
+    tma_box(st + T::NBOX * T::XBOX + b * T::WBOX, tmw, (int)(k0 + b * LIN_BOXK), (int)n0, bar, w_policy);
+}
+// ... and its x boxes.
+template <int MB, int NB>
+__device__ __forceinline__ void issue_stage_x(const CUtensorMap* tmx, uint32_t st, uint32_t bar, long long m0,
+                                              long long k0) {
+  using T = LinShape<MB, NB>;
+  unsigned long long x_policy;  // x is read by every CTA
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(x_policy));
+#pragma unroll
+  for (int b = 0; b < T::NBOX; ++b) tma_box(st + b * T::XBOX, tmx, (int)(k0 + b * LIN_BOXK), (int)m0, bar, x_policy);
+}
+// The x and weight boxes of stage k0 .. k0 + KS into ring slot `st`, all completing on `bar`.
 template <int MB, int NB>
 __device__ __forceinline__ void issue_stage(const LinArgs& a, const CUtensorMap* tmx, const CUtensorMap* tmw,
                                             uint32_t st, uint32_t bar, long long m0, long long n0, long long k0) {
-  using T = LinShape<MB, NB>;
-  unsigned long long w_policy, x_policy;  // the weight is read once, x by every CTA
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w_policy));
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(x_policy));
-  mbar_expect_tx(bar, T::NBOX * (a.x_box_bytes + T::WBOX));
-#pragma unroll
-  for (int b = 0; b < T::NBOX; ++b) {
-    tma_box(st + b * T::XBOX, tmx, (int)(k0 + b * LIN_BOXK), (int)m0, bar, x_policy);
-    tma_box(st + T::NBOX * T::XBOX + b * T::WBOX, tmw, (int)(k0 + b * LIN_BOXK), (int)n0, bar, w_policy);
-  }
+  issue_stage_w<MB, NB>(a, tmw, st, bar, n0, k0);
+  issue_stage_x<MB, NB>(tmx, st, bar, m0, k0);
 }
 
 template <int MB, int NB>
@@ -234,16 +248,23 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
   // ldmatrix row addresses: lane l feeds row l & 7 of 8x8 matrix l >> 3
   const int lr = lane & 7, lm = lane >> 3;
 
+  // the first pass's prologue stages, whose weight boxes go out at once: they depend
+  // on no earlier kernel (the x boxes follow after the dependent-launch wait)
+  const long long early = stages < STAGES - 1 ? stages : STAGES - 1;
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmw)) : "memory");
     for (int i = 0; i < STAGES; ++i) mbar_init(bar0 + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (long long s = 0; s < early; ++s)
+      issue_stage_w<MB, NB>(a, &tmw, ring_s + (uint32_t)s * T::STAGE, bar0 + 8 * (uint32_t)s, n0,
+                            (s_begin + s) * T::KS);
   }
   __syncthreads();
 
-  // As a programmatic dependent (a layer plan's o_proj) the set-up above
-  // overlaps the previous kernel's tail; x is its output. Otherwise a no-op.
+  // As a programmatic dependent (a layer plan's o_proj) the set-up above and the
+  // first weight boxes overlap the previous kernel's tail; x is its output.
+  // Otherwise a no-op.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   bool dead = false;  // a copy wait gave up: no more copies, outputs not meaningful
   long long g0 = 0;   // ring stages used by earlier passes (slot and phase bookkeeping)
@@ -255,8 +276,11 @@ __global__ void __launch_bounds__(LinShape<MB, NB>::THREADS) kda_linear_kernel(
     if (threadIdx.x == 0) {  // ring prologue: stages 0 .. STAGES-2 in flight
       for (int s = 0; s < STAGES - 1 && s < run; ++s) {
         const uint32_t slot = (uint32_t)((g0 + s) % STAGES);
-        issue_stage<MB, NB>(a, &tmx, &tmw, ring_s + slot * T::STAGE, bar0 + 8 * slot, m0, n0,
-                            (s_begin + s) * T::KS);
+        if (g0 == 0 && s < early)  // the first pass: its weight boxes are already out
+          issue_stage_x<MB, NB>(&tmx, ring_s + slot * T::STAGE, bar0 + 8 * slot, m0, (s_begin + s) * T::KS);
+        else
+          issue_stage<MB, NB>(a, &tmx, &tmw, ring_s + slot * T::STAGE, bar0 + 8 * slot, m0, n0,
+                              (s_begin + s) * T::KS);
       }
     }
     long long issued = run < STAGES - 1 ? run : STAGES - 1;
