@@ -170,7 +170,7 @@ class DeviceWorkload:
     read slots filled from the seeded generator)."""
 
     def __init__(self, si: I.StepInputs, device, gate_mode: int = 0, plan: bool = False, state_dtype: str = "f32",
-                 prep=None):
+                 prep=None, v_split: int = 1):
         import torch
         import linear_attention_decode_03_gb300 as kda
 
@@ -187,7 +187,7 @@ class DeviceWorkload:
             bf16(wt.conv_w), None if wt.bias is None else bf16(wt.bias), bf16(wt.f_b),
             torch.from_numpy(wt.A_log).to(device), torch.from_numpy(wt.dt_bias).to(device),
             torch.from_numpy(wt.o_norm).to(device), gate_lower_bound=wt.gate_lower_bound,
-            eps=wt.eps, conv_dim_first=True, gate_mode=gate_mode, state_dtype=state_dtype)
+            eps=wt.eps, conv_dim_first=True, gate_mode=gate_mode, state_dtype=state_dtype, v_split=v_split)
         self.projected = bf16(si.projected)
         idx = torch.from_numpy(si.read_slots).to(device)
         if state_dtype == "bf16":
@@ -359,6 +359,7 @@ def workload_config(w: I.Workload, args):
             "parallelism": "replicas" if args.gpus > 1 else "single GPU",
             "gate": getattr(args, "gate_mode", "sigmoid"),
             "launch": getattr(args, "launch", "direct"),
+            "v_split": getattr(args, "v_split", 1),
             "state_storage": getattr(args, "state_dtype", "f32")}
 
 
@@ -575,7 +576,7 @@ def run_layer(args, w: I.Workload):
     kda.load_library()
     si = I.make_step_inputs(w)
     dw = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1,
-                        state_dtype=args.state_dtype)
+                        state_dtype=args.state_dtype, v_split=args.v_split)
     rng = np.random.Generator(np.random.PCG64(w.seed + 29))
     xb = I.to_bf16_bits(rng.normal(0.0, 1.0, size=(w.rows, HIDDEN)).astype(np.float32))
     wib = I.to_bf16_bits(rng.normal(0.0, 0.02, size=(w.pitch, HIDDEN)).astype(np.float32))
@@ -753,7 +754,7 @@ def make_copies(si: I.StepInputs, device, args, n: int):
     weight handle (the layer's weights are the same for every copy)."""
     plan = args.launch == "plan"
     first = DeviceWorkload(si, device, gate_mode=0 if args.gate_mode == "sigmoid" else 1, plan=plan,
-                           state_dtype=args.state_dtype)
+                           state_dtype=args.state_dtype, v_split=getattr(args, "v_split", 1))
     return [first] + [DeviceWorkload(si, device, plan=plan, state_dtype=args.state_dtype, prep=first.prep)
                       for _ in range(n - 1)]
 
@@ -943,6 +944,8 @@ def main():
     ap.add_argument("--layer-pdl", choices=["none", "step_edge", "o_proj_edge", "both"], default="step_edge",
                     help="--op layer: the edges of the timed graph launched as programmatic dependents "
                          "(the others are timed too and reported under layer_ms)")
+    ap.add_argument("--v-split", type=int, choices=[1, 2], default=1,
+                    help="CTAs a (request, head) (kda_set_v_split); 2 splits the v rows over a cluster of two")
     ap.add_argument("--gate-mode", choices=["sigmoid", "softplus"], default="sigmoid",
                     help="decay gate form (kda_set_gate_mode); the default is the reading the step follows")
     args = ap.parse_args()

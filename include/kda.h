@@ -175,6 +175,23 @@ int kda_set_gate_mode(kda_handle* handle, int mode);
 int kda_set_state_dtype(kda_handle* handle, int dtype);
 
 /*
+ * kda_set_v_split -- how many CTAs share one (request, head) of a step: 1
+ * (default), or 2 in a thread-block cluster, each owning 64 of the 128 v rows
+ * of the state (one recurrence pass, half the state copy and half the
+ * outputs; both run the conv, the gates and the l2norm, and they swap their
+ * halves of o through distributed shared memory for the RMSNorm).  The K1
+ * page splits a head's state rows over several workers (8 v-chunks of 16
+ * rows); here the split is a launch option, and on GB300 it is slower on every
+ * workload measured (the halves repeat the prologue, and the doubled grid of
+ * three-per-SM CTAs needs more waves), so it is off unless asked for.  It
+ * applies to the window-first conv layout (conv_dim_first = 1); the other
+ * layout always runs one CTA.  Results are the same either way.  Applies to
+ * steps enqueued (and plans made) after the call.  Returns KDA_OK, or
+ * KDA_EINVAL for a NULL handle or another value.  No CUDA call.
+ */
+int kda_set_v_split(kda_handle* handle, int v_split);
+
+/*
  * Launch plans.  A plan records one kda_step, with exactly these arguments,
  * as a CUDA graph (captured once on a private stream and instantiated), so
  * that each later step is a single graph launch: the analogue of the

@@ -8,7 +8,7 @@ missing or fails to load, every call raises.
 
 Low-level functions carry the C names (:func:`kda_prepare`, :func:`kda_step`,
 :func:`kda_check`, :func:`kda_destroy`, :func:`kda_strerror`,
-:func:`kda_launch_info`, :func:`kda_set_gate_mode`, :func:`kda_plan_create`,
+:func:`kda_launch_info`, :func:`kda_set_gate_mode`, :func:`kda_set_v_split`, :func:`kda_plan_create`,
 :func:`kda_plan_launch`, :func:`kda_plan_destroy`) and take raw device pointers.  :class:`PreparedKda`
 mirrors the PreparedKda wrapper on the
 "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.kda.prepared" page:
@@ -28,7 +28,7 @@ from ._build import DEBUG_LIB_PATH, LIB_PATH, build
 __all__ = [
     "KdaError", "build", "load_library", "kda_prepare", "kda_step", "kda_check", "kda_destroy",
     "kda_strerror", "kda_launch_info", "kda_set_gate_mode", "kda_plan_create", "kda_layer_plan_create", "kda_plan_launch",
-    "kda_plan_destroy", "kda_set_state_dtype", "kda_linear", "kda_linear_check", "linear", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_PDL_STEP", "KDA_PDL_O_PROJ", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
+    "kda_plan_destroy", "kda_set_state_dtype", "kda_set_v_split", "kda_linear", "kda_linear_check", "linear", "PreparedKda", "KdaPlan", "KDA_STATE_F32", "KDA_STATE_BF16", "KDA_PDL_STEP", "KDA_PDL_O_PROJ", "KDA_ERR_SLOT", "KDA_ERR_ACCEPTED",
     "KDA_ERR_TIMEOUT", "KDA_ERR_DUPLICATE", "KDA_MAX_TOKENS", "DEBUG_LIB_PATH", "KDA_GATE_SIGMOID", "KDA_GATE_SOFTPLUS", "HEAD_DIM",
 ]
 
@@ -83,6 +83,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_plan_destroy.restype = None
     lib.kda_set_state_dtype.argtypes = [vp, i32]
     lib.kda_set_state_dtype.restype = i32
+    lib.kda_set_v_split.argtypes = [vp, i32]
+    lib.kda_set_v_split.restype = i32
     lib.kda_linear.argtypes = [vp, ll, ll, vp, ll, ll, vp, ll, vp]
     lib.kda_linear.restype = i32
     lib.kda_linear_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -195,6 +197,13 @@ def kda_set_state_dtype(handle: int, dtype: int) -> None:
         raise KdaError("kda_set_state_dtype", rc)
 
 
+def kda_set_v_split(handle: int, v_split: int) -> None:
+    """1 (default) or 2 CTAs a (request, head) for the handle's later steps (see include/kda.h)."""
+    rc = load_library().kda_set_v_split(handle, int(v_split))
+    if rc != KDA_OK:
+        raise KdaError("kda_set_v_split", rc)
+
+
 def kda_set_gate_mode(handle: int, mode: int) -> None:
     """KDA_GATE_SIGMOID (default) or KDA_GATE_SOFTPLUS for the handle's later steps."""
     rc = load_library().kda_set_gate_mode(handle, int(mode))
@@ -244,12 +253,14 @@ class PreparedKda:
     to fp32 as the page's __init__ does).  ``gate_mode`` picks the decay gate
     (``KDA_GATE_SIGMOID``, the default, or ``KDA_GATE_SOFTPLUS``; see
     ``include/kda.h``); ``state_dtype`` the state pool's storage type ("f32",
-    the default, or "bf16": computed in fp32, each stored state rounded).
+    the default, or "bf16": computed in fp32, each stored state rounded);
+    ``v_split`` the CTAs a (request, head) (1, the default, or 2; see
+    ``kda_set_v_split`` in ``include/kda.h``).
     """
 
     def __init__(self, conv_w, conv_bias, f_b, A_log, dt_bias, o_norm, *, gate_lower_bound: float = -5.0,
                  eps: float = 1e-6, conv_dim_first: bool = True, gate_mode: int = KDA_GATE_SIGMOID,
-                 state_dtype: str = "f32"):
+                 state_dtype: str = "f32", v_split: int = 1):
         import torch
 
         self.heads = int(A_log.numel())
@@ -280,6 +291,8 @@ class PreparedKda:
             self.state_dtype = state_dtype
             if state_dtype == "bf16":
                 kda_set_state_dtype(self.handle, KDA_STATE_BF16)
+            if v_split != 1:
+                kda_set_v_split(self.handle, v_split)
 
     def _args(self, projected, out, caches, slots, accepted):
         """kda_step's arguments (pointers and sizes) for these tensors, and the

@@ -479,8 +479,37 @@ __device__ __forceinline__ float conv_dot(const ConvLane<N>& q, float& run) {
   return y;
 }
 
+// Thread-block cluster helpers for the two-CTA split of a (request, head).
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster: writes before it are seen by reads after it.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 8 bytes of CTA `rank`'s shared memory at the address that `p` has in this CTA.
+__device__ __forceinline__ uint2 ld_peer_u2(const void* p, unsigned rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_peer_s32(const void* p, unsigned rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // DF: conv_state laid out [pool, 3D, W-1] (true) or [pool, W-1, 3D] (false).
-template <int L, bool BS, bool DF>
+// VS: the CTAs of a (request, head) -- 1, or 2 in a cluster, each owning 64 of the 128
+// v rows (one pass of the recurrence) and half of the outputs; both run the prologue
+// and swap their halves of o through distributed shared memory for the RMSNorm.
+template <int L, bool BS, bool DF, int VS>
 __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(const StepArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using S = Smem<L, BS>;
@@ -503,8 +532,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + S::mbar);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x % a.heads;
-  const long long r = blockIdx.x / a.heads;
+  static_assert(VS == 1 || VS == 2, "one or two CTAs a (request, head)");
+  const unsigned slice = VS == 1 ? 0u : cluster_rank();  // which 64 v rows (VS = 2)
+  const long long task = (long long)blockIdx.x / VS;    // the clusters of a launch are consecutive blocks
+  const int h = (int)(task % a.heads);
+  const long long r = task / a.heads;
   const long long row0 = r * L;
   const int D = a.D, SL = a.W - 1;
 
@@ -586,9 +618,10 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       if (tid == 0) atomicOr(a.err, KDA_ERR_SLOT);
     }
   }
-  if (status == TASK_PADDING) {  // zero output rows, no cache traffic
-    for (int i = tid; i < L * HD; i += THREADS)
-      a.out[(row0 + i / HD) * D + h * HD + (i % HD)] = __float2bfloat16_rn(0.0f);
+  if (status == TASK_PADDING) {  // zero output rows (this CTA's columns), no cache traffic
+    constexpr int CW = HD / VS;
+    for (int i = tid; i < L * CW; i += THREADS)
+      a.out[(row0 + i / CW) * D + h * HD + slice * CW + (i % CW)] = __float2bfloat16_rn(0.0f);
     return;
   }
   if (status != TASK_OK) return;
@@ -632,6 +665,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   // once; verify (often a single wave of CTAs, all in this phase together)
   // first waits for the conv inputs, which would otherwise queue behind every
   // CTA's state copies, and has its conv and gates to cover the state's latency.
+  const int Q0 = (int)slice * (QUARTERS / VS);  // this CTA's first quarter of the state
   auto issue_state = [&]() {
     if (tid == 0) {
       const unsigned char* src = static_cast<const unsigned char*>(a.state_pool) +
@@ -640,7 +674,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       for (int q = 0; q < QUARTERS; ++q) mbar_init(smem_u32(&mbar[q]), 1);
       fence_mbar_init();
 #pragma unroll
-      for (int q = 0; q < QUARTERS; ++q) {
+      for (int q = Q0; q < Q0 + QUARTERS / VS; ++q) {  // this CTA's quarters
         const uint32_t bar = smem_u32(&mbar[q]);
         mbar_expect_tx(bar, SB::QBYTES);
         bulk_load(smem_u32(stc + q * SB::QBYTES), src + q * SB::QBYTES, SB::QBYTES, bar);
@@ -815,7 +849,12 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     }
   }
   __syncthreads();
-  store_windows();
+  if constexpr (VS == 2) {
+    // Both CTAs read the start window, and it may be one of the windows written
+    // below: the other CTA's conv inputs are in its registers before slice 0 stores.
+    cluster_barrier();
+  }
+  if (VS == 1 || slice == 0) store_windows();  // the windows once per (request, head)
 
   // ---- recurrence: 2 passes of 2 quarters; 16 lanes per v row, 8 k values a lane --
   // Lane l: half hs = l >> 4 of the warp, kl = l & 15 owns k = 64 m + 4 kl + (0..3)
@@ -830,7 +869,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   // element (h, row, 64 m + 4 kl) of a slot's state, in bytes from the slot's block
   unsigned char* dst_k = static_cast<unsigned char*>(a.state_pool) + ((long long)h * STATE_FLOATS + kl * 4) * SB::ELEM;
 #pragma unroll 1
-  for (int pass = 0; pass < 2; ++pass) {
+  for (int pass = (int)slice; pass < (int)slice + 2 / VS; ++pass) {  // VS = 2: the CTA's one pass
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mbar[2 * pass]), 0) &&
                                                 mbar_wait_bounded(smem_u32(&mbar[2 * pass + 1]), 0));
     if (!ok) timed_out = true;
@@ -964,11 +1003,28 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     atomicOr(a.err, KDA_ERR_TIMEOUT);
   }
   __syncthreads();
+  if constexpr (VS == 2) {
+    // Both CTAs reach both cluster barriers, timed out or not. The first makes each
+    // CTA's half of o (and its timeout flag) visible to the other; each then copies the
+    // other's half into its own o; the second keeps each CTA's shared memory until the
+    // other has read it.
+    cluster_barrier();
+    const unsigned peer = slice ^ 1u;
+    constexpr int HALF = HD / 2;
+    for (int i = tid; i < L * HALF / 4; i += THREADS) {  // 4 bf16 a load
+      const int t = i / (HALF / 4), c = (int)peer * HALF + (i % (HALF / 4)) * 4;
+      *reinterpret_cast<uint2*>(ob + t * HD + c) = ld_peer_u2(ob + t * HD + c, peer);
+    }
+    const int peer_timeout = (tid == 0) ? ld_peer_s32(ctl, peer) : 0;
+    cluster_barrier();
+    if (tid == 0 && peer_timeout) ctl[0] = 1;  // either half timed out: the request's outputs are not written
+    __syncthreads();
+  }
   if (ctl[0] != 0) {
     // Give copies still in flight a second bounded chance to land before the
     // shared memory is released; the outputs of this request stay unwritten.
     if (tid == 0) {
-      for (int q = 0; q < QUARTERS; ++q) (void)mbar_wait_bounded(smem_u32(&mbar[q]), 0);
+      for (int q = Q0; q < Q0 + QUARTERS / VS; ++q) (void)mbar_wait_bounded(smem_u32(&mbar[q]), 0);
       if constexpr (L == 1) bulk_wait_read();
     }
     return;
@@ -987,7 +1043,8 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       y[e] = __float2bfloat16_rn(o[e] * rstd * wn[e] * __half2float(gsig_s[t * HD + lane * 4 + e]));
-    if (warp < L) *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
+    if (warp < L && (VS == 1 || (unsigned)(lane >> 4) == slice))  // VS = 2: this CTA's 64 columns
+      *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
   }
   if constexpr (L == 1) {
     if (tid == 0) bulk_wait_read();  // shared memory stays until the bulk stores have read it
@@ -1041,14 +1098,18 @@ __global__ void row_norms(const __nv_bfloat16* m, float* norms, int rows) {
 
 template <int L>
 cudaError_t set_smem_attr() {
-  const cudaError_t e[4] = {
-      cudaFuncSetAttribute(kda_step_kernel<L, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t e[6] = {
+      cudaFuncSetAttribute(kda_step_kernel<L, false, true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Smem<L, false>::bytes),
-      cudaFuncSetAttribute(kda_step_kernel<L, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(kda_step_kernel<L, true, true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Smem<L, true>::bytes),
-      cudaFuncSetAttribute(kda_step_kernel<L, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(kda_step_kernel<L, false, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Smem<L, false>::bytes),
-      cudaFuncSetAttribute(kda_step_kernel<L, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(kda_step_kernel<L, true, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Smem<L, true>::bytes),
+      cudaFuncSetAttribute(kda_step_kernel<L, false, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Smem<L, false>::bytes),
+      cudaFuncSetAttribute(kda_step_kernel<L, true, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Smem<L, true>::bytes)};
   for (cudaError_t x : e)
     if (x != cudaSuccess) return x;
@@ -1065,30 +1126,44 @@ cudaError_t set_all_smem_attrs() {
 }
 
 template <int L>
-cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream, bool bf16_state, bool pdl) {
+cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream, bool bf16_state, bool pdl, int vs) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.gridDim = dim3((unsigned)(ctas * vs), 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = bf16_state ? Smem<L, true>::bytes : Smem<L, false>::bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the previous kernel ends
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (vs == 2) {  // the two CTAs of a (request, head) as one cluster
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the previous kernel ends
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = n;
   cudaError_t e;
-  if (a.conv_dim_first)
-    e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true, true>, a)
-                   : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false, true>, a);
+  if (vs == 2)  // built for the window-first conv layout only
+    e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true, true, 2>, a)
+                   : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false, true, 2>, a);
+  else if (a.conv_dim_first)
+    e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true, true, 1>, a)
+                   : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false, true, 1>, a);
   else
-    e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true, false>, a)
-                   : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false, false>, a);
+    e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true, false, 1>, a)
+                   : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false, false, 1>, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int L>
 const void* kernel_fn() {
-  return reinterpret_cast<const void*>(kda_step_kernel<L, false, true>);
+  return reinterpret_cast<const void*>(kda_step_kernel<L, false, true, 1>);
 }
 
 bool aligned(const void* p, unsigned n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
@@ -1110,6 +1185,7 @@ struct kda_handle {
   float lb, eps;
   int gate_mode;
   int state_dtype;  // KDA_STATE_F32 or KDA_STATE_BF16
+  int v_split;      // 1 or 2 CTAs a (request, head)
 };
 
 extern "C" {
@@ -1154,6 +1230,7 @@ int kda_prepare(int heads, int conv_width, const void* conv_w, const void* bias,
   h->lb = gate_lower_bound;
   h->gate_mode = KDA_GATE_SIGMOID;
   h->state_dtype = KDA_STATE_F32;
+  h->v_split = 1;
   h->eps = eps;
   cudaError_t e = cudaGetDevice(&h->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device);
@@ -1242,16 +1319,21 @@ int step_enqueue(kda_handle* h, const void* projected, long long rows, long long
   debug_duplicate_slots<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(slots, rows, L, pool_slots, h->err);
   if (cudaGetLastError() != cudaSuccess) return KDA_ECUDA;
 #endif
+  // One CTA a (request, head) unless the handle asks for two (measured slower on every
+  // workload: each half repeats the prologue, and the doubled grid needs more waves).
+  int vs = h->v_split;
+  if (!a.conv_dim_first) vs = 1;  // the split is built for the window-first conv layout
+  if (vs * ctas > 0x7fffffffLL) return KDA_EINVAL;
   cudaError_t e;
   switch (L) {
-    case 1: e = launch<1>(a, ctas, s, bs, pdl); break;
-    case 2: e = launch<2>(a, ctas, s, bs, pdl); break;
-    case 3: e = launch<3>(a, ctas, s, bs, pdl); break;
-    case 4: e = launch<4>(a, ctas, s, bs, pdl); break;
-    case 5: e = launch<5>(a, ctas, s, bs, pdl); break;
-    case 6: e = launch<6>(a, ctas, s, bs, pdl); break;
-    case 7: e = launch<7>(a, ctas, s, bs, pdl); break;
-    default: e = launch<8>(a, ctas, s, bs, pdl); break;
+    case 1: e = launch<1>(a, ctas, s, bs, pdl, vs); break;
+    case 2: e = launch<2>(a, ctas, s, bs, pdl, vs); break;
+    case 3: e = launch<3>(a, ctas, s, bs, pdl, vs); break;
+    case 4: e = launch<4>(a, ctas, s, bs, pdl, vs); break;
+    case 5: e = launch<5>(a, ctas, s, bs, pdl, vs); break;
+    case 6: e = launch<6>(a, ctas, s, bs, pdl, vs); break;
+    case 7: e = launch<7>(a, ctas, s, bs, pdl, vs); break;
+    default: e = launch<8>(a, ctas, s, bs, pdl, vs); break;
   }
   return e == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
@@ -1350,6 +1432,12 @@ void kda_plan_destroy(kda_plan* p) {
 int kda_set_state_dtype(kda_handle* h, int dtype) {
   if (h == nullptr || (dtype != KDA_STATE_F32 && dtype != KDA_STATE_BF16)) return KDA_EINVAL;
   h->state_dtype = dtype;
+  return KDA_OK;
+}
+
+int kda_set_v_split(kda_handle* h, int v_split) {
+  if (h == nullptr || (v_split != 1 && v_split != 2)) return KDA_EINVAL;
+  h->v_split = v_split;
   return KDA_OK;
 }
 

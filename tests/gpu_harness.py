@@ -35,7 +35,8 @@ def bf16_value(bits) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def prepare(weights: I.LayerWeights, device, dim_first=True, gate_mode=0, state_dtype="f32") -> kda.PreparedKda:
+def prepare(weights: I.LayerWeights, device, dim_first=True, gate_mode=0, state_dtype="f32",
+            v_split=1) -> kda.PreparedKda:
     return kda.PreparedKda(
         bf16_np_to_torch(weights.conv_w, device),
         None if weights.bias is None else bf16_np_to_torch(weights.bias, device),
@@ -44,19 +45,19 @@ def prepare(weights: I.LayerWeights, device, dim_first=True, gate_mode=0, state_
         torch.from_numpy(weights.dt_bias).to(device),
         torch.from_numpy(weights.o_norm).to(device),
         gate_lower_bound=weights.gate_lower_bound, eps=weights.eps, conv_dim_first=dim_first, gate_mode=gate_mode,
-        state_dtype=state_dtype)
+        state_dtype=state_dtype, v_split=v_split)
 
 
 class DeviceStep:
     """Device copies of one step's inputs (full pools, sentinel-filled)."""
 
     def __init__(self, si: I.StepInputs, device="cuda:0", dim_first=True, weights=None, gate_mode=0,
-                 state_dtype="f32"):
+                 state_dtype="f32", v_split=1):
         w = si.workload
         self.si, self.w, self.dim_first = si, w, dim_first
         self.device = torch.device(device)
         self.state_dtype = state_dtype
-        self.prep = prepare(weights or si.weights, self.device, dim_first, gate_mode, state_dtype)
+        self.prep = prepare(weights or si.weights, self.device, dim_first, gate_mode, state_dtype, v_split)
         self.projected = bf16_np_to_torch(si.projected, self.device)
         H, sl = w.heads, w.width - 1
         if state_dtype == "bf16":

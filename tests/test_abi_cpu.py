@@ -30,7 +30,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == sorted(["kda_prepare", "kda_step", "kda_check", "kda_destroy", "kda_strerror",
-                            "kda_launch_info", "kda_set_gate_mode", "kda_set_state_dtype", "kda_plan_create",
+                            "kda_launch_info", "kda_set_gate_mode", "kda_set_state_dtype", "kda_set_v_split",
+                            "kda_plan_create",
                             "kda_plan_launch", "kda_plan_destroy", "kda_linear", "kda_linear_check",
                             "kda_layer_plan_create"])
 
@@ -52,6 +53,7 @@ def test_host_validation_without_gpu(lib):
     # step / check with no handle
     assert lib.kda_step(None, 16, 1, 1154, 16, 1, 16, 4, 16, 1, None, 16, None) == -1
     assert lib.kda_check(None, None, None) == -1
+    assert lib.kda_set_v_split(None, 1) == -1
     lib.kda_destroy(None)
     assert lib.kda_launch_info(0, None, None, None) == -1
     assert lib.kda_launch_info(9, None, None, None) == -1

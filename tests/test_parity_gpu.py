@@ -29,11 +29,11 @@ def _lib():
     kda.load_library()
 
 
-def _check_full(si: I.StepInputs, dim_first=True, reqs=None, gate_mode=0):
+def _check_full(si: I.StepInputs, dim_first=True, reqs=None, gate_mode=0, v_split=1):
     """Run the whole step on the GPU; compare requests `reqs` (default all)
     with the oracle and check the untouched part of every pool."""
     w = si.workload
-    ds = G.DeviceStep(si, dim_first=dim_first, gate_mode=gate_mode)
+    ds = G.DeviceStep(si, dim_first=dim_first, gate_mode=gate_mode, v_split=v_split)
     flags = ds.run()
     if reqs is None:
         reqs = np.arange(w.requests)
@@ -92,10 +92,19 @@ def test_full_width_verify_full_parity():
     ds.close()
 
 
-@pytest.mark.parametrize("L", [1, 2, 3, 5, 6, 7, 8])
-def test_every_token_count(L):
+@pytest.mark.parametrize("v_split", [1, 2])
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_every_token_count(L, v_split):
+    # one CTA a (request, head), or two in a cluster (64 v rows each, o halves swapped)
     si = case(heads=2, requests=5, L=L, pool=5 * L + 3, seed=40 + L, verify=L > 1)
-    _check_full(si)
+    _check_full(si, v_split=v_split)
+
+
+@pytest.mark.parametrize("name", ["batched_decode", "spec_verify"])
+def test_two_ctas_per_head_on_many_waves(name):
+    # the split forced where the automatic choice keeps one CTA: 2 x 768 or 2 x 384 CTAs,
+    # clusters of two in more than one wave
+    _check_full(I.make_step_inputs(I.WORKLOADS[name]), v_split=2)
 
 
 @pytest.mark.parametrize("width", [2, 3])
@@ -140,12 +149,12 @@ def test_plan_replays_equal_steps(L):
     b.close()
 
 
-def _check_bf16_state(si: I.StepInputs, reqs=None):
+def _check_bf16_state(si: I.StepInputs, reqs=None, v_split=1):
     """The bf16 state pool (kda_set_state_dtype): outputs and windows as in
     fp32, each stored state within one bf16 step of the oracle's, untouched
     slots keep their bf16 sentinel."""
     w = si.workload
-    ds = G.DeviceStep(si, state_dtype="bf16")
+    ds = G.DeviceStep(si, state_dtype="bf16", v_split=v_split)
     flags = ds.run()
     if reqs is None:
         reqs = np.arange(w.requests)
@@ -174,9 +183,10 @@ def test_bf16_state_large_decode_sampled():
     _check_bf16_state(si, reqs=np.array([0, 1, 77, 300, 511]))
 
 
+@pytest.mark.parametrize("v_split", [1, 2])
 @pytest.mark.parametrize("L", [1, 3, 8])
-def test_bf16_state_token_counts(L):
-    _check_bf16_state(case(heads=2, requests=4, L=L, pool=4 * L + 3, seed=90 + L, verify=L > 1))
+def test_bf16_state_token_counts(L, v_split):
+    _check_bf16_state(case(heads=2, requests=4, L=L, pool=4 * L + 3, seed=90 + L, verify=L > 1), v_split=v_split)
 
 
 def test_verify_with_one_token_accepted_array():
@@ -189,10 +199,11 @@ def _full_pool_oracle(si, slots, acc, dim_first=True):
                        acc, dim_first=dim_first)
 
 
-def test_padding_and_bad_values():
+@pytest.mark.parametrize("v_split", [1, 2])
+def test_padding_and_bad_values(v_split):
     """slot -1 first = padding (zero out, no cache I/O); accepted outside 1..L
     and slots outside the pool set their error bits and skip the request,
-    exactly as the oracle does."""
+    exactly as the oracle does (one or two CTAs a (request, head))."""
     R, L = 6, 3
     si = case(heads=2, requests=R, L=L, pool=24, seed=63, accepted=[3, 1, 2, 2, 1, 3])
     slots = si.slots.reshape(R, L).copy()
@@ -204,7 +215,7 @@ def test_padding_and_bad_values():
     si.slots = slots.reshape(-1).copy()
     out_ref, conv_ref, pool_ref, err = _full_pool_oracle(si, si.slots, acc)
     assert err == oracle.ERR_ACCEPTED | oracle.ERR_SLOT
-    ds = G.DeviceStep(si)
+    ds = G.DeviceStep(si, v_split=v_split)
     ds.accepted = torch.from_numpy(acc).to(ds.device)
     flags = ds.run()
     assert flags == err
@@ -223,11 +234,12 @@ def test_padding_and_bad_values():
     ds.close()
 
 
-def test_decode_padding_rows():
+@pytest.mark.parametrize("v_split", [1, 2])
+def test_decode_padding_rows(v_split):
     si = case(heads=2, requests=5, L=1, pool=8, seed=64)
     si.slots[[1, 3]] = -1
     out_ref, conv_ref, pool_ref, err = _full_pool_oracle(si, si.slots, None)
-    ds = G.DeviceStep(si)
+    ds = G.DeviceStep(si, v_split=v_split)
     assert ds.run() == err == 0
     out = G.torch_bf16_to_np(ds.out)
     G.assert_out_close(out, out_ref)
