@@ -534,9 +534,9 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   static_assert(VS == 1 || VS == 2, "one or two CTAs a (request, head)");
   const unsigned slice = VS == 1 ? 0u : cluster_rank();  // which 64 v rows (VS = 2)
-  const long long task = (long long)blockIdx.x / VS;    // the clusters of a launch are consecutive blocks
-  const int h = (int)(task % a.heads);
-  const long long r = task / a.heads;
+  const unsigned task = blockIdx.x / VS;                // the clusters of a launch are consecutive blocks
+  const int h = (int)(task % (unsigned)a.heads);        // 32-bit: a 64-bit division costs every CTA
+  const long long r = task / (unsigned)a.heads;
   const long long row0 = r * L;
   const int D = a.D, SL = a.W - 1;
 
