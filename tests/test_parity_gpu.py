@@ -115,6 +115,20 @@ def test_conv_widths(width):
 def test_transposed_conv_state_and_bias():
     _check_full(case(heads=3, requests=4, L=4, pool=20, seed=60, with_bias=True), dim_first=False)
     _check_full(case(heads=1, requests=7, L=1, pool=9, seed=61, with_bias=True), dim_first=True)
+    # the two-CTA split is built for the window-first layout: asked for on the other, the step runs one CTA
+    _check_full(case(heads=3, requests=4, L=4, pool=20, seed=60, with_bias=True), dim_first=False, v_split=2)
+
+
+def test_v_split_rejects_other_values():
+    import linear_attention_decode_03_gb300 as kda
+
+    ds = G.DeviceStep(case(heads=2, requests=2, L=1, pool=4, seed=65))
+    for bad in (0, 3, -1):
+        with pytest.raises(kda.KdaError):
+            kda.kda_set_v_split(ds.prep.handle, bad)
+    kda.kda_set_v_split(ds.prep.handle, 2)
+    kda.kda_set_v_split(ds.prep.handle, 1)
+    ds.close()
 
 
 @pytest.mark.parametrize("L", [1, 4])
