@@ -74,3 +74,23 @@ def test_rotation_applies_to_the_mid_sized_workloads():
     assert bench.rotation_copies(I.WORKLOADS["spec_verify"]) > 0
     assert bench.rotation_copies(I.WORKLOADS["large_decode"]) == 0
     assert bench.rotation_copies(I.WORKLOADS["tiny_decode"]) == 0
+
+
+def test_reference_arm_line():
+    # the reference arm (the fp64 oracle on the host's cores) prints the contract's line
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload",
+                          "batched_decode", "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                         timeout=600, cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["config"]["workload"] == "batched_decode" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["gpu_launches"] == 0
