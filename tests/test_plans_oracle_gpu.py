@@ -42,11 +42,13 @@ def _state_close(gpu: np.ndarray, ref: np.ndarray):
     G.assert_state_close(gpu[~nan], ref[~nan])
 
 
+@pytest.mark.parametrize("v_split", [1, 2])
 @pytest.mark.parametrize("L", [1, 4])
-def test_plan_replays_match_oracle(L):
+def test_plan_replays_match_oracle(L, v_split):
+    # v_split = 2: the recorded launch is a cluster launch of two CTAs a (request, head)
     si = case(heads=2, requests=4, L=L, pool=4 * L + 3, seed=180 + L, verify=L > 1)
     W = oracle.Weights(**si.weights.as_dict())
-    ds = G.DeviceStep(si)
+    ds = G.DeviceStep(si, v_split=v_split)
     plan = ds.prep.plan(ds.projected, ds.out, caches=(ds.conv, ds.state), slots=ds.slots, accepted=ds.accepted)
     conv, pool = si.full_conv_state(), si.full_state_pool()
     proj = si.projected.copy()
