@@ -941,7 +941,7 @@ def main():
     ap.add_argument("--op", choices=["step", "in_proj", "o_proj", "layer"], default="step",
                     help="step: the KDA core (default); in_proj / o_proj: the layer's projections (kda_linear) "
                          "for the workload's rows; layer: in_proj -> core -> o_proj as one CUDA graph")
-    ap.add_argument("--layer-pdl", choices=["none", "step_edge", "o_proj_edge", "both"], default="step_edge",
+    ap.add_argument("--layer-pdl", choices=["none", "step_edge", "o_proj_edge", "both"], default="both",
                     help="--op layer: the edges of the timed graph launched as programmatic dependents "
                          "(the others are timed too and reported under layer_ms)")
     ap.add_argument("--v-split", type=int, choices=[1, 2], default=1,
