@@ -598,6 +598,26 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     cv[kind].wp[1] = wt.y;
     cv[kind].bb = a.bias ? reinterpret_cast<const unsigned short*>(a.bias)[kind * D + h * HD + c] : (unsigned short)0;
   }
+  // The conv inputs from the projected rows (sequence positions 3 on) need no slot.
+  // Decode's (one a channel) go out with round trip 1, the start window below them
+  // waiting for the slots (large decode 127.3 -> 124.9 us); verify's, several a
+  // channel, go out with the window in round trip 2 (issued here they delayed round
+  // trip 1: spec-verify 24.7 -> 25.3 us).
+  constexpr bool EARLY_X = (L == 1);
+  const unsigned short* prow = reinterpret_cast<const unsigned short*>(a.projected) + row0 * a.pitch + h * HD + c;
+  unsigned short xin[3][CA + 3];
+  if constexpr (EARLY_X) {
+#pragma unroll
+    for (int kind = 0; kind < 3; ++kind) {
+      const int t0 = conv_t0(kind), n = conv_n(kind);
+#pragma unroll
+      for (int i = 0; i < CA + 3; ++i) {
+        const int pos = t0 + i;  // sequence position; pos - 3 < t0 + n <= L
+        xin[kind][i] = (n > 0 && i < n + 3 && pos >= 3) ? prow[(long long)(pos - 3) * a.pitch + kind * D]
+                                                        : (unsigned short)0;
+      }
+    }
+  }
 
   // ---- validate (every thread decides the same from the same loaded values) ---
   int status = TASK_OK, start = 0;
@@ -627,19 +647,16 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   if (status != TASK_OK) return;
 
   // ---- round trip 2: the conv inputs, then the start state (bulk) -------------
-  // The conv inputs of the thread's tokens (projected x from position 3 on, the
-  // start window below it) go out first so that they do not queue behind the
-  // state's bulk copies; they are packed once the copies are issued.
+  // The start window of the thread's channels (sequence positions below 3; verify:
+  // and the projected x above it) goes out first so that it does not queue behind
+  // the state's bulk copies; the conv inputs are packed once the copies are issued.
   // Conv cache addressing (elements): slot s, channel ch, window slot j at
   // s * slot_elems + ch * CHS + j * JS.
   const long long slot_elems = 3LL * D * SL;
   const long long CHS = DF ? SL : 1, JS = DF ? 1 : 3LL * D;
   // the thread's q channel: column h * 128 + c; k and v are D and 2 D further
   const long long cch = (long long)(h * HD + c) * CHS;
-  unsigned short xin[3][CA + 3];
   {
-    const unsigned short* prow =
-        reinterpret_cast<const unsigned short*>(a.projected) + row0 * a.pitch + h * HD + c;
     const unsigned short* win =
         reinterpret_cast<const unsigned short*>(a.conv_state) + (long long)start * slot_elems + cch;
 #pragma unroll
@@ -648,16 +665,13 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
       for (int i = 0; i < CA + 3; ++i) {
         const int pos = t0 + i;  // sequence position; pos - 3 < t0 + n <= L
-        unsigned short v = 0;
-        if (n > 0 && i < n + 3) {
-          if (pos >= 3) {
-            v = prow[(long long)(pos - 3) * a.pitch + kind * D];
-          } else {
-            const int j = pos + SL - 3;  // window slot of the position
-            if (j >= 0) v = win[(long long)kind * D * CHS + j * JS];
-          }
+        const int j = pos + SL - 3;  // window slot of the position (pos < 3)
+        if (pos < 3) {
+          if (n > 0 && j >= 0) xin[kind][i] = win[(long long)kind * D * CHS + j * JS];
+          else if constexpr (!EARLY_X) xin[kind][i] = 0;
+        } else if constexpr (!EARLY_X) {
+          xin[kind][i] = (n > 0 && i < n + 3) ? prow[(long long)(pos - 3) * a.pitch + kind * D] : (unsigned short)0;
         }
-        xin[kind][i] = v;
       }
     }
   }
