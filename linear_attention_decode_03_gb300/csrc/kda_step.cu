@@ -604,9 +604,10 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   // channel, go out with the window in round trip 2 (issued here they delayed round
   // trip 1: spec-verify 24.7 -> 25.3 us).
   constexpr bool EARLY_X = (L == 1);
-  const unsigned short* prow = reinterpret_cast<const unsigned short*>(a.projected) + row0 * a.pitch + h * HD + c;
   unsigned short xin[3][CA + 3];
   if constexpr (EARLY_X) {
+    const unsigned short* prow =
+        reinterpret_cast<const unsigned short*>(a.projected) + row0 * a.pitch + h * HD + c;
 #pragma unroll
     for (int kind = 0; kind < 3; ++kind) {
       const int t0 = conv_t0(kind), n = conv_n(kind);
@@ -656,7 +657,22 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   const long long CHS = DF ? SL : 1, JS = DF ? 1 : 3LL * D;
   // the thread's q channel: column h * 128 + c; k and v are D and 2 D further
   const long long cch = (long long)(h * HD + c) * CHS;
-  {
+  if constexpr (EARLY_X) {  // the start window alone
+    const unsigned short* win =
+        reinterpret_cast<const unsigned short*>(a.conv_state) + (long long)start * slot_elems + cch;
+#pragma unroll
+    for (int kind = 0; kind < 3; ++kind) {
+      const int t0 = conv_t0(kind), n = conv_n(kind);
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {  // positions t0 + i < 3 only
+        const int pos = t0 + i;
+        const int j = pos + SL - 3;  // window slot of the position
+        if (n > 0 && pos < 3 && j >= 0) xin[kind][i] = win[(long long)kind * D * CHS + j * JS];
+      }
+    }
+  } else {  // projected x and the start window together
+    const unsigned short* prow =
+        reinterpret_cast<const unsigned short*>(a.projected) + row0 * a.pitch + h * HD + c;
     const unsigned short* win =
         reinterpret_cast<const unsigned short*>(a.conv_state) + (long long)start * slot_elems + cch;
 #pragma unroll
@@ -665,13 +681,16 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
       for (int i = 0; i < CA + 3; ++i) {
         const int pos = t0 + i;  // sequence position; pos - 3 < t0 + n <= L
-        const int j = pos + SL - 3;  // window slot of the position (pos < 3)
-        if (pos < 3) {
-          if (n > 0 && j >= 0) xin[kind][i] = win[(long long)kind * D * CHS + j * JS];
-          else if constexpr (!EARLY_X) xin[kind][i] = 0;
-        } else if constexpr (!EARLY_X) {
-          xin[kind][i] = (n > 0 && i < n + 3) ? prow[(long long)(pos - 3) * a.pitch + kind * D] : (unsigned short)0;
+        unsigned short v = 0;
+        if (n > 0 && i < n + 3) {
+          if (pos >= 3) {
+            v = prow[(long long)(pos - 3) * a.pitch + kind * D];
+          } else {
+            const int j = pos + SL - 3;  // window slot of the position
+            if (j >= 0) v = win[(long long)kind * D * CHS + j * JS];
+          }
         }
+        xin[kind][i] = v;
       }
     }
   }
