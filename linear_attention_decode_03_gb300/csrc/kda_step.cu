@@ -14,13 +14,14 @@
 //   * round trip 1 (issued at entry, by every thread, with no dependence):
 //       the request's slots / accepted, the lane's share of the head's f_b
 //       (4 rows x 16 k, two 16-byte loads a row), the f_a, out-gate and beta
-//       values, the packed conv taps and bias of the thread's channels.
+//       values, the packed conv taps and bias of the thread's channels, and
+//       for decode the conv input from the projected row.
 //   * round trip 2 (once the slots are in): every thread validates them and
-//       loads the conv inputs of its channels (projected x and the start
-//       window); thread 0 puts the 64 KiB start state of (slot, head) in
-//       flight as four 16 KiB bulk async copies (cp.async.bulk, L2
-//       evict-first) on four mbarriers -- decode at once, verify once its own
-//       conv inputs are in.
+//       loads the rest of the conv inputs of its channels (the start window;
+//       verify: and the projected x); thread 0 puts the 64 KiB start state of
+//       (slot, head) in flight as four 16 KiB bulk async copies
+//       (cp.async.bulk, L2 evict-first) on four mbarriers -- decode at once,
+//       verify once its own conv inputs are in.
 //   * while the state lands: the causal conv of the q, k, v channels over the
 //       L tokens; z = f_b . f_a (4 channels x 16 k a lane with mixed-precision
 //       bf16 FMAs, a reduce-scatter over 8 lanes, a closed-form bound on the
@@ -35,6 +36,9 @@
 //       each quarter with a TMA bulk store, verify sends every token's rows to
 //       slots[r, t] with 128-bit stores.
 //   * gated RMSNorm, one warp per token (run by every warp) -> bf16 core_out.
+// As an option (kda_set_v_split) a (request, head) runs as a cluster of two
+// CTAs, each with 64 of the v rows (one recurrence pass) and half the outputs,
+// the halves of o swapped through distributed shared memory for the norm.
 // The bf16 hand-offs (conv outputs, z) are rounded correctly: each fp32 value
 // carries a bound on its error and is recomputed exactly (fp64, or a
 // compensated TwoSum sum) when the bound straddles a bf16 rounding boundary.
