@@ -107,9 +107,10 @@ def test_two_ctas_per_head_on_many_waves(name):
     _check_full(I.make_step_inputs(I.WORKLOADS[name]), v_split=2)
 
 
+@pytest.mark.parametrize("L", [1, 3])
 @pytest.mark.parametrize("width", [2, 3])
-def test_conv_widths(width):
-    _check_full(case(heads=2, requests=3, L=3, pool=12, width=width, seed=50 + width))
+def test_conv_widths(width, L):
+    _check_full(case(heads=2, requests=3, L=L, pool=12, width=width, seed=50 + width, verify=L > 1))
 
 
 def test_transposed_conv_state_and_bias():
