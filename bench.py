@@ -8,7 +8,10 @@ Prints ONE JSON line:
   value      tokens/s with every input resident in HBM: blocks of exactly
              --steps steps (CUDA events on the launching stream) repeated
              until --min-timed-s seconds of timed work; ms_per_step is the
-             median block
+             median block.  By default (--launch graph) a block is recorded
+             once as a CUDA graph of the same kda_step launches and replayed;
+             the same blocks launched one step at a time are reported beside
+             it (`direct`)
   e2e        the same metric through the public API with host buffers:
              each step copies its projected rows, slots (and accepted) from
              pinned host memory and reads `out` back
