@@ -51,7 +51,7 @@ from linear_attention_decode_03_gb300 import inputs as I  # noqa: E402
 
 METRIC = "KDA tokens/s and achieved HBM GB/s (state R+W) vs GB300 peak, 1 GPU"
 L2_BYTES = 129 * 1024 * 1024
-E2E_BLOCK = 16  # steps a recorded e2e graph holds
+E2E_BLOCK = 128  # steps a recorded e2e graph holds (each replay refills the copy pipeline)
 HEAD_DIM = 128
 
 
@@ -69,11 +69,21 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def measured_traffic(workload: str):
+def traffic_key(workload: str, state_dtype: str = "f32", v_split: int = 1):
+    """The name a capture is filed under: the workload, `_bf16` for a bf16 state
+    pool; None for launch shapes that no capture covers (two CTAs a head)."""
+    if v_split != 1:
+        return None
+    return workload if state_dtype == "f32" else f"{workload}_{state_dtype}"
+
+
+def measured_traffic(workload: str, state_dtype: str = "f32", v_split: int = 1):
     """DRAM bytes (read + write) per launch that an ncu capture recorded for
-    this workload, or None when there is none or the kernel source changed
-    since (the summary stores the hash of the sources it was taken on)."""
-    if not os.path.exists(TRAFFIC_FILE):
+    this workload and state type, or None when there is none or the kernel
+    source changed since (the summary stores the hash of the sources it was
+    taken on)."""
+    key = traffic_key(workload, state_dtype, v_split)
+    if key is None or not os.path.exists(TRAFFIC_FILE):
         return None
     src_hash, per_wl = None, {}
     with open(TRAFFIC_FILE) as f:
@@ -85,7 +95,7 @@ def measured_traffic(workload: str):
                 per_wl[parts[1]] = int(parts[2])
     if src_hash != kernel_source_hash():
         return None
-    return per_wl.get(workload)
+    return per_wl.get(key)
 
 
 def max_over_ranks(values, dist=None, device=None):
@@ -904,7 +914,7 @@ def measure_workload(w: I.Workload, device, args):
                   f"({n_copies * touched_bytes(w, args.state_dtype) / 1e6:.0f} MB touched a round), stepped "
                   "through in turn back to back" if n_copies else
                   "inputs larger than L2" if flush_bufs is None else "L2 flushed between timed steps"),
-           "traffic": measured_traffic(w.name)}
+           "traffic": measured_traffic(w.name, args.state_dtype, getattr(args, "v_split", 1))}
     if direct is not None:
         rec["direct_launch"] = direct_record(direct, w, state_b, all_b, peak)
     if flush_rec is not None:
@@ -1122,7 +1132,8 @@ def main():
         "data": "synthetic", "config": workload_config(w, args),
         "state_gbs": state_gbs, "state_frac_of_peak": state_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": measured_traffic(w.name), "kernel": "kda_step_kernel",
+                     "traffic": measured_traffic(w.name, args.state_dtype, args.v_split),
+                     "kernel": "kda_step_kernel",
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": whole_job_rate(world, w.rows, e2e_steps, e2e_ms), "unit": "tokens/s",

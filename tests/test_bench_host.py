@@ -94,3 +94,23 @@ def test_reference_arm_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["gpu_launches"] == 0
+
+
+def test_traffic_is_filed_by_state_type_and_launch_shape(tmp_path, monkeypatch):
+    # a bf16-state line must not carry the fp32 capture's bytes, nor a two-CTA line either
+    f = tmp_path / "traffic.txt"
+    f.write_text(f"source_sha256 {bench.kernel_source_hash()}\n"
+                 "traffic large_decode 100\ntraffic large_decode_bf16 60\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.measured_traffic("large_decode") == 100
+    assert bench.measured_traffic("large_decode", "bf16") == 60
+    assert bench.measured_traffic("large_decode", "f32", 2) is None
+    assert bench.measured_traffic("spec_verify", "bf16") is None
+    f.write_text("source_sha256 0123\ntraffic large_decode 100\n")  # another source: no figure
+    assert bench.measured_traffic("large_decode") is None
+
+
+def test_committed_traffic_matches_the_kernel_source():
+    # the committed captures were taken on the kernel as it stands
+    assert bench.measured_traffic("large_decode") is not None
+    assert bench.measured_traffic("large_decode", "bf16") is not None
