@@ -233,6 +233,17 @@ def kda_launch_info(L: int) -> Tuple[int, int, int]:
     return t.value, s.value, c.value
 
 
+def _current_stream(device) -> int:
+    """The raw handle of the device's current stream (without building a
+    torch Stream object on every call)."""
+    import torch
+
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None and device.index is not None:
+        return raw(device.index)
+    return torch.cuda.current_stream(device).cuda_stream
+
+
 def _dev(t, dtype, name):
     import torch
 
@@ -296,7 +307,10 @@ class PreparedKda:
 
     def _args(self, projected, out, caches, slots, accepted):
         """kda_step's arguments (pointers and sizes) for these tensors, and the
-        tensors they point into (kept alive by a plan)."""
+        tensors they point into (kept alive by a plan).  The step reads the
+        first rows of ``slots`` / ``accepted`` only, so longer ones are passed
+        as they are; a copy is made only where a layout needs one (strided
+        verify slots, a non-contiguous ``accepted``)."""
         import torch
 
         conv, state = caches[:2]
@@ -305,20 +319,32 @@ class PreparedKda:
         if accepted is not None:
             L = int(slots.shape[1])
             rows = batch // L
-            accepted = _dev(accepted[:rows].contiguous(), torch.int32, "accepted")
-            slots = slots[:rows]
+            if accepted.shape[0] < rows or slots.shape[0] < rows:
+                raise ValueError("slots and accepted need a row for each request of the batch")
+            if not accepted.is_contiguous():
+                accepted = accepted[:rows].contiguous()
+            _dev(accepted, torch.int32, "accepted")
             if slots.stride() != (L, 1):
-                slots = slots.contiguous()
-        else:
-            slots = slots[:batch]
+                slots = slots[:rows].contiguous()
+        elif slots.shape[0] < batch:
+            raise ValueError("slots needs an entry for each row of the batch")
         _dev(slots, torch.int32, "slots")
         if projected.dtype != torch.bfloat16 or not projected.is_cuda or projected.stride(1) != 1:
             raise TypeError("projected must be a CUDA bf16 tensor with unit column stride")
+        if batch > 0 and projected.shape[1] < 4 * self.dim + HEAD_DIM + self.heads:
+            raise ValueError("projected needs the q|k|v|gate|f_a|beta columns (4D + 128 + H)")
         _dev(out, torch.bfloat16, "out")
         _dev(conv, torch.bfloat16, "conv_state")
         _dev(state, torch.bfloat16 if self.state_dtype == "bf16" else torch.float32, "state_pool")
+        pool = state.shape[0]
+        if out.numel() < batch * self.dim:
+            raise ValueError("out needs [rows, D] elements")
+        if state.numel() != pool * self.heads * HEAD_DIM * HEAD_DIM:
+            raise ValueError("state_pool must be [pool, H, 128, 128]")
+        if conv.numel() < pool * 3 * self.dim * (self.width - 1):
+            raise ValueError("conv_state needs a window for every slot of the state pool")
         args = (projected.data_ptr(), batch, projected.stride(0), conv.data_ptr(), self.conv_dim_first,
-                state.data_ptr(), state.shape[0], slots.data_ptr(), L,
+                state.data_ptr(), pool, slots.data_ptr(), L,
                 None if accepted is None else accepted.data_ptr(), out.data_ptr())
         return args, (projected, out, conv, state, slots, accepted)
 
@@ -330,7 +356,7 @@ class PreparedKda:
 
         args, _ = self._args(projected, out, caches, slots, accepted)
         if stream is None:
-            stream = torch.cuda.current_stream(self.device).cuda_stream
+            stream = _current_stream(self.device)
         kda_step(self.handle, *args, stream)
         return out
 
@@ -407,7 +433,7 @@ class KdaPlan:
         import torch
 
         if stream is None:
-            stream = torch.cuda.current_stream(self.device).cuda_stream
+            stream = _current_stream(self.device)
         kda_plan_launch(self.plan, stream)
 
     def close(self) -> None:
