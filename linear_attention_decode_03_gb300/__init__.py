@@ -185,7 +185,7 @@ def linear(x, w, out=None, stream=None):
     if out.dtype != torch.bfloat16 or out.dim() != 2 or out.stride(1) != 1 or tuple(out.shape) != (rows, N):
         raise ValueError("out must be bf16 [rows, N] with unit column stride")
     if stream is None:
-        stream = torch.cuda.current_stream(x.device).cuda_stream
+        stream = _current_stream(x.device)
     kda_linear(x.data_ptr(), rows, x.stride(0), w.data_ptr(), N, K, out.data_ptr(), out.stride(0), stream)
     return out
 
