@@ -26,8 +26,8 @@
 //       L tokens; z = f_b . f_a (4 channels x 16 k a lane with mixed-precision
 //       bf16 FMAs, a reduce-scatter over 8 lanes, a closed-form bound on the
 //       fp32 error), the lower-bound gate and e^g; the l2norm of q and k and
-//       k^.q^ (one warp per token, run by every warp); then the windows after
-//       each token go to slots[r, t].
+//       k^.q^ (warp t on token t); then the windows after each token go to
+//       slots[r, t].
 //   * recurrence: two passes over pairs of 32-row quarters of the state
 //       (rows = v; each pass waits on its two copies); 16 lanes own a v row,
 //       8 k values a lane, four rows a thread in registers across the L
@@ -35,7 +35,7 @@
 //       reduce-scatter; decode writes the rows back to shared memory and sends
 //       each quarter with a TMA bulk store, verify sends every token's rows to
 //       slots[r, t] with 128-bit stores.
-//   * gated RMSNorm, one warp per token (run by every warp) -> bf16 core_out.
+//   * gated RMSNorm, warp t on token t -> bf16 core_out.
 // As an option (kda_set_v_split) a (request, head) runs as a cluster of two
 // CTAs, each with 64 of the v rows (one recurrence pass) and half the outputs,
 // the halves of o swapped through distributed shared memory for the norm.
@@ -863,12 +863,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 
   __syncthreads();  // raw q, k, v and e^g of every channel written
 
-  // ---- l2norm of q and k, k^.q^: one warp per token -----------------------------
-  // Every warp runs it (warp w on token w mod L) and warps < L store: with one
-  // warp alone on this short stretch (the others parked at the barrier) it
-  // took ~1.6 us, with all warps on it ~0.1 us (measured, globaltimer stamps).
-  {
-    const int t = warp % L;
+  // ---- l2norm of q and k, k^.q^: warp t on token t ----------------------------------
+  // Each warp reads and rewrites its own token only; the other warps go on to
+  // the barrier.
+  if (warp < L) {
+    const int t = warp;
     float4 q = *reinterpret_cast<float4*>(qh + t * HD + lane * 4);
     float4 k = *reinterpret_cast<float4*>(kh + t * HD + lane * 4);
     const float sq = warp_sum(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
@@ -878,12 +877,9 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     const float fq = rq * a.q_scale;
     q.x *= fq; q.y *= fq; q.z *= fq; q.w *= fq;
     k.x *= rk; k.y *= rk; k.z *= rk; k.w *= rk;
-    __syncthreads();  // every warp has read q and k before they are overwritten
-    if (warp < L) {
-      *reinterpret_cast<float4*>(qh + t * HD + lane * 4) = q;
-      *reinterpret_cast<float4*>(kh + t * HD + lane * 4) = k;
-      if (lane == 0) kq_s[t] = sqk * fq * rk;
-    }
+    *reinterpret_cast<float4*>(qh + t * HD + lane * 4) = q;
+    *reinterpret_cast<float4*>(kh + t * HD + lane * 4) = k;
+    if (lane == 0) kq_s[t] = sqk * fq * rk;
   }
   __syncthreads();
   if constexpr (VS == 2) {
@@ -1067,9 +1063,10 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     return;
   }
 
-  // ---- gated RMSNorm: one warp per token (all warps run it, as the l2norm) --------
+  // ---- gated RMSNorm: warp t on token t; the other warps are done ------------------
+  if (warp >= L) return;
   {
-    const int t = warp % L;
+    const int t = warp;
     float o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[e] = bf(ob[t * HD + lane * 4 + e]);
@@ -1080,7 +1077,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       y[e] = __float2bfloat16_rn(o[e] * rstd * wn[e] * __half2float(gsig_s[t * HD + lane * 4 + e]));
-    if (warp < L && (VS == 1 || (unsigned)(lane >> 4) == slice))  // VS = 2: this CTA's 64 columns
+    if (VS == 1 || (unsigned)(lane >> 4) == slice)  // VS = 2: this CTA's 64 columns
       *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
   }
   if constexpr (L == 1) {
