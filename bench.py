@@ -77,6 +77,14 @@ def traffic_key(workload: str, state_dtype: str = "f32", v_split: int = 1):
     return workload if state_dtype == "f32" else f"{workload}_{state_dtype}"
 
 
+def step_kernel_name(w: I.Workload, state_dtype: str = "f32", v_split: int = 1) -> str:
+    """The kernel kda_step launches for this workload: decode of two rows or more
+    with a bf16 state pool runs two rows of one head a CTA."""
+    if not w.verify and w.L == 1 and state_dtype == "bf16" and v_split == 1 and w.rows >= 2:
+        return "kda_decode_pair_kernel"
+    return "kda_step_kernel"
+
+
 def measured_traffic(workload: str, state_dtype: str = "f32", v_split: int = 1):
     """DRAM bytes (read + write) per launch that an ncu capture recorded for
     this workload and state type, or None when there is none or the kernel
@@ -1133,7 +1141,7 @@ def main():
         "state_gbs": state_gbs, "state_frac_of_peak": state_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": measured_traffic(w.name, args.state_dtype, args.v_split),
-                     "kernel": "kda_step_kernel",
+                     "kernel": step_kernel_name(w, args.state_dtype, args.v_split),
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": whole_job_rate(world, w.rows, e2e_steps, e2e_ms), "unit": "tokens/s",

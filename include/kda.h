@@ -77,8 +77,11 @@ typedef struct kda_handle kda_handle;
  * that (request, head) is written; if the second does, rows 0..63 of the
  * states may already be in every slots[r, t] (decode: in slots[b]) while rows
  * 64..127 are not.  Either way its out rows are not written, and the conv
- * windows (stored before the state is needed) are.  Treat the request's
- * caches as undefined after a timeout. */
+ * windows (stored before the state is needed) are.  Decode of two rows or
+ * more with a bf16 state pool serves rows 2p and 2p + 1 of a head in one CTA:
+ * a wait that gives up on either row leaves both rows' out unwritten, while the
+ * other row's state may already be stored.  Treat the requests' caches as
+ * undefined after a timeout. */
 
 /* Maximum verify tokens per request. */
 #define KDA_MAX_TOKENS 8

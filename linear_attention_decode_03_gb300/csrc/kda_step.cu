@@ -39,6 +39,10 @@
 // As an option (kda_set_v_split) a (request, head) runs as a cluster of two
 // CTAs, each with 64 of the v rows (one recurrence pass) and half the outputs,
 // the halves of o swapped through distributed shared memory for the norm.
+// Decode of two rows or more with a bf16 state pool runs rows 2p and 2p + 1 of
+// one head in one CTA (kda_decode_pair_kernel): the rows share the load round
+// trips and the head's f_b, and their two 32 KiB states fill the shared memory
+// that one fp32 state takes.
 // The bf16 hand-offs (conv outputs, z) are rounded correctly: each fp32 value
 // carries a bound on its error and is recomputed exactly (fp64, or a
 // compensated TwoSum sum) when the bound straddles a bf16 rounding boundary.
@@ -1085,6 +1089,391 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   }
 }
 
+// ---- decode with a bf16 state pool: two rows of one head a CTA --------------------
+// With half the state bytes, a one-row CTA spends most of its life on its two
+// dependent load round trips (the slot, then the window and state it
+// addresses). A CTA that serves rows 2p and 2p + 1 of head h shares those round
+// trips and the head's f_b between the rows, and holds the two 32 KiB states in
+// the shared memory one fp32 state takes (three CTAs an SM as before). The
+// arithmetic of a row is the one-row kernel's: thread half t runs row t's conv
+// (q, k and v of its channel), z takes the two rows as a verify takes two tokens,
+// warp t runs row t's norms, and each row's state goes through two passes of
+// its own.
+struct SmemPair {
+  static constexpr int state = 0;                              // bf16 [2][128][128]
+  static constexpr int eg = state + 2 * StateT<true>::BYTES;   // float [2][128]
+  static constexpr int kh = eg + 2 * HD * 4;                   // float [2][128]   k, then k^
+  static constexpr int qh = kh + 2 * HD * 4;                   // float [2][128]   q, then q^
+  static constexpr int fa = qh + 2 * HD * 4;                   // bf16  [2][128]   f_a; later o
+  static constexpr int vv = fa + 2 * HD * 2;                   // bf16  [2][128]
+  static constexpr int gate = vv + 2 * HD * 2;                 // fp16  [2][128]   sigmoid(out-gate)
+  static constexpr int fnp = gate + 2 * HD * 2;                // float [2][4]
+  static constexpr int beta = fnp + 32;                        // float [2]
+  static constexpr int kq = beta + 8;                          // float [2]
+  static constexpr int slot = kq + 8;                          // int   [2]
+  static constexpr int ctl = slot + 8;                         // int   [2]
+  static constexpr int mbar = (ctl + 8 + 7) / 8 * 8;           // u64   [2][4]
+  static constexpr int bytes = mbar + 8 * 2 * QUARTERS;
+};
+
+template <bool DF>
+__global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepArgs a, int rows) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using S = SmemPair;
+  using SB = StateT<true>;
+  unsigned short* stb = reinterpret_cast<unsigned short*>(smem + S::state);
+  float* eg = reinterpret_cast<float*>(smem + S::eg);
+  float* kh = reinterpret_cast<float*>(smem + S::kh);
+  float* qh = reinterpret_cast<float*>(smem + S::qh);
+  unsigned short* fa_b = reinterpret_cast<unsigned short*>(smem + S::fa);
+  __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(smem + S::fa);  // reuses the f_a space
+  __nv_bfloat16* vv = reinterpret_cast<__nv_bfloat16*>(smem + S::vv);
+  __half* gsig_s = reinterpret_cast<__half*>(smem + S::gate);
+  float* fnp = reinterpret_cast<float*>(smem + S::fnp);
+  float* beta_s = reinterpret_cast<float*>(smem + S::beta);
+  float* kq_s = reinterpret_cast<float*>(smem + S::kq);
+  int* slot_s = reinterpret_cast<int*>(smem + S::slot);
+  int* ctl = reinterpret_cast<int*>(smem + S::ctl);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + S::mbar);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned task = blockIdx.x;
+  const int h = (int)(task % (unsigned)a.heads);
+  const long long row0 = 2LL * (task / (unsigned)a.heads);
+  const int nrow = (row0 + 1 < rows) ? 2 : 1;
+  const int D = a.D, SL = a.W - 1;
+  const int c = tid & (HD - 1), my = tid >> 7;  // the thread's channel and row for the conv
+
+  // ---- round trip 1 -----------------------------------------------------------------
+  const int sl0 = a.slots[row0];
+  const int sl1 = nrow == 2 ? a.slots[row0 + 1] : -1;
+  const int zc = warp * Z_CHANNELS + (lane >> 3) * 4 + ((lane >> 1) & 3);
+  uint4 fbw[4][2];
+  {
+    const uint4* fb = reinterpret_cast<const uint4*>(a.f_b + (long long)(h * HD + warp * Z_CHANNELS + (lane >> 3) * 4) * HD);
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+      for (int m = 0; m < 2; ++m) fbw[rr][m] = __ldg(fb + rr * (HD / 8) + m * 8 + (lane & 7));
+  }
+  const float fbn = a.fb_norm[h * HD + zc];
+  const float dtc = a.dt_bias[h * HD + zc];
+  const float a_log = a.A_log[h];
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in the one-row kernel
+  unsigned short fa_v = 0, gate_v = 0;
+  const unsigned short* prow = reinterpret_cast<const unsigned short*>(a.projected) + (row0 + my) * a.pitch;
+  if (my < nrow) {
+    fa_v = prow[4 * D + c];
+    gate_v = prow[3 * D + h * HD + c];
+  }
+  float beta_logit = 0.0f;
+  if (tid < nrow) beta_logit = bf(a.projected[(row0 + tid) * a.pitch + 4 * D + HD + h]);
+  ConvLane<1> cv[3];
+  unsigned short xin[3][4];
+#pragma unroll
+  for (int kind = 0; kind < 3; ++kind) {
+    const uint2 wt = a.conv_w[kind * D + h * HD + c];
+    cv[kind].wp[0] = wt.x;
+    cv[kind].wp[1] = wt.y;
+    cv[kind].bb = a.bias ? reinterpret_cast<const unsigned short*>(a.bias)[kind * D + h * HD + c] : (unsigned short)0;
+    xin[kind][0] = xin[kind][1] = xin[kind][2] = 0;
+    xin[kind][3] = my < nrow ? prow[kind * D + h * HD + c] : (unsigned short)0;
+  }
+
+  // ---- validate each row (every thread decides the same) ------------------------------
+  constexpr int TASK_NONE = 3;  // past the last row
+  const int sl[2] = {sl0, sl1};
+  int status[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    if (t >= nrow) status[t] = TASK_NONE;
+    else if (sl[t] == -1) status[t] = TASK_PADDING;
+    else if (sl[t] < 0 || sl[t] >= a.pool) status[t] = TASK_SKIP;
+    else status[t] = TASK_OK;
+  }
+  // row t's status without a run-time index into the array
+  auto row_ok = [&](int t) { return (t == 0 ? status[0] : status[1]) == TASK_OK; };
+  if (tid == 0 && (status[0] == TASK_SKIP || status[1] == TASK_SKIP)) atomicOr(a.err, KDA_ERR_SLOT);
+#pragma unroll
+  for (int t = 0; t < 2; ++t)  // padding rows: zero output columns, no cache traffic
+    if (status[t] == TASK_PADDING && my == t) a.out[(row0 + t) * D + h * HD + c] = __float2bfloat16_rn(0.0f);
+  if (status[0] != TASK_OK && status[1] != TASK_OK) return;
+
+  // ---- round trip 2: the start window of the thread's row, then the states (bulk) -----
+  const long long slot_elems = 3LL * D * SL;
+  const long long CHS = DF ? SL : 1, JS = DF ? 1 : 3LL * D;
+  const long long cch = (long long)(h * HD + c) * CHS;
+  const int my_slot = my == 0 ? sl0 : sl1;
+  const bool my_ok = row_ok(my);
+  if (my_ok) {
+    const unsigned short* win = reinterpret_cast<const unsigned short*>(a.conv_state) + (long long)my_slot * slot_elems + cch;
+#pragma unroll
+    for (int kind = 0; kind < 3; ++kind)
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        const int j = i + SL - 3;  // window slot of sequence position i
+        if (j >= 0) xin[kind][i] = win[(long long)kind * D * CHS + j * JS];
+      }
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int q = 0; q < 2 * QUARTERS; ++q) mbar_init(smem_u32(&mbar[q]), 1);
+    fence_mbar_init();
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      if (status[t] != TASK_OK) continue;
+      const unsigned char* src = static_cast<const unsigned char*>(a.state_pool) + ((long long)sl[t] * a.heads + h) * SB::BYTES;
+#pragma unroll
+      for (int q = 0; q < QUARTERS; ++q) {
+        const uint32_t bar = smem_u32(&mbar[t * QUARTERS + q]);
+        mbar_expect_tx(bar, SB::QBYTES);
+        bulk_load(smem_u32(reinterpret_cast<unsigned char*>(stb) + t * SB::BYTES + q * SB::QBYTES), src + q * SB::QBYTES,
+                  SB::QBYTES, bar);
+      }
+    }
+    ctl[0] = 0;
+  }
+  if (tid == 0) slot_s[0] = sl0;
+  if (tid == 1) slot_s[1] = sl1;
+  fa_b[tid] = fa_v;  // [row][channel] = [tid >> 7][tid & 127]
+  gsig_s[tid] = __float2half_rn(sigmoid_fast(bf_bits(gate_v)));
+  {
+    const float f = bf_bits(fa_v);
+    const float sq = warp_sum(f * f);
+    if (lane == 0) fnp[my * 4 + c / 32] = sq;
+  }
+  if (tid < 2) beta_s[tid] = sigmoid_fast(beta_logit);
+#pragma unroll
+  for (int kind = 0; kind < 3; ++kind) {
+    cv[kind].sp[0] = xin[kind][0] | ((unsigned)xin[kind][1] << 16);
+    cv[kind].sp[1] = xin[kind][2] | ((unsigned)xin[kind][3] << 16);
+  }
+  __syncthreads();  // barriers initialised, f_a, its squares and the slots staged
+
+  // ---- causal conv: q, k and v of the thread's channel for its row ---------------------
+#pragma unroll
+  for (int kind = 0; kind < 3; ++kind) {
+    const ConvLane<1>& q = cv[kind];
+    float run;
+    const float y = conv_dot<0>(q, run);
+    const float sy = y * sigmoid_fast(y);  // SiLU; error bound as in the one-row kernel
+    float yb;
+    if (!bf16_rounding_uncertain(sy, 2.0f * (1.21f * U32 * run + (2.5f * U32 * fabsf(y) + 0x1p-20f) * fabsf(sy))))
+      yb = bf_round(sy);
+    else
+      yb = silu_bf16_exact(bf_bits(q.bb), q.wp[0], q.wp[1], q.sp[0], q.sp[1]);
+    if (kind == 0) qh[my * HD + c] = yb;
+    else if (kind == 1) kh[my * HD + c] = yb;
+    else vv[my * HD + c] = __float2bfloat16_rn(yb);
+  }
+  // ---- z = f_b . f_a for both rows (even lanes row 0, odd lanes row 1), gate, e^g ------
+  {
+    const float expA = expf(a_log);
+    const uint4* f0 = reinterpret_cast<const uint4*>(fa_b);
+    const uint4* f1 = reinterpret_cast<const uint4*>(fa_b + HD);
+    float p0[4], p1[4];
+    z_partials(fbw, f0[lane & 7], f0[8 + (lane & 7)], p0);
+    z_partials(fbw, f1[lane & 7], f1[8 + (lane & 7)], p1);
+    float z = z_reduce(p0, lane);
+    const float z1 = z_reduce(p1, lane);
+    const int tt = lane & 1;
+    if (tt) z = z1;
+    const float4 np = *reinterpret_cast<const float4*>(fnp + tt * 4);
+    const float fnorm = sqrt_fast((np.x + np.y) + (np.z + np.w)) * (1.0f + 0x1p-12f);
+    const float bound = 12.0f * U32 * (1.0f + 0x1p-10f) * fbn * fnorm;
+    const bool unsure = bf16_rounding_uncertain(z, bound);
+    unsigned redo = __ballot_sync(0xffffffffu, unsure);
+    z = bf_round(z);
+    const int g8 = lane & 24;
+    while (redo) {
+      const unsigned mine = (redo >> g8) & 0xffu;
+      const int li = g8 + (mine ? __ffs(mine) - 1 : 0);
+      redo &= ~__ballot_sync(0xffffffffu, mine != 0 && lane == li);
+      const uint4* fr = reinterpret_cast<const uint4*>(fa_b + (li & 1) * HD);
+      uint4 w0, w1;
+      fb_row(fbw, (li >> 1) & 3, w0, w1);
+      const float ex = z_exact(w0, w1, fr[lane & 7], fr[8 + (lane & 7)]);
+      if (mine != 0 && lane == li) z = ex;
+    }
+    const float x = z + dtc;
+    const float g = (a.gate_mode == KDA_GATE_SOFTPLUS) ? fmaxf(-expA * softplus_fast(x), a.lb)
+                                                      : a.lb * sigmoid_fast(expA * x);
+    eg[tt * HD + zc] = __expf(g);
+  }
+  __syncthreads();  // raw q, k, v and e^g of both rows written
+
+  // ---- l2norm of q and k, k^.q^: warp t on row t ---------------------------------------
+  if (warp < 2) {
+    const int t = warp;
+    float4 q = *reinterpret_cast<float4*>(qh + t * HD + lane * 4);
+    float4 k = *reinterpret_cast<float4*>(kh + t * HD + lane * 4);
+    const float sq = warp_sum(q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w);
+    const float sk = warp_sum(k.x * k.x + k.y * k.y + k.z * k.z + k.w * k.w);
+    const float sqk = warp_sum(q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w);
+    const float rq = rsqrtf(sq + 1e-6f), rk = rsqrtf(sk + 1e-6f);
+    const float fq = rq * a.q_scale;
+    q.x *= fq; q.y *= fq; q.z *= fq; q.w *= fq;
+    k.x *= rk; k.y *= rk; k.z *= rk; k.w *= rk;
+    *reinterpret_cast<float4*>(qh + t * HD + lane * 4) = q;
+    *reinterpret_cast<float4*>(kh + t * HD + lane * 4) = k;
+    if (lane == 0) kq_s[t] = sqk * fq * rk;
+  }
+  __syncthreads();
+  // the new window of the thread's row: sequence positions 1..3
+  if (my_ok) {
+    unsigned short* conv16 = reinterpret_cast<unsigned short*>(a.conv_state);
+#pragma unroll
+    for (int kind = 0; kind < 3; ++kind) {
+      const long long cb = (long long)my_slot * slot_elems + cch + (long long)kind * D * CHS + (long long)(SL - 4) * JS;
+#pragma unroll
+      for (int p = 1; p <= 3; ++p)
+        if (p + SL >= 4) conv16[cb + p * JS] = cv[kind].get(p);
+    }
+  }
+
+  // ---- recurrence: each row's state in two passes (as the one-row kernel) -------------
+  const int hs = lane >> 4, kl = lane & 15;
+  const int rbase = warp * 2 + hs;
+  const bool b3 = (kl & 8) != 0, b2 = (kl & 4) != 0, b1 = (kl & 2) != 0;
+  const int rsel = (b2 ? 2 : 0) + (b1 ? 1 : 0);
+  bool timed_out = false;
+#pragma unroll 1
+  for (int t = 0; t < 2; ++t) {
+    if (!row_ok(t)) continue;  // uniform across the CTA
+    unsigned short* st_t = stb + t * STATE_FLOATS;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mbar[t * QUARTERS + 2 * pass]), 0) &&
+                                                  mbar_wait_bounded(smem_u32(&mbar[t * QUARTERS + 2 * pass + 1]), 0));
+      if (!ok) timed_out = true;
+      if (ok) {
+        float2 sv[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const int row = pass * 64 + (r >> 1) * 32 + (r & 1) * 16 + rbase;
+            const uint2 x = *reinterpret_cast<const uint2*>(st_t + row * HD + m * 64 + kl * 4);
+            sv[r][2 * m] = make_float2(bf_lo(x.x), bf_hi(x.x));
+            sv[r][2 * m + 1] = make_float2(bf_lo(x.y), bf_hi(x.y));
+          }
+        const int vq = pass * 64 + (rsel >> 1) * 32 + (rsel & 1) * 16 + rbase;
+        float2 kv[4], dk2[4], dq2[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) dk2[r] = dq2[r] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int k0 = t * HD + m * 64 + kl * 4;
+          const float4 e = *reinterpret_cast<const float4*>(eg + k0);
+          const float4 qv = *reinterpret_cast<const float4*>(qh + k0);
+          const float4 k4 = *reinterpret_cast<const float4*>(kh + k0);
+          const float2 e0 = make_float2(e.x, e.y), e1 = make_float2(e.z, e.w);
+          const float2 q0 = make_float2(qv.x, qv.y), q1 = make_float2(qv.z, qv.w);
+          kv[2 * m] = make_float2(k4.x, k4.y);
+          kv[2 * m + 1] = make_float2(k4.z, k4.w);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            sv[r][2 * m] = mul2(sv[r][2 * m], e0);
+            sv[r][2 * m + 1] = mul2(sv[r][2 * m + 1], e1);
+            dk2[r] = fma2(sv[r][2 * m], kv[2 * m], dk2[r]);
+            dk2[r] = fma2(sv[r][2 * m + 1], kv[2 * m + 1], dk2[r]);
+            dq2[r] = fma2(sv[r][2 * m], q0, dq2[r]);
+            dq2[r] = fma2(sv[r][2 * m + 1], q1, dq2[r]);
+          }
+        }
+        float v8[8];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          v8[r] = dk2[r].x + dk2[r].y;
+          v8[4 + r] = dq2[r].x + dq2[r].y;
+        }
+        float w4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float keep = b3 ? v8[4 + i] : v8[i], send = b3 ? v8[i] : v8[4 + i];
+          w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        float w2[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float keep = b2 ? w4[2 + i] : w4[i], send = b2 ? w4[i] : w4[2 + i];
+          w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        float rv = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
+        rv += __shfl_xor_sync(0xffffffffu, rv, 1);
+        const float bt = beta_s[t];
+        const float bu_own = bt * (bf(vv[t * HD + vq]) - rv);
+        const int src = lane & 16;
+        float bu[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) bu[r] = __shfl_sync(0xffffffffu, bu_own, src | (2 * r));
+        if (b3 && (kl & 1) == 0) {
+          const float bur = b2 ? (b1 ? bu[3] : bu[2]) : (b1 ? bu[1] : bu[0]);
+          ob[t * HD + vq] = __float2bfloat16_rn(fmaf(bur, kq_s[t], rv));
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int row = pass * 64 + (r >> 1) * 32 + (r & 1) * 16 + rbase;
+          const float2 bu2 = make_float2(bu[r], bu[r]);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            sv[r][2 * m] = fma2(bu2, kv[2 * m], sv[r][2 * m]);
+            sv[r][2 * m + 1] = fma2(bu2, kv[2 * m + 1], sv[r][2 * m + 1]);
+            const uint2 w = make_uint2(pack_bf16x2(sv[r][2 * m].x, sv[r][2 * m].y),
+                                       pack_bf16x2(sv[r][2 * m + 1].x, sv[r][2 * m + 1].y));
+            *reinterpret_cast<uint2*>(st_t + row * HD + m * 64 + kl * 4) = w;
+          }
+        }
+      }  // ok
+      // Every thread reaches this barrier, timed out or not; the quarters go out only
+      // when no warp of the CTA timed out.
+      fence_proxy_async();
+      if (timed_out && lane == 0) ctl[0] = 1;
+      __syncthreads();
+      if (tid == 0 && ctl[0] == 0) {
+        unsigned char* gdst = static_cast<unsigned char*>(a.state_pool) + ((long long)slot_s[t] * a.heads + h) * SB::BYTES;
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const int q = 2 * pass + qq;
+          bulk_store(gdst + q * SB::QBYTES, smem_u32(reinterpret_cast<unsigned char*>(st_t) + q * SB::QBYTES), SB::QBYTES);
+        }
+        bulk_commit();
+      }
+    }
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const float4 onw = *reinterpret_cast<const float4*>(a.o_norm + lane * 4);
+  if (timed_out && lane == 0) {
+    ctl[0] = 1;
+    atomicOr(a.err, KDA_ERR_TIMEOUT);
+  }
+  __syncthreads();
+  if (ctl[0] != 0) {
+    if (tid == 0) {
+      for (int q = 0; q < 2 * QUARTERS; ++q)
+        if (row_ok(q / QUARTERS)) (void)mbar_wait_bounded(smem_u32(&mbar[q]), 0);
+      bulk_wait_read();
+    }
+    return;
+  }
+  // ---- gated RMSNorm: warp t on row t ---------------------------------------------------
+  if (warp < 2 && row_ok(warp)) {
+    const int t = warp;
+    float o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = bf(ob[t * HD + lane * 4 + e]);
+    const float ss = warp_sum(o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3]);
+    const float rstd = rsqrtf(ss * (1.0f / HD) + a.eps);
+    const float wn[4] = {onw.x, onw.y, onw.z, onw.w};
+    __align__(8) __nv_bfloat16 y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      y[e] = __float2bfloat16_rn(o[e] * rstd * wn[e] * __half2float(gsig_s[t * HD + lane * 4 + e]));
+    *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
+  }
+  if (tid == 0) bulk_wait_read();  // shared memory stays until the bulk stores have read it
+}
+
 // [3D, 1, W] -> [3D] of 4 taps right-aligned (zeros in front when W < 4),
 // two bf16 a word: one 8-byte load gives a channel all its taps (the
 // PreparedKda page re-lays the weight out once, in decode_conv_weight).
@@ -1152,6 +1541,11 @@ cudaError_t set_smem_attr() {
 
 cudaError_t set_all_smem_attrs() {
   cudaError_t e = cudaSuccess;
+  const cudaError_t d[2] = {
+      cudaFuncSetAttribute(kda_decode_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemPair::bytes),
+      cudaFuncSetAttribute(kda_decode_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemPair::bytes)};
+  for (cudaError_t x : d)
+    if (x != cudaSuccess) e = x;
   cudaError_t r[KDA_MAX_TOKENS] = {set_smem_attr<1>(), set_smem_attr<2>(), set_smem_attr<3>(), set_smem_attr<4>(),
                                    set_smem_attr<5>(), set_smem_attr<6>(), set_smem_attr<7>(), set_smem_attr<8>()};
   for (int i = 0; i < KDA_MAX_TOKENS; ++i)
@@ -1192,6 +1586,25 @@ cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream, bool 
   else
     e = bf16_state ? cudaLaunchKernelEx(&cfg, kda_step_kernel<L, true, false, 1>, a)
                    : cudaLaunchKernelEx(&cfg, kda_step_kernel<L, false, false, 1>, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Decode with a bf16 state pool: two rows of one head a CTA.
+cudaError_t launch_decode_pair(const StepArgs& a, long long rows, cudaStream_t stream, bool pdl) {
+  const long long ctas = (rows + 1) / 2 * a.heads;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SmemPair::bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the previous kernel ends
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = a.conv_dim_first ? cudaLaunchKernelEx(&cfg, kda_decode_pair_kernel<true>, a, (int)rows)
+                                         : cudaLaunchKernelEx(&cfg, kda_decode_pair_kernel<false>, a, (int)rows);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -1359,6 +1772,10 @@ int step_enqueue(kda_handle* h, const void* projected, long long rows, long long
   if (!a.conv_dim_first) vs = 1;  // the split is built for the window-first conv layout
   if (vs * ctas > 0x7fffffffLL) return KDA_EINVAL;
   cudaError_t e;
+  if (L == 1 && bs && vs == 1 && rows >= 2) {  // bf16 pool decode: two rows a CTA
+    e = launch_decode_pair(a, rows, s, pdl);
+    return e == cudaSuccess ? KDA_OK : KDA_ECUDA;
+  }
   switch (L) {
     case 1: e = launch<1>(a, ctas, s, bs, pdl, vs); break;
     case 2: e = launch<2>(a, ctas, s, bs, pdl, vs); break;

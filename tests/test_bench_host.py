@@ -114,3 +114,15 @@ def test_committed_traffic_matches_the_kernel_source():
     # the committed captures were taken on the kernel as it stands
     assert bench.measured_traffic("large_decode") is not None
     assert bench.measured_traffic("large_decode", "bf16") is not None
+
+
+def test_roofline_names_the_kernel_that_runs():
+    # decode of two rows or more with a bf16 pool runs two rows of one head a CTA
+    W = I.WORKLOADS
+    assert bench.step_kernel_name(W["large_decode"], "bf16") == "kda_decode_pair_kernel"
+    assert bench.step_kernel_name(W["batched_decode"], "bf16") == "kda_decode_pair_kernel"
+    assert bench.step_kernel_name(W["tiny_decode"], "bf16") == "kda_step_kernel"  # one row
+    assert bench.step_kernel_name(W["large_decode"], "bf16", 2) == "kda_step_kernel"  # two CTAs a head
+    for name in ("large_decode", "spec_verify", "full_width_verify"):
+        assert bench.step_kernel_name(W[name], "f32") == "kda_step_kernel"
+    assert bench.step_kernel_name(W["spec_verify"], "bf16") == "kda_step_kernel"
