@@ -97,14 +97,18 @@ def test_layer_plan_equals_the_three_calls(w):
     ds.close()
 
 
-@pytest.mark.parametrize("variant", ["bf16_state", "softplus_gate", "conv_transposed"])
+@pytest.mark.parametrize("variant", ["bf16_state", "bf16_state_decode", "softplus_gate", "conv_transposed"])
 def test_layer_plan_variants(variant):
-    # the layer graph on the core's variants (bf16 state pool, the second gate form, the
+    # the layer graph on the core's variants (bf16 state pool -- for decode the two-row
+    # kernel, an odd row count leaving its last CTA one row --, the second gate form, the
     # [pool, W-1, 3D] conv layout), PDL on both edges, against the three separate calls
-    w = I.Workload("verify_24_rows_v", heads=2, requests=6, L=4, pool=32, verify=True, seed=2124)
+    if variant == "bf16_state_decode":
+        w = I.Workload("decode_9_rows_v", heads=2, requests=9, L=1, pool=16, verify=False, seed=2125)
+    else:
+        w = I.Workload("verify_24_rows_v", heads=2, requests=6, L=4, pool=32, verify=True, seed=2124)
     si = I.make_step_inputs(w)
-    kw = {"bf16_state": dict(state_dtype="bf16"), "softplus_gate": dict(gate_mode=1),
-          "conv_transposed": dict(dim_first=False)}[variant]
+    kw = {"bf16_state": dict(state_dtype="bf16"), "bf16_state_decode": dict(state_dtype="bf16"),
+          "softplus_gate": dict(gate_mode=1), "conv_transposed": dict(dim_first=False)}[variant]
     ds = G.DeviceStep(si, **kw)
     conv0, state0 = ds.conv.clone(), ds.state.clone()
     gen = torch.Generator().manual_seed(w.seed)

@@ -68,6 +68,38 @@ def test_plan_replays_match_oracle(L, v_split):
     ds.close()
 
 
+def test_bf16_decode_plan_replays_match_oracle():
+    # bf16 state pool, decode: the recorded launch is the two-row kernel (five rows, so its
+    # last CTA serves one).  Each launch is compared with the oracle applied to the caches
+    # the GPU held before it: two bf16 pools rounded from fp32 and fp64 may drift by more
+    # than one step when each is chained on its own.
+    si = case(heads=2, requests=5, L=1, pool=9, seed=187)
+    W = oracle.Weights(**si.weights.as_dict())
+    ds = G.DeviceStep(si, state_dtype="bf16")
+    plan = ds.prep.plan(ds.projected, ds.out, caches=(ds.conv, ds.state), slots=ds.slots, accepted=None)
+    proj = si.projected.copy()
+    rng = np.random.default_rng(187)
+    written = np.unique(si.slots)
+    rest = np.setdiff1d(np.arange(si.workload.pool), written)
+    for launch in range(3):
+        if launch == 2:  # new inputs into the plan's buffer
+            proj = I.to_bf16_bits(rng.normal(0.0, 1.0, size=proj.shape).astype(np.float32))
+            ds.projected.copy_(G.bf16_np_to_torch(proj, ds.device))
+        conv_in, pool_in = G.torch_bf16_to_np(ds.conv), G.torch_bf16_to_np(ds.state)
+        plan.launch()
+        assert ds.prep.check() == 0
+        out_ref, conv_ref, pool_ref, err = oracle.step(W, proj, conv_in, pool_in, si.slots, 1, None,
+                                                       state_dtype="bf16")
+        assert err == 0
+        G.assert_out_close(G.torch_bf16_to_np(ds.out), out_ref)
+        assert np.array_equal(G.torch_bf16_to_np(ds.conv), conv_ref)
+        st = G.torch_bf16_to_np(ds.state)
+        G.assert_state_close_bf16(st[written], pool_ref[written])
+        assert np.array_equal(st[rest], pool_ref[rest])
+    plan.close()
+    ds.close()
+
+
 def _linear_close(y_bits, x_bits, w_bits):
     """kda_linear's criterion: one bf16 step of the correctly rounded product
     plus the fp32 accumulation's share, 2^-14 sum |x_k w_k|."""
