@@ -169,8 +169,11 @@ int kda_set_gate_mode(kda_handle* handle, int mode);
  *                             each stored state to bf16 (nearest even); half
  *                             the state bytes, at bf16 precision of the cache
  * For KDA_STATE_BF16 pass the bf16 pool as kda_step's state_pool (same
- * 16-byte alignment rule).  Applies to steps enqueued (and plans made) after
- * the call.  Returns KDA_OK, or KDA_EINVAL for a NULL handle or an unknown
+ * 16-byte alignment rule).  A bf16-pool decode of two rows or more runs rows
+ * 2p and 2p + 1 of a head in one CTA (their two 32 KiB states take the shared
+ * memory of one fp32 state, and they share their load round trips); each row's
+ * results are those of one row a CTA.  Applies to steps enqueued (and plans
+ * made) after the call.  Returns KDA_OK, or KDA_EINVAL for a NULL handle or an unknown
  * type.  No CUDA call.
  */
 #define KDA_STATE_F32 0
@@ -188,9 +191,10 @@ int kda_set_state_dtype(kda_handle* handle, int dtype);
  * workload measured (the halves repeat the prologue, and the doubled grid of
  * three-per-SM CTAs needs more waves), so it is off unless asked for.  It
  * applies to the window-first conv layout (conv_dim_first = 1); the other
- * layout always runs one CTA.  Results are the same either way.  Applies to
- * steps enqueued (and plans made) after the call.  Returns KDA_OK, or
- * KDA_EINVAL for a NULL handle or another value.  No CUDA call.
+ * layout always runs one CTA.  With a bf16 pool, decode under v_split 2 runs
+ * one row a cluster instead of two rows a CTA.  Results are the same either
+ * way.  Applies to steps enqueued (and plans made) after the call.  Returns
+ * KDA_OK, or KDA_EINVAL for a NULL handle or another value.  No CUDA call.
  */
 int kda_set_v_split(kda_handle* handle, int v_split);
 
