@@ -72,16 +72,14 @@ typedef struct kda_handle kda_handle;
 #define KDA_ERR_DUPLICATE 8u /* KDA_DEBUG builds only: two rows of the step write the same slot    */
 
 /* KDA_ERR_TIMEOUT: the step reads a (request, head)'s start state in two
- * halves of 64 v rows (one wait each) and finishes each half over all L tokens
- * before it waits for the next.  If the first wait gives up, no state row of
- * that (request, head) is written; if the second does, rows 0..63 of the
- * states may already be in every slots[r, t] (decode: in slots[b]) while rows
- * 64..127 are not.  Either way its out rows are not written, and the conv
- * windows (stored before the state is needed) are.  Decode of two rows or
- * more with a bf16 state pool serves rows 2p and 2p + 1 of a head in one CTA:
- * a wait that gives up on either row leaves both rows' out unwritten, while the
- * other row's state may already be stored.  Treat the requests' caches as
- * undefined after a timeout. */
+ * halves of 64 v rows, each warp waiting (about 1 s at most) for the half it
+ * needs.  A warp that gives up writes none of its state rows; the warps whose
+ * copies landed may already have written theirs to slots[r, t] (decode:
+ * slots[b]).  The out rows of a CTA that saw a wait give up are not written
+ * (decode of two rows or more with a bf16 state pool serves rows 2p and 2p + 1
+ * of a head in one CTA, so both rows' out stay unwritten), and the conv
+ * windows, stored before the state is needed, are.  Treat the requests' caches
+ * as undefined after a timeout. */
 
 /* Maximum verify tokens per request. */
 #define KDA_MAX_TOKENS 8

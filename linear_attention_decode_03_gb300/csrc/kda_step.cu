@@ -32,17 +32,18 @@
 //       (rows = v; each pass waits on its two copies); 16 lanes own a v row,
 //       8 k values a lane, four rows a thread in registers across the L
 //       tokens; S'^T k^ and S'^T q^ are reduced with one 16-lane
-//       reduce-scatter; decode writes the rows back to shared memory and sends
-//       each quarter with a TMA bulk store, verify sends every token's rows to
-//       slots[r, t] with 128-bit stores.
+//       reduce-scatter; every token's new rows leave straight from registers
+//       for slots[r, t] (decode: slots[b]) as streaming stores, 128-bit for
+//       fp32 and 64-bit for bf16 (a shared-memory write-back and bulk store
+//       needed a barrier a pass and measured no faster).
 //   * gated RMSNorm, warp t on token t -> bf16 core_out.
 // As an option (kda_set_v_split) a (request, head) runs as a cluster of two
 // CTAs, each with 64 of the v rows (one recurrence pass) and half the outputs,
 // the halves of o swapped through distributed shared memory for the norm.
 // Decode of two rows or more with a bf16 state pool runs rows 2p and 2p + 1 of
 // one head in one CTA (kda_decode_pair_kernel): the rows share the load round
-// trips and the head's f_b, and their two 32 KiB states fill the shared memory
-// that one fp32 state takes.
+// trips and the head's f_b, their two 32 KiB states fill the shared memory that
+// one fp32 state takes, and the new states leave with streaming stores.
 // The bf16 hand-offs (conv outputs, z) are rounded correctly: each fp32 value
 // carries a bound on its error and is recomputed exactly (fp64, or a
 // compensated TwoSum sum) when the bound straddles a bf16 rounding boundary.
@@ -178,18 +179,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, unsigne
       : "memory");
 }
 
-// Bulk async shared -> global copy (one bulk group per call site commit).
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, unsigned bytes) {
-  unsigned long long policy;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
-               "r"(src), "r"(bytes), "l"(policy)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every committed bulk store has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void store_streaming_u2(void* p, uint2 v) {
   asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
@@ -1000,13 +989,7 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
           const float4 row4 = make_float4(sv[r][2 * m].x, sv[r][2 * m].y, sv[r][2 * m + 1].x, sv[r][2 * m + 1].y);
           if constexpr (BS) {  // rounded to bf16 (nearest even) as it is stored
             const uint2 w = make_uint2(pack_bf16x2(row4.x, row4.y), pack_bf16x2(row4.z, row4.w));
-            if constexpr (L == 1)
-              *reinterpret_cast<uint2*>(stb + row * HD + m * 64 + kl * 4) = w;
-            else
-              store_streaming_u2(dst + (row * HD + m * 64) * 2, w);
-          } else if constexpr (L == 1) {
-            // decode: back into the shared-memory state; TMA stores the quarter
-            *reinterpret_cast<float4*>(st + row * HD + m * 64 + kl * 4) = row4;
+            store_streaming_u2(dst + (row * HD + m * 64) * 2, w);
           } else {
             store_streaming(reinterpret_cast<float*>(dst + (row * HD + m * 64) * 4), row4);
           }
@@ -1014,22 +997,6 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
       }
     }
     }  // ok
-    if constexpr (L == 1) {
-      // Every thread reaches this barrier, timed out or not; the quarters go out
-      // only when no warp of the CTA timed out.
-      fence_proxy_async();  // this thread's shared-memory writes -> async proxy
-      if (timed_out && lane == 0) ctl[0] = 1;
-      __syncthreads();
-      if (tid == 0 && ctl[0] == 0) {
-        unsigned char* gdst = static_cast<unsigned char*>(a.state_pool) + ((long long)slot_s[0] * a.heads + h) * SB::BYTES;
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const int q = 2 * pass + qq;
-          bulk_store(gdst + q * SB::QBYTES, smem_u32(stc + q * SB::QBYTES), SB::QBYTES);
-        }
-        bulk_commit();
-      }
-    }
   }
   // a dependent launch (the o_proj of a layer plan) may start its CTAs now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1062,7 +1029,6 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     // shared memory is released; the outputs of this request stay unwritten.
     if (tid == 0) {
       for (int q = Q0; q < Q0 + QUARTERS / VS; ++q) (void)mbar_wait_bounded(smem_u32(&mbar[q]), 0);
-      if constexpr (L == 1) bulk_wait_read();
     }
     return;
   }
@@ -1084,9 +1050,6 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
     if (VS == 1 || (unsigned)(lane >> 4) == slice)  // VS = 2: this CTA's 64 columns
       *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
   }
-  if constexpr (L == 1) {
-    if (tid == 0) bulk_wait_read();  // shared memory stays until the bulk stores have read it
-  }
 }
 
 // ---- decode with a bf16 state pool: two rows of one head a CTA --------------------
@@ -1098,7 +1061,11 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
 // arithmetic of a row is the one-row kernel's: thread half t runs row t's conv
 // (q, k and v of its channel), z takes the two rows as a verify takes two tokens,
 // warp t runs row t's norms, and each row's state goes through two passes of
-// its own.
+// its own. The new state rows leave straight from registers as 8-byte streaming
+// stores, as in the one-row kernel: with four passes a CTA, the barrier a pass
+// that a shared-memory write-back and bulk store need cost more than the
+// stores save (two rows a CTA, large decode: 79.6 us with bulk stores, 73.4
+// without).
 struct SmemPair {
   static constexpr int state = 0;                              // bf16 [2][128][128]
   static constexpr int eg = state + 2 * StateT<true>::BYTES;   // float [2][128]
@@ -1341,6 +1308,7 @@ __global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepA
   for (int t = 0; t < 2; ++t) {
     if (!row_ok(t)) continue;  // uniform across the CTA
     unsigned short* st_t = stb + t * STATE_FLOATS;
+    unsigned char* gdst_t = static_cast<unsigned char*>(a.state_pool) + ((long long)(t == 0 ? sl0 : sl1) * a.heads + h) * SB::BYTES;
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mbar[t * QUARTERS + 2 * pass]), 0) &&
@@ -1421,24 +1389,10 @@ __global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepA
             sv[r][2 * m + 1] = fma2(bu2, kv[2 * m + 1], sv[r][2 * m + 1]);
             const uint2 w = make_uint2(pack_bf16x2(sv[r][2 * m].x, sv[r][2 * m].y),
                                        pack_bf16x2(sv[r][2 * m + 1].x, sv[r][2 * m + 1].y));
-            *reinterpret_cast<uint2*>(st_t + row * HD + m * 64 + kl * 4) = w;
+            store_streaming_u2(gdst_t + ((long long)row * HD + m * 64 + kl * 4) * 2, w);
           }
         }
       }  // ok
-      // Every thread reaches this barrier, timed out or not; the quarters go out only
-      // when no warp of the CTA timed out.
-      fence_proxy_async();
-      if (timed_out && lane == 0) ctl[0] = 1;
-      __syncthreads();
-      if (tid == 0 && ctl[0] == 0) {
-        unsigned char* gdst = static_cast<unsigned char*>(a.state_pool) + ((long long)slot_s[t] * a.heads + h) * SB::BYTES;
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const int q = 2 * pass + qq;
-          bulk_store(gdst + q * SB::QBYTES, smem_u32(reinterpret_cast<unsigned char*>(st_t) + q * SB::QBYTES), SB::QBYTES);
-        }
-        bulk_commit();
-      }
     }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1452,7 +1406,6 @@ __global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepA
     if (tid == 0) {
       for (int q = 0; q < 2 * QUARTERS; ++q)
         if (row_ok(q / QUARTERS)) (void)mbar_wait_bounded(smem_u32(&mbar[q]), 0);
-      bulk_wait_read();
     }
     return;
   }
@@ -1471,7 +1424,6 @@ __global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepA
       y[e] = __float2bfloat16_rn(o[e] * rstd * wn[e] * __half2float(gsig_s[t * HD + lane * 4 + e]));
     *reinterpret_cast<uint2*>(a.out + (row0 + t) * D + h * HD + lane * 4) = *reinterpret_cast<uint2*>(y);
   }
-  if (tid == 0) bulk_wait_read();  // shared memory stays until the bulk stores have read it
 }
 
 // [3D, 1, W] -> [3D] of 4 taps right-aligned (zeros in front when W < 4),
