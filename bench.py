@@ -79,8 +79,8 @@ def traffic_key(workload: str, state_dtype: str = "f32", v_split: int = 1):
 
 def step_kernel_name(w: I.Workload, state_dtype: str = "f32", v_split: int = 1) -> str:
     """The kernel kda_step launches for this workload: decode of two rows or more
-    with a bf16 state pool runs two rows of one head a CTA."""
-    if not w.verify and w.L == 1 and state_dtype == "bf16" and v_split == 1 and w.rows >= 2:
+    runs two rows of one head a CTA."""
+    if not w.verify and w.L == 1 and v_split == 1 and w.rows >= 2:
         return "kda_decode_pair_kernel"
     return "kda_step_kernel"
 

@@ -76,10 +76,17 @@ typedef struct kda_handle kda_handle;
  * needs.  A warp that gives up writes none of its state rows; the warps whose
  * copies landed may already have written theirs to slots[r, t] (decode:
  * slots[b]).  The out rows of a CTA that saw a wait give up are not written
- * (decode of two rows or more with a bf16 state pool serves rows 2p and 2p + 1
- * of a head in one CTA, so both rows' out stay unwritten), and the conv
+ * (decode of two rows or more serves rows 2p and 2p + 1 of a head in one CTA,
+ * so both rows' out stay unwritten), and the conv
  * windows, stored before the state is needed, are.  Treat the requests' caches
  * as undefined after a timeout. */
+
+/* Decode of two rows or more (L = 1, rows >= 2, one CTA a (request, head))
+ * runs rows 2p and 2p + 1 of a head in one CTA: the rows share their load
+ * round trips and the head's f_b; with a bf16 pool their two 32 KiB states sit
+ * side by side, with an fp32 pool the second row's halves are loaded into the
+ * one 64 KiB state buffer as the first row's passes free them.  Each row's
+ * results are those of one row a CTA. */
 
 /* Maximum verify tokens per request. */
 #define KDA_MAX_TOKENS 8
@@ -167,10 +174,7 @@ int kda_set_gate_mode(kda_handle* handle, int mode);
  *                             each stored state to bf16 (nearest even); half
  *                             the state bytes, at bf16 precision of the cache
  * For KDA_STATE_BF16 pass the bf16 pool as kda_step's state_pool (same
- * 16-byte alignment rule).  A bf16-pool decode of two rows or more runs rows
- * 2p and 2p + 1 of a head in one CTA (their two 32 KiB states take the shared
- * memory of one fp32 state, and they share their load round trips); each row's
- * results are those of one row a CTA.  Applies to steps enqueued (and plans
+ * 16-byte alignment rule).  Applies to steps enqueued (and plans
  * made) after the call.  Returns KDA_OK, or KDA_EINVAL for a NULL handle or an unknown
  * type.  No CUDA call.
  */
@@ -189,8 +193,8 @@ int kda_set_state_dtype(kda_handle* handle, int dtype);
  * workload measured (the halves repeat the prologue, and the doubled grid of
  * three-per-SM CTAs needs more waves), so it is off unless asked for.  It
  * applies to the window-first conv layout (conv_dim_first = 1); the other
- * layout always runs one CTA.  With a bf16 pool, decode under v_split 2 runs
- * one row a cluster instead of two rows a CTA.  Results are the same either
+ * layout always runs one CTA.  Decode under v_split 2 runs one row a cluster
+ * instead of two rows a CTA.  Results are the same either
  * way.  Applies to steps enqueued (and plans made) after the call.  Returns
  * KDA_OK, or KDA_EINVAL for a NULL handle or another value.  No CUDA call.
  */
@@ -281,7 +285,10 @@ const char* kda_strerror(int code);
  * kda_launch_info -- the launch shape kda_step uses for L tokens (one CTA per
  * (request, head), fp32 state pool, window-first conv cache): threads per
  * CTA, dynamic shared memory bytes per CTA and the resident CTAs per SM the
- * occupancy calculator reports (each output pointer may be NULL).  Returns
+ * occupancy calculator reports (each output pointer may be NULL).  A decode of
+ * two rows or more runs two rows of one head a CTA in a second kernel with the
+ * same threads and residency and a little more shared memory (the second row's
+ * norms and gates); L = 1 reports the one-row kernel.  Returns
  * KDA_OK, KDA_EINVAL (L outside 1..KDA_MAX_TOKENS) or KDA_ECUDA.  Needs a
  * current CUDA device when ctas_per_sm is not NULL.
  */

@@ -40,10 +40,11 @@
 // As an option (kda_set_v_split) a (request, head) runs as a cluster of two
 // CTAs, each with 64 of the v rows (one recurrence pass) and half the outputs,
 // the halves of o swapped through distributed shared memory for the norm.
-// Decode of two rows or more with a bf16 state pool runs rows 2p and 2p + 1 of
-// one head in one CTA (kda_decode_pair_kernel): the rows share the load round
-// trips and the head's f_b, their two 32 KiB states fill the shared memory that
-// one fp32 state takes, and the new states leave with streaming stores.
+// Decode of two rows or more runs rows 2p and 2p + 1 of one head in one CTA
+// (kda_decode_pair_kernel): the rows share the load round trips and the head's
+// f_b; two bf16 states sit side by side in the shared memory one fp32 state
+// takes, and with an fp32 pool the second row's halves follow the first row's
+// passes into the one state buffer.
 // The bf16 hand-offs (conv outputs, z) are rounded correctly: each fp32 value
 // carries a bound on its error and is recomputed exactly (fp64, or a
 // compensated TwoSum sum) when the bound straddles a bf16 rounding boundary.
@@ -1052,23 +1053,28 @@ __global__ void __launch_bounds__(THREADS, (L <= 4 ? 3 : 2)) kda_step_kernel(con
   }
 }
 
-// ---- decode with a bf16 state pool: two rows of one head a CTA --------------------
-// With half the state bytes, a one-row CTA spends most of its life on its two
-// dependent load round trips (the slot, then the window and state it
-// addresses). A CTA that serves rows 2p and 2p + 1 of head h shares those round
-// trips and the head's f_b between the rows, and holds the two 32 KiB states in
-// the shared memory one fp32 state takes (three CTAs an SM as before). The
-// arithmetic of a row is the one-row kernel's: thread half t runs row t's conv
-// (q, k and v of its channel), z takes the two rows as a verify takes two tokens,
-// warp t runs row t's norms, and each row's state goes through two passes of
-// its own. The new state rows leave straight from registers as 8-byte streaming
-// stores, as in the one-row kernel: with four passes a CTA, the barrier a pass
-// that a shared-memory write-back and bulk store need cost more than the
-// stores save (two rows a CTA, large decode: 79.6 us with bulk stores, 73.4
-// without).
+// ---- decode: two rows of one head a CTA -----------------------------------------------
+// A one-row CTA spends much of its life on its two dependent load round trips
+// (the slot, then the window and state it addresses). A CTA that serves rows 2p
+// and 2p + 1 of head h shares those round trips and the head's f_b between the
+// rows. With a bf16 pool the two 32 KiB states take the shared memory one fp32
+// state takes; with an fp32 pool the second row's state halves are loaded into
+// the one 64 KiB buffer as each of the first row's passes has taken its half
+// into registers (a barrier a pass of the first row), so the second row's copies
+// run under the first row's work. Three CTAs an SM either way. The arithmetic of
+// a row is the one-row kernel's: thread half t runs row t's conv (q, k and v of
+// its channel), z takes the two rows as a verify takes two tokens, warp t runs
+// row t's norms, and each row's state goes through two passes of its own. The
+// new state rows leave straight from registers as streaming stores, as in the
+// one-row kernel: with four passes a CTA, the barrier a pass that a shared-memory
+// write-back and bulk store need cost more than the stores save (bf16 pool, large
+// decode: 79.6 us with bulk stores, 73.4 without).
+template <bool BS>
 struct SmemPair {
-  static constexpr int state = 0;                              // bf16 [2][128][128]
-  static constexpr int eg = state + 2 * StateT<true>::BYTES;   // float [2][128]
+  // bf16: one [128][128] state a row; fp32: one [128][128] state, the second row's
+  // halves loaded into it as the first row's passes free them
+  static constexpr int state = 0;
+  static constexpr int eg = state + (BS ? 2 * StateT<true>::BYTES : StateT<false>::BYTES);  // float [2][128]
   static constexpr int kh = eg + 2 * HD * 4;                   // float [2][128]   k, then k^
   static constexpr int qh = kh + 2 * HD * 4;                   // float [2][128]   q, then q^
   static constexpr int fa = qh + 2 * HD * 4;                   // bf16  [2][128]   f_a; later o
@@ -1083,12 +1089,13 @@ struct SmemPair {
   static constexpr int bytes = mbar + 8 * 2 * QUARTERS;
 };
 
-template <bool DF>
+template <bool BS, bool DF>
 __global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepArgs a, int rows) {
   extern __shared__ __align__(128) unsigned char smem[];
-  using S = SmemPair;
-  using SB = StateT<true>;
+  using S = SmemPair<BS>;
+  using SB = StateT<BS>;
   unsigned short* stb = reinterpret_cast<unsigned short*>(smem + S::state);
+  float* st = reinterpret_cast<float*>(smem + S::state);
   float* eg = reinterpret_cast<float*>(smem + S::eg);
   float* kh = reinterpret_cast<float*>(smem + S::kh);
   float* qh = reinterpret_cast<float*>(smem + S::qh);
@@ -1182,21 +1189,29 @@ __global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepA
         if (j >= 0) xin[kind][i] = win[(long long)kind * D * CHS + j * JS];
       }
   }
+  // Row t's quarter q goes into buffer `buf` (bf16: the row's own; fp32: the one buffer)
+  // on mbarrier t * 4 + q; thread 0 keeps the mask of the barriers it armed.
+  unsigned armed = 0;
+  auto issue_quarter = [&](int t, int q, int buf) {
+    const unsigned char* src = static_cast<const unsigned char*>(a.state_pool) +
+                               ((long long)(t == 0 ? sl0 : sl1) * a.heads + h) * SB::BYTES;
+    const uint32_t bar = smem_u32(&mbar[t * QUARTERS + q]);
+    mbar_expect_tx(bar, SB::QBYTES);
+    bulk_load(smem_u32(smem + S::state + buf * SB::BYTES + q * SB::QBYTES), src + q * SB::QBYTES, SB::QBYTES, bar);
+    if constexpr (!BS) armed |= 1u << (t * QUARTERS + q);  // bf16: every good row's copies go out at once
+  };
+  // fp32: the second row's halves follow the first row's passes, unless the first row
+  // has none (padding or a bad slot), in which case they go out now
+  const bool row1_later = !BS && row_ok(0) && row_ok(1);
   if (tid == 0) {
 #pragma unroll
     for (int q = 0; q < 2 * QUARTERS; ++q) mbar_init(smem_u32(&mbar[q]), 1);
     fence_mbar_init();
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      if (status[t] != TASK_OK) continue;
-      const unsigned char* src = static_cast<const unsigned char*>(a.state_pool) + ((long long)sl[t] * a.heads + h) * SB::BYTES;
+      if (!row_ok(t) || (t == 1 && row1_later)) continue;
 #pragma unroll
-      for (int q = 0; q < QUARTERS; ++q) {
-        const uint32_t bar = smem_u32(&mbar[t * QUARTERS + q]);
-        mbar_expect_tx(bar, SB::QBYTES);
-        bulk_load(smem_u32(reinterpret_cast<unsigned char*>(stb) + t * SB::BYTES + q * SB::QBYTES), src + q * SB::QBYTES,
-                  SB::QBYTES, bar);
-      }
+      for (int q = 0; q < QUARTERS; ++q) issue_quarter(t, q, BS ? t : 0);
     }
     ctl[0] = 0;
   }
@@ -1304,27 +1319,20 @@ __global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepA
   const bool b3 = (kl & 8) != 0, b2 = (kl & 4) != 0, b1 = (kl & 2) != 0;
   const int rsel = (b2 ? 2 : 0) + (b1 ? 1 : 0);
   bool timed_out = false;
+  bool row1_live = true;  // fp32: the first row's passes put the second row's halves in flight
 #pragma unroll 1
   for (int t = 0; t < 2; ++t) {
-    if (!row_ok(t)) continue;  // uniform across the CTA
-    unsigned short* st_t = stb + t * STATE_FLOATS;
+    if (!row_ok(t) || (t == 1 && !row1_live)) continue;  // uniform across the CTA
+    unsigned short* st_t = stb + (BS ? t : 0) * STATE_FLOATS;
+    float* stf = st;
     unsigned char* gdst_t = static_cast<unsigned char*>(a.state_pool) + ((long long)(t == 0 ? sl0 : sl1) * a.heads + h) * SB::BYTES;
 #pragma unroll 1
     for (int pass = 0; pass < 2; ++pass) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&mbar[t * QUARTERS + 2 * pass]), 0) &&
                                                   mbar_wait_bounded(smem_u32(&mbar[t * QUARTERS + 2 * pass + 1]), 0));
       if (!ok) timed_out = true;
-      if (ok) {
-        float2 sv[4][4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            const int row = pass * 64 + (r >> 1) * 32 + (r & 1) * 16 + rbase;
-            const uint2 x = *reinterpret_cast<const uint2*>(st_t + row * HD + m * 64 + kl * 4);
-            sv[r][2 * m] = make_float2(bf_lo(x.x), bf_hi(x.x));
-            sv[r][2 * m + 1] = make_float2(bf_lo(x.y), bf_hi(x.y));
-          }
+      // the update of the pass's four rows from the state values in sv
+      auto update = [&](float2 (&sv)[4][4]) {
         const int vq = pass * 64 + (rsel >> 1) * 32 + (rsel & 1) * 16 + rbase;
         float2 kv[4], dk2[4], dq2[4];
 #pragma unroll
@@ -1387,12 +1395,59 @@ __global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepA
           for (int m = 0; m < 2; ++m) {
             sv[r][2 * m] = fma2(bu2, kv[2 * m], sv[r][2 * m]);
             sv[r][2 * m + 1] = fma2(bu2, kv[2 * m + 1], sv[r][2 * m + 1]);
-            const uint2 w = make_uint2(pack_bf16x2(sv[r][2 * m].x, sv[r][2 * m].y),
-                                       pack_bf16x2(sv[r][2 * m + 1].x, sv[r][2 * m + 1].y));
-            store_streaming_u2(gdst_t + ((long long)row * HD + m * 64 + kl * 4) * 2, w);
+            if constexpr (BS) {
+              const uint2 w = make_uint2(pack_bf16x2(sv[r][2 * m].x, sv[r][2 * m].y),
+                                         pack_bf16x2(sv[r][2 * m + 1].x, sv[r][2 * m + 1].y));
+              store_streaming_u2(gdst_t + ((long long)row * HD + m * 64 + kl * 4) * 2, w);
+            } else {
+              store_streaming(reinterpret_cast<float*>(gdst_t + ((long long)row * HD + m * 64 + kl * 4) * 4),
+                              make_float4(sv[r][2 * m].x, sv[r][2 * m].y, sv[r][2 * m + 1].x, sv[r][2 * m + 1].y));
+            }
           }
         }
-      }  // ok
+      };
+      if constexpr (BS) {
+        if (ok) {
+          float2 sv[4][4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              const int row = pass * 64 + (r >> 1) * 32 + (r & 1) * 16 + rbase;
+              const uint2 x = *reinterpret_cast<const uint2*>(st_t + row * HD + m * 64 + kl * 4);
+              sv[r][2 * m] = make_float2(bf_lo(x.x), bf_hi(x.x));
+              sv[r][2 * m + 1] = make_float2(bf_lo(x.y), bf_hi(x.y));
+            }
+          update(sv);
+        }
+      } else {
+        float2 sv[4][4];
+        if (ok) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              const int row = pass * 64 + (r >> 1) * 32 + (r & 1) * 16 + rbase;
+              const float4 x = *reinterpret_cast<const float4*>(stf + row * HD + m * 64 + kl * 4);
+              sv[r][2 * m] = make_float2(x.x, x.y);
+              sv[r][2 * m + 1] = make_float2(x.z, x.w);
+            }
+        }
+        if (t == 0 && row1_later) {  // uniform: this half of the buffer is free once every warp holds its rows
+          if (!ok && lane == 0) ctl[0] = 1;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // these reads before the copy's writes
+          __syncthreads();
+          // ctl[0] only goes from 0 to 1, and after this barrier only a warp that has given up
+          // on a wait of the second row writes it: a warp that reads it late skips that row,
+          // which a timeout leaves undefined anyway, and no barrier depends on the choice
+          row1_live = ctl[0] == 0;
+          if (tid == 0 && row1_live) {
+            issue_quarter(1, 2 * pass, 0);
+            issue_quarter(1, 2 * pass + 1, 0);
+          }
+        }
+        if (ok) update(sv);
+      }
     }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1405,7 +1460,7 @@ __global__ void __launch_bounds__(THREADS, 3) kda_decode_pair_kernel(const StepA
   if (ctl[0] != 0) {
     if (tid == 0) {
       for (int q = 0; q < 2 * QUARTERS; ++q)
-        if (row_ok(q / QUARTERS)) (void)mbar_wait_bounded(smem_u32(&mbar[q]), 0);
+        if (BS ? row_ok(q / QUARTERS) : (armed & (1u << q)) != 0) (void)mbar_wait_bounded(smem_u32(&mbar[q]), 0);
     }
     return;
   }
@@ -1493,9 +1548,15 @@ cudaError_t set_smem_attr() {
 
 cudaError_t set_all_smem_attrs() {
   cudaError_t e = cudaSuccess;
-  const cudaError_t d[2] = {
-      cudaFuncSetAttribute(kda_decode_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemPair::bytes),
-      cudaFuncSetAttribute(kda_decode_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemPair::bytes)};
+  const cudaError_t d[4] = {
+      cudaFuncSetAttribute(kda_decode_pair_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SmemPair<true>::bytes),
+      cudaFuncSetAttribute(kda_decode_pair_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SmemPair<true>::bytes),
+      cudaFuncSetAttribute(kda_decode_pair_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SmemPair<false>::bytes),
+      cudaFuncSetAttribute(kda_decode_pair_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SmemPair<false>::bytes)};
   for (cudaError_t x : d)
     if (x != cudaSuccess) e = x;
   cudaError_t r[KDA_MAX_TOKENS] = {set_smem_attr<1>(), set_smem_attr<2>(), set_smem_attr<3>(), set_smem_attr<4>(),
@@ -1542,21 +1603,26 @@ cudaError_t launch(const StepArgs& a, long long ctas, cudaStream_t stream, bool 
 }
 
 // Decode with a bf16 state pool: two rows of one head a CTA.
-cudaError_t launch_decode_pair(const StepArgs& a, long long rows, cudaStream_t stream, bool pdl) {
+cudaError_t launch_decode_pair(const StepArgs& a, long long rows, cudaStream_t stream, bool pdl, bool bs) {
   const long long ctas = (rows + 1) / 2 * a.heads;
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SmemPair::bytes;
+  cfg.dynamicSmemBytes = bs ? SmemPair<true>::bytes : SmemPair<false>::bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start before the previous kernel ends
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  const cudaError_t e = a.conv_dim_first ? cudaLaunchKernelEx(&cfg, kda_decode_pair_kernel<true>, a, (int)rows)
-                                         : cudaLaunchKernelEx(&cfg, kda_decode_pair_kernel<false>, a, (int)rows);
+  cudaError_t e;
+  if (bs)
+    e = a.conv_dim_first ? cudaLaunchKernelEx(&cfg, kda_decode_pair_kernel<true, true>, a, (int)rows)
+                         : cudaLaunchKernelEx(&cfg, kda_decode_pair_kernel<true, false>, a, (int)rows);
+  else
+    e = a.conv_dim_first ? cudaLaunchKernelEx(&cfg, kda_decode_pair_kernel<false, true>, a, (int)rows)
+                         : cudaLaunchKernelEx(&cfg, kda_decode_pair_kernel<false, false>, a, (int)rows);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -1724,8 +1790,8 @@ int step_enqueue(kda_handle* h, const void* projected, long long rows, long long
   if (!a.conv_dim_first) vs = 1;  // the split is built for the window-first conv layout
   if (vs * ctas > 0x7fffffffLL) return KDA_EINVAL;
   cudaError_t e;
-  if (L == 1 && bs && vs == 1 && rows >= 2) {  // bf16 pool decode: two rows a CTA
-    e = launch_decode_pair(a, rows, s, pdl);
+  if (L == 1 && vs == 1 && rows >= 2) {  // decode: two rows a CTA
+    e = launch_decode_pair(a, rows, s, pdl, bs);
     return e == cudaSuccess ? KDA_OK : KDA_ECUDA;
   }
   switch (L) {

@@ -117,12 +117,12 @@ def test_committed_traffic_matches_the_kernel_source():
 
 
 def test_roofline_names_the_kernel_that_runs():
-    # decode of two rows or more with a bf16 pool runs two rows of one head a CTA
+    # decode of two rows or more runs two rows of one head a CTA, whatever the pool type
     W = I.WORKLOADS
-    assert bench.step_kernel_name(W["large_decode"], "bf16") == "kda_decode_pair_kernel"
-    assert bench.step_kernel_name(W["batched_decode"], "bf16") == "kda_decode_pair_kernel"
-    assert bench.step_kernel_name(W["tiny_decode"], "bf16") == "kda_step_kernel"  # one row
-    assert bench.step_kernel_name(W["large_decode"], "bf16", 2) == "kda_step_kernel"  # two CTAs a head
-    for name in ("large_decode", "spec_verify", "full_width_verify"):
-        assert bench.step_kernel_name(W[name], "f32") == "kda_step_kernel"
-    assert bench.step_kernel_name(W["spec_verify"], "bf16") == "kda_step_kernel"
+    for sd in ("f32", "bf16"):
+        assert bench.step_kernel_name(W["large_decode"], sd) == "kda_decode_pair_kernel"
+        assert bench.step_kernel_name(W["batched_decode"], sd) == "kda_decode_pair_kernel"
+        assert bench.step_kernel_name(W["tiny_decode"], sd) == "kda_step_kernel"  # one row
+        assert bench.step_kernel_name(W["large_decode"], sd, 2) == "kda_step_kernel"  # two CTAs a head
+        assert bench.step_kernel_name(W["spec_verify"], sd) == "kda_step_kernel"
+        assert bench.step_kernel_name(W["full_width_verify"], sd) == "kda_step_kernel"
